@@ -1,0 +1,386 @@
+"""Benchmark: draft + schedule + verify cycles on synthetic inputs, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full cycle (ds_draft_block, ds_confidence_schedule, ds_verify) over
+one batch of the workload with inputs resident in HBM. The metric is drafted
+block tokens per second, B*K / t_cycle, summed over replicas. Multi-GPU runs are
+independent replicas (one process per GPU, no collective on the data path).
+`--impl reference` times the float64 CPU oracle on a bounded sample instead.
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft+verify tokens/s at B=128,K=16,V=151936; % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "B128_K16_V151936"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---- clocks (read-only NVML queries during the timed region) -------------------
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons every few ms through NVML (ctypes)."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, index, period_s=0.005):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], 0
+        self.max_mhz = None
+        self.ok = False
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_r = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self.stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(int(clk.value))
+            if get_r(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.stop = threading.Event()
+            self.th = threading.Thread(target=self._run, daemon=True)
+            self.th.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self.stop.set()
+            self.th.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        names = sorted(n for bit, n in self.REASONS.items() if self.reasons & bit and bit != 0x1)
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ---- workload accounting ---------------------------------------------------------
+
+def draft_algorithmic(inp):
+    """HBM bytes and tensor FLOPs of one ds_draft_block call (P counted once)."""
+    B, K, V, r = inp["B"], inp["K"], inp["V"], inp["r"]
+    eb = 2 if inp["bf16"] else 4
+    by = B * K * V * eb + r * V * eb + B * K * r * eb + B * K * (4 + 4 + 16)
+    return by, 2.0 * B * K * r * V
+
+
+def verify_algorithmic(inp, L, n_final_residual, n_final_bonus):
+    B, K, V, r = inp["B"], inp["K"], inp["V"], inp["r"]
+    eb = 2 if inp["bf16"] else 4
+    rows = int(sum(int(l) + 1 for l in L))
+    by = rows * V * eb + n_final_bonus * V * eb + n_final_residual * 2 * V * eb
+    if n_final_residual:
+        by += r * V * eb
+    return by, 2.0 * n_final_residual * r * V
+
+
+# ---- CPU oracle timing ------------------------------------------------------------
+
+def oracle_sample(inp, seed, n_req):
+    """Time the oracle's cycle on the first n_req requests (schedule on all)."""
+    import numpy as np
+    import oracle
+    rows = np.arange(n_req)
+    t0 = time.perf_counter()
+    d = oracle.draft_block(inp["base_logits"][rows], inp["E"], inp["P"], inp["anchor"][rows],
+                           inp["temperature"][rows], seed)
+    c = oracle.confidence(inp["h"][rows], inp["E"], inp["anchor"][rows], d["tokens"], inp["w_h"],
+                          inp["w_e"], inp["conf_bias"], inp["sts_temp"])
+    sch = oracle.schedule(oracle.survival(c), inp["sps"])
+    oracle.verify(inp["target_logits"][rows], inp["base_logits"][rows], inp["E"], inp["P"],
+                  inp["anchor"][rows], d["tokens"], sch["L"], inp["temperature"][rows], seed)
+    dt = time.perf_counter() - t0
+    return dt, n_req * inp["K"]
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, seed, budget_s=12.0):
+    n_req = 1
+    dt, toks = oracle_sample(inp, seed, n_req)
+    if dt < budget_s / 4:
+        n_req = max(1, min(inp["B"], int(budget_s / max(dt, 1e-3))))
+        dt, toks = oracle_sample(inp, seed, n_req)
+    return {"value": toks / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": "%d of %d requests x K=%d positions: float64 draft (bias matmul + exp/cumsum "
+                      "per position), confidence + schedule, verify; %.1f s" %
+                      (n_req, inp["B"], inp["K"], dt)}
+
+
+# ---- main -------------------------------------------------------------------------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    import torch
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def reduce_max(x, ws):
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    from speculative_decoding_draft_block_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    n_req = max(1, int(os.environ.get("DS_REF_REQUESTS", "2")))
+    for i in range(args.warmup):
+        oracle_sample(inp, 0x5EED0000 + i, n_req)
+    tot, toks = 0.0, 0
+    for i in range(args.steps):
+        dt, t = oracle_sample(inp, 0x5EED1000 + i, n_req)
+        tot += dt
+        toks += t
+    value = toks / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V, "r": w.r, "d": w.d,
+                       "sample_requests": n_req},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
+                             "kind": "oracle",
+                             "sample": "%d of %d requests per step, all K=%d positions" %
+                                       (n_req, w.B, w.K)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--mode", type=int, default=0, help="0 greedy+early stop, 1 fixed K")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, ws, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+        return
+
+    import numpy as np
+    import torch
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.cycle import DeviceCycle, to_host_pinned, INPUT_KEYS
+    from speculative_decoding_draft_block_gb300.workloads import WORKLOADS, make_inputs
+
+    if not os.path.exists(_lib.LIB_PATH):
+        from speculative_decoding_draft_block_gb300 import build
+        build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    cyc = DeviceCycle(inp, device=dev, mode=args.mode)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+    seed0 = 0x5EED0000 + 7919 * rank
+
+    for i in range(args.warmup):
+        cyc.run(seed0 + i)
+    torch.cuda.synchronize(dev)
+    cyc.reset_status()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    t_wall = time.perf_counter()
+    with sampler:
+        for i in range(K):
+            flush.zero_()                       # untimed L2 flush between cycles
+            e = ev[i]
+            e[0].record(stream)
+            cyc.draft(seed0 + 1000 + i)
+            e[1].record(stream)
+            cyc.schedule()
+            e[2].record(stream)
+            cyc.verify(seed0 + 1000 + i)
+            e[3].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    cyc.check_status()
+    per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                    for e in ev])
+    cycle_ms = per.sum(axis=1)
+    total_s = reduce_max(float(cycle_ms.sum()) / 1e3, ws)
+    B, Kb, V = w.B, w.K, w.V
+    value = ws * B * Kb * K / total_s
+    res = cyc.results()
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tc = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    d_by, d_fl = draft_algorithmic(inp)
+    d_ms = float(per[:, 0].mean())
+    t_hbm = d_by / (hbm * 1e9)
+    t_tc = d_fl / (tc * 1e12)
+    if t_hbm >= t_tc:
+        achieved = d_by / (d_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None}
+    else:
+        achieved = d_fl / (d_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc, "unit": "TFLOP/s",
+                "frac": achieved / tc, "traffic": None}
+    roof.update({"kernel": "ds_draft_block (all K steps)", "peak_source": peak_src,
+                 "algorithmic_bytes": d_by, "algorithmic_flops": d_fl,
+                 "t_roof_us": 1e6 * max(t_hbm, t_tc), "t_meas_us": 1e3 * d_ms})
+    n_res = int(np.sum((res["accept_count"] < res["L"]) & (inp["temperature"] > 0)))
+    n_bon = int(np.sum((res["accept_count"] >= res["L"]) & (inp["temperature"] > 0)))
+    v_by, v_fl = verify_algorithmic(inp, res["L"], n_res, n_bon)
+    cycle_roof_us = 1e6 * (max(t_hbm, t_tc) + max(v_by / (hbm * 1e9), v_fl / (tc * 1e12)))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": float(cycle_ms.mean()), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.bf16 else "f32",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {"workload": w.name, "B": B, "K": Kb, "V": V, "r": w.r, "d": w.d,
+                   "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write, outside the timed events); "
+                         "inputs also exceed L2",
+                   "mode": "greedy_earlystop" if args.mode == 0 else "fixed_k"},
+        "components_ms": {"draft": float(per[:, 0].mean()), "schedule": float(per[:, 1].mean()),
+                          "verify": float(per[:, 2].mean())},
+        "emitted_tokens_per_s": ws * float(res["num_emitted"].sum()) / (total_s / K),
+        "verified_tokens_per_s": ws * float((res["L"] + 1).sum()) / (total_s / K),
+        "mean_sched_len": float(res["L"].mean()), "mean_accepted": float(res["accept_count"].mean()),
+        "cycle_roofline_us": cycle_roof_us, "cycle_roofline_frac": cycle_roof_us / (1e3 * cycle_ms.mean()),
+        "roofline": roof,
+        "gpu_launches": K * (2 * Kb + 2 + 4),
+        "wall_s": wall,
+        "clocks": sampler.summary(),
+    }
+
+    if not args.no_e2e:
+        # End to end through the public API: pinned host inputs copied in and the
+        # emitted tokens copied out inside the timed region, every step.
+        host = {k: to_host_pinned(inp[k]) for k in INPUT_KEYS}
+        out_host = torch.empty((B, Kb + 1), dtype=torch.int32).pin_memory()
+        nem_host = torch.empty((B,), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * 4 + nem_host.numel() * 4
+        for i in range(2):
+            for k in INPUT_KEYS:
+                cyc.t[k].copy_(host[k].view(cyc.t[k].dtype) if host[k].dtype != cyc.t[k].dtype else host[k], non_blocking=True)
+            cyc.run(seed0 + i)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        E = max(1, args.e2e_steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(E):
+            for k in INPUT_KEYS:
+                src = host[k] if host[k].dtype == cyc.t[k].dtype else host[k].view(cyc.t[k].dtype)
+                cyc.t[k].copy_(src, non_blocking=True)
+            cyc.run(seed0 + 5000 + i)
+            out_host.copy_(cyc.out_tokens, non_blocking=True)
+            nem_host.copy_(cyc.num_emitted, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws)
+        line["e2e"] = {"value": ws * B * Kb * E / e2e_s, "unit": "tokens/s",
+                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                       "steps": E}
+        cyc.check_status()
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, 0x5EED0000)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+/*
+ * ds_draft.h -- C ABI of the draft-block sampling, confidence scheduling and
+ * lossless verification hot path (one GPU, NVIDIA GB300 / sm_103a).
+ *
+ * Method sources (cited by page and section):
+ *   [DSpark]  "DSpark: 반자기회귀 생성과 신뢰도 기반 검증으로 speculative decoding
+ *             가속하기" -- sections 배경 (background: draft/verify cycle, lossless
+ *             rejection rule), 방법론 › 반자기회귀 생성 (semi-autoregressive
+ *             generation, Markov head), 방법론 › 신뢰도 기반 검증 (confidence head,
+ *             STS, survival, hardware-aware prefix scheduler).
+ *   [DFlash]  "[vLLM] MTP & DFlash" -- section DFlashProposer 초기화 (one bonus
+ *             token plus K drafted tokens per request and cycle).
+ *   [Philox]  Salmon et al., "Parallel random numbers: as easy as 1, 2, 3", SC'11.
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller allocates every buffer, including the workspace;
+ *     the library never allocates, frees or keeps a pointer after returning.
+ *   - Asynchrony: compute calls enqueue kernels on `stream` and return; no call
+ *     synchronises except ds_check_status.
+ *   - Errors: arguments the host can check are validated before anything is
+ *     launched; a failing check returns a non-zero ds_status and launches
+ *     nothing. Conditions only the device can see (token id out of range, a
+ *     NaN or +inf logit, a bad temperature) are written to the caller's
+ *     device word `status` (first error wins) and leave the outputs undefined.
+ *     The caller zeroes `status` before the cycle and reads it with
+ *     ds_check_status afterwards.
+ *   - Layout: row-major, the last index contiguous; token ids are int32.
+ *     Device pointers must be 16-byte aligned.
+ *   - Limits: 1 <= B, 1 <= K <= 64, B*K <= 16384, 8 <= V, V % 8 == 0,
+ *     16 <= r <= 1024, r % 16 == 0, d % 8 == 0. A logit of -inf has zero
+ *     probability; NaN and +inf are errors. Sampling temperatures are 0
+ *     (greedy) or in [1e-3, 1e3].
+ *   - Randomness: one uniform per decision, u = (w0 + 0.5) * 2^-32 where w0 is
+ *     word 0 of Philox4x32-10 with key (seed & 0xffffffff, seed >> 32) and
+ *     counter (request, position, stage, 0); positions are 1-based.
+ *   - Reentrancy: stateless; calls with distinct outputs and workspaces may run
+ *     concurrently on different streams.
+ */
+#ifndef DS_DRAFT_H
+#define DS_DRAFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* ds_stream_t; /* a cudaStream_t; NULL is the legacy default stream */
+
+typedef enum {
+  DS_OK = 0,
+  DS_ERR_INVALID_ARG = 1, /* a size, pointer, alignment or mode is out of its range */
+  DS_ERR_UNSUPPORTED = 2, /* no device of compute capability 10.3, or a dtype not supported */
+  DS_ERR_WORKSPACE = 3,   /* workspace pointer missing or smaller than *_workspace_bytes */
+  DS_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch or query) */
+  DS_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+  DS_ERR_BOUNDS = 6,      /* a token id read from device memory is outside [0, V) */
+  DS_ERR_NONFINITE = 7    /* a NaN or +inf logit, or a row with no finite logit */
+} ds_status;
+
+typedef enum { DS_F32 = 0, DS_BF16 = 1 } ds_dtype;
+
+enum { DS_STAGE_DRAFT = 0, DS_STAGE_ACCEPT = 1, DS_STAGE_RESAMPLE = 2 };
+
+enum {
+  DS_SCHED_GREEDY_EARLYSTOP = 0, /* [DSpark] 신뢰도 기반 검증: global greedy + early stop */
+  DS_SCHED_FIXED_K = 1,          /* verify every drafted token (scheduler off) */
+  DS_SCHED_THRESHOLD = 2         /* static survival threshold (the page's threshold sweep) */
+};
+
+/*
+ * Per-position statistics of a draft distribution, written by ds_draft_block
+ * for every sampled (T > 0) position and read back by ds_verify. With
+ * t_i = (z_i + bias_i) * log2(e) / T, the draft probability of token i is
+ *     q_i = 2^(t_i - ref) / (sum_hi + sum_lo).
+ * For greedy positions sum_hi = 1, sum_lo = 0, ref = 0 and `argmax` holds the
+ * chosen token; for sampled positions argmax = -1.
+ */
+typedef struct {
+  float sum_hi;
+  float sum_lo;
+  int32_t ref;
+  int32_t argmax;
+} ds_row_stats;
+
+/* ------------------------------------------------------------------------ */
+/* Randomness                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* [Philox] Philox4x32-10: ten rounds of two 32x32->64 multiplies (constants
+ * 0xD2511F53, 0xCD9E8D57) with a Weyl key schedule (0x9E3779B9, 0xBB67AE85).
+ * Host function; `ctr`, `key`, `out` are host arrays of 4, 2 and 4 words. */
+void ds_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* The cycle's uniform for (seed, request, position, stage), exact in double,
+ * strictly inside (0, 1). Host function. */
+double ds_uniform(uint64_t seed, uint32_t request, uint32_t position, uint32_t stage);
+
+/* Device evaluation of the same generator, for checking the kernels' copy:
+ * ctr is a device array [n][4], out a device array [n][4]; key as above. */
+ds_status ds_philox_fill(const uint32_t* ctr, uint32_t key0, uint32_t key1, uint32_t* out,
+                         int32_t n, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Draft block: Markov head + sequential sampling                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [DSpark] 방법론 › 반자기회귀 생성. For k = 1..K, with x_0 = anchor[b]:
+ *     l_k = z_k + E[x_{k-1}] . P             (low-rank first-order transition bias)
+ *     x_k ~ softmax(l_k / T_b)                (T_b = 0: argmax, lowest index on ties)
+ * The draw is the inverse CDF in token order: x = min{i : u * S < C_i} with
+ * u = U(seed, b, k, DS_STAGE_DRAFT). The loop is sequential over k and
+ * parallel over requests and vocabulary; the V-wide logits are never stored.
+ */
+typedef struct {
+  int32_t B, K, V, r;
+  int32_t dtype;              /* ds_dtype of base_logits, E and P */
+  const void* base_logits;    /* [B][K][V]  z_k, the parallel backbone's logits */
+  const void* E;              /* [V][r]     Markov embedding table */
+  const void* P;              /* [r][V]     Markov projection */
+  const int32_t* anchor;      /* [B]        x_0, the last verified token */
+  const float* temperature;   /* [B]        sampling temperature, 0 = greedy */
+  uint64_t seed;              /* Philox key */
+  int32_t* draft_tokens;      /* out [B][K] x_k */
+  float* q_token;             /* out [B][K] q_k(x_k) (1.0 for greedy positions) */
+  ds_row_stats* q_stats;      /* out [B][K] statistics of q_k, read by ds_verify */
+  void* workspace;            /* scratch, ds_draft_workspace_bytes(B, K, V, r) bytes */
+  size_t workspace_bytes;
+  int32_t* status;            /* device word, see Errors above */
+} ds_draft_args;
+
+size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
+ds_status ds_draft_block(const ds_draft_args* args, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Confidence head, survival and prefix scheduler                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [DSpark] 방법론 › 신뢰도 기반 검증.
+ *     c_k = sigmoid((w_h . h_k + w_e . E[x_{k-1}] + bias) / sts_temp[k])
+ *     s_k = c_1 * ... * c_k                    (survival, monotone in k)
+ * GREEDY_EARLYSTOP: candidates (b, k) sorted by s descending (ties: k then b
+ * ascending); starting from N = B, A = B, J = SPS(B), each candidate is taken
+ * iff J' = SPS(N+1) * (A + s) / (N+1) > J, and the walk stops at the first
+ * candidate that is not taken. SPS(n) = sps[min(n, n_max) - 1].
+ * FIXED_K: L_b = K. THRESHOLD: L_b = #{k : s_k >= threshold}.
+ * The objective J is evaluated in double precision.
+ */
+typedef struct {
+  int32_t B, K, d, r, V;
+  int32_t dtype;              /* ds_dtype of h, E, w_h and w_e */
+  const void* h;              /* [B][K][d]  backbone hidden states */
+  const void* E;              /* [V][r]     Markov embedding table */
+  const int32_t* anchor;      /* [B] */
+  const int32_t* draft_tokens;/* [B][K] */
+  const void* w_h;            /* [d] */
+  const void* w_e;            /* [r] */
+  float bias;                 /* b */
+  const float* sts_temp;      /* [K] per-position STS temperatures (> 0) */
+  const float* sps;           /* [n_max] SPS(n) for n = 1..n_max (tokens/s) */
+  int32_t n_max;
+  int32_t mode;               /* DS_SCHED_* */
+  float threshold;            /* DS_SCHED_THRESHOLD only */
+  float* conf;                /* out [B][K] c_k */
+  float* survival;            /* out [B][K] s_k */
+  int32_t* sched_len;         /* out [B]    L_b in [0, K] */
+  double* objective;          /* out [1]    J at the chosen lengths */
+  void* workspace;            /* ds_sched_workspace_bytes(B, K) bytes */
+  size_t workspace_bytes;
+  int32_t* status;
+} ds_sched_args;
+
+size_t ds_sched_workspace_bytes(int32_t B, int32_t K);
+ds_status ds_confidence_schedule(const ds_sched_args* args, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Lossless verification                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [DSpark] 배경: left-to-right rejection sampling that preserves the target
+ * distribution. For k = 1..L_b with p_k = softmax(target_k / T_b):
+ *     accept iff u * q_k(x_k) < p_k(x_k),   u = U(seed, b, k, DS_STAGE_ACCEPT)
+ * At the first rejection k: y ~ normalize(max(0, p_k - q_k)) by inverse CDF
+ * with u = U(seed, b, k, DS_STAGE_RESAMPLE); if all L_b pass, the bonus
+ * y ~ p_{L_b+1} with u = U(seed, b, L_b+1, DS_STAGE_RESAMPLE) ([DFlash]: the
+ * target scores K+1 positions per request). T_b = 0: accept iff x_k is the
+ * target argmax; emit the target argmax. q_k is rebuilt from base_logits, E,
+ * P and q_stats exactly as ds_draft_block defined it.
+ */
+typedef struct {
+  int32_t B, K, V, r;
+  int32_t dtype;              /* ds_dtype of target_logits, base_logits, E and P */
+  const void* target_logits;  /* [B][K+1][V] */
+  const void* base_logits;    /* [B][K][V] */
+  const void* E;              /* [V][r] */
+  const void* P;              /* [r][V] */
+  const int32_t* anchor;      /* [B] */
+  const int32_t* draft_tokens;/* [B][K] */
+  const float* q_token;       /* [B][K] */
+  const ds_row_stats* q_stats;/* [B][K] */
+  const int32_t* sched_len;   /* [B] */
+  const float* temperature;   /* [B] */
+  uint64_t seed;
+  int32_t* out_tokens;        /* out [B][K+1]: accepted prefix then y, -1 padded */
+  int32_t* accept_count;      /* out [B] */
+  int32_t* num_emitted;       /* out [B] = accept_count + 1 */
+  void* workspace;            /* ds_verify_workspace_bytes(B, K, V, r) bytes */
+  size_t workspace_bytes;
+  int32_t* status;
+} ds_verify_args;
+
+size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
+ds_status ds_verify(const ds_verify_args* args, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status and identification                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, reads the device status word and returns it (or
+ * DS_ERR_CUDA if the stream reports an error). */
+ds_status ds_check_status(const int32_t* device_status, ds_stream_t stream);
+
+/* Static description of a status code. */
+const char* ds_status_string(ds_status s);
+
+/* Library version, "major.minor.patch". */
+const char* ds_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS_DRAFT_H */

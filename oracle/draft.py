@@ -53,7 +53,7 @@ def draft_step(ell_row, temperature, u):
     return x, float(w[x] / s), margin
 
 
-def draft_block(base_logits, E, P, anchor, temperature, seed, prev_tokens=None):
+def draft_block(base_logits, E, P, anchor, temperature, seed, prev_tokens=None, request_ids=None):
     """Sample a whole draft block, position by position.
 
     base_logits: [B, K, V] (bfloat16 bits or floats); E: [V, r]; P: [r, V];
@@ -64,6 +64,9 @@ def draft_block(base_logits, E, P, anchor, temperature, seed, prev_tokens=None):
     k = 1) instead of the oracle's own previous draw, so each draw can be
     compared on its own against another implementation's prefix.
 
+    ``request_ids`` (optional [B]) gives each row's request index in the Philox
+    counter when the rows are a subset of a larger batch (default: 0..B-1).
+
     Returns a dict with tokens [B, K] (int64), q_token [B, K] (float64),
     margin [B, K] and greedy [B] (bool).
     """
@@ -73,13 +76,14 @@ def draft_block(base_logits, E, P, anchor, temperature, seed, prev_tokens=None):
     tokens = np.zeros((B, K), dtype=np.int64)
     q_token = np.zeros((B, K), dtype=np.float64)
     margin = np.zeros((B, K), dtype=np.float64)
+    rid = np.arange(B) if request_ids is None else np.asarray(request_ids, dtype=np.int64)
     prev = anchor.copy()
     for k in range(K):
         if prev_tokens is not None and k > 0:
             prev = np.asarray(prev_tokens, dtype=np.int64)[:, k - 1]
         ell = markov_logits(base_logits[:, k, :], E, P, prev)
         for b in range(B):
-            u = uniform(seed, b, k + 1, STAGE_DRAFT)
+            u = uniform(seed, int(rid[b]), k + 1, STAGE_DRAFT)
             x, q, m = draft_step(ell[b], float(temperature[b]), u)
             tokens[b, k] = x
             q_token[b, k] = q

@@ -74,11 +74,15 @@ def verify_request(tokens, L, p_row, q_row, u_accept, u_resample, greedy=False):
     return accepted, [int(t) for t in tokens[:accepted]] + [int(y)], decisions
 
 
-def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperature, seed):
+def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperature, seed,
+           request_ids=None):
     """Verify a batch. target_logits: [B, K+1, V]; base_logits: [B, K, V].
 
     The draft distribution q_k is recomputed from the base logits and the Markov
     bias of the drafted prefix (x_0 = anchor), exactly as the draft defined it.
+
+    ``request_ids`` (optional [B]) gives each row's request index in the Philox
+    counter when the rows are a subset of a larger batch.
 
     Returns a dict with accept_count [B], num_emitted [B], out_tokens [B, K+1]
     (-1 padded) and decisions (per request, see verify_request).
@@ -91,6 +95,7 @@ def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperat
     out = -np.ones((B, K + 1), dtype=np.int64)
     acc = np.zeros(B, dtype=np.int64)
     decisions = []
+    rid = np.arange(B) if request_ids is None else np.asarray(request_ids, dtype=np.int64)
     for b in range(B):
         T = float(temperature[b])
         greedy = T == 0
@@ -109,8 +114,8 @@ def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperat
 
         a, emitted, dec = verify_request(
             tokens[b], L, p_row, q_row,
-            lambda j, b=b: uniform(seed, b, j + 1, STAGE_ACCEPT),
-            lambda j, b=b: uniform(seed, b, j + 1, STAGE_RESAMPLE),
+            lambda j, b=b: uniform(seed, int(rid[b]), j + 1, STAGE_ACCEPT),
+            lambda j, b=b: uniform(seed, int(rid[b]), j + 1, STAGE_RESAMPLE),
             greedy=greedy)
         acc[b] = a
         out[b, :len(emitted)] = emitted

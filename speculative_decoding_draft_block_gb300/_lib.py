@@ -1,0 +1,233 @@
+"""ctypes binding of libdsdraft.so (argument marshalling only).
+
+Every function keeps the C name and forwards device pointers, sizes and the
+current CUDA stream; all computation happens in the library's kernels. PyTorch
+tensors are used only as device memory. If the shared library is missing, every
+call raises: there is no fallback path.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsdraft.so")
+
+DS_OK = 0
+DS_F32, DS_BF16 = 0, 1
+DS_STAGE_DRAFT, DS_STAGE_ACCEPT, DS_STAGE_RESAMPLE = 0, 1, 2
+DS_SCHED_GREEDY_EARLYSTOP, DS_SCHED_FIXED_K, DS_SCHED_THRESHOLD = 0, 1, 2
+STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_UNSUPPORTED", 3: "DS_ERR_WORKSPACE",
+                4: "DS_ERR_CUDA", 5: "DS_ERR_TIMEOUT", 6: "DS_ERR_BOUNDS", 7: "DS_ERR_NONFINITE"}
+
+# Every symbol include/ds_draft.h declares.
+EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspace_bytes",
+           "ds_draft_block", "ds_sched_workspace_bytes", "ds_confidence_schedule",
+           "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
+           "ds_version")
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+
+
+class DraftArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("K", _i32), ("V", _i32), ("r", _i32), ("dtype", _i32),
+                ("base_logits", _vp), ("E", _vp), ("P", _vp), ("anchor", _vp),
+                ("temperature", _vp), ("seed", ctypes.c_uint64), ("draft_tokens", _vp),
+                ("q_token", _vp), ("q_stats", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
+
+
+class SchedArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("K", _i32), ("d", _i32), ("r", _i32), ("V", _i32), ("dtype", _i32),
+                ("h", _vp), ("E", _vp), ("anchor", _vp), ("draft_tokens", _vp), ("w_h", _vp),
+                ("w_e", _vp), ("bias", ctypes.c_float), ("sts_temp", _vp), ("sps", _vp),
+                ("n_max", _i32), ("mode", _i32), ("threshold", ctypes.c_float),
+                ("conf", _vp), ("survival", _vp), ("sched_len", _vp), ("objective", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
+
+
+class VerifyArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("K", _i32), ("V", _i32), ("r", _i32), ("dtype", _i32),
+                ("target_logits", _vp), ("base_logits", _vp), ("E", _vp), ("P", _vp),
+                ("anchor", _vp), ("draft_tokens", _vp), ("q_token", _vp), ("q_stats", _vp),
+                ("sched_len", _vp), ("temperature", _vp), ("seed", ctypes.c_uint64),
+                ("out_tokens", _vp), ("accept_count", _vp), ("num_emitted", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
+
+
+_lib = None
+
+
+def load():
+    """Load libdsdraft.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libdsdraft.so is not built (run `python -m "
+                           "speculative_decoding_draft_block_gb300.build`); no fallback exists")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.ds_philox4x32_10.argtypes = [ctypes.POINTER(ctypes.c_uint32)] * 3
+    lib.ds_philox4x32_10.restype = None
+    lib.ds_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
+    lib.ds_uniform.restype = ctypes.c_double
+    lib.ds_philox_fill.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32, _vp, _i32, _vp]
+    lib.ds_philox_fill.restype = ctypes.c_int
+    for f in ("ds_draft_workspace_bytes", "ds_verify_workspace_bytes"):
+        getattr(lib, f).argtypes = [_i32] * 4
+        getattr(lib, f).restype = ctypes.c_size_t
+    lib.ds_sched_workspace_bytes.argtypes = [_i32] * 2
+    lib.ds_sched_workspace_bytes.restype = ctypes.c_size_t
+    lib.ds_draft_block.argtypes = [ctypes.POINTER(DraftArgs), _vp]
+    lib.ds_confidence_schedule.argtypes = [ctypes.POINTER(SchedArgs), _vp]
+    lib.ds_verify.argtypes = [ctypes.POINTER(VerifyArgs), _vp]
+    for f in ("ds_draft_block", "ds_confidence_schedule", "ds_verify"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.ds_check_status.argtypes = [_vp, _vp]
+    lib.ds_check_status.restype = ctypes.c_int
+    lib.ds_status_string.argtypes = [ctypes.c_int]
+    lib.ds_status_string.restype = ctypes.c_char_p
+    lib.ds_version.argtypes = []
+    lib.ds_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+class DsError(RuntimeError):
+    def __init__(self, code, what=""):
+        super().__init__("%s%s" % (STATUS_NAMES.get(code, str(code)), (": " + what) if what else ""))
+        self.code = code
+
+
+def check(code, what=""):
+    if code != DS_OK:
+        raise DsError(code, what)
+    return code
+
+
+def _ptr(t, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return DS_BF16
+    if t.dtype == torch.float32:
+        return DS_F32
+    raise ValueError("logits/weights must be bfloat16 or float32")
+
+
+# ---- randomness --------------------------------------------------------------
+
+def ds_philox4x32_10(ctr, key):
+    lib = load()
+    c = (ctypes.c_uint32 * 4)(*[int(v) & 0xFFFFFFFF for v in ctr])
+    k = (ctypes.c_uint32 * 2)(*[int(v) & 0xFFFFFFFF for v in key])
+    o = (ctypes.c_uint32 * 4)()
+    lib.ds_philox4x32_10(c, k, o)
+    return tuple(o)
+
+
+def ds_uniform(seed, request, position, stage):
+    return load().ds_uniform(int(seed), int(request), int(position), int(stage))
+
+
+def ds_philox_fill(ctr, key0, key1, out, stream=None):
+    """ctr, out: int32 CUDA tensors [n, 4] (bit patterns of uint32)."""
+    return load().ds_philox_fill(_ptr(ctr, "ctr"), int(key0) & 0xFFFFFFFF, int(key1) & 0xFFFFFFFF,
+                                 _ptr(out, "out"), int(ctr.shape[0]), _stream(stream))
+
+
+# ---- workspace sizes --------------------------------------------------------------
+
+def ds_draft_workspace_bytes(B, K, V, r):
+    return load().ds_draft_workspace_bytes(B, K, V, r)
+
+
+def ds_sched_workspace_bytes(B, K):
+    return load().ds_sched_workspace_bytes(B, K)
+
+
+def ds_verify_workspace_bytes(B, K, V, r):
+    return load().ds_verify_workspace_bytes(B, K, V, r)
+
+
+# ---- the three calls ----------------------------------------------------------
+
+def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q_token, q_stats,
+                   workspace, status, stream=None):
+    B, K, V = base_logits.shape
+    a = DraftArgs(B=B, K=K, V=V, r=E.shape[1], dtype=_dtype_code(base_logits),
+                  base_logits=_ptr(base_logits, "base_logits"), E=_ptr(E, "E"), P=_ptr(P, "P"),
+                  anchor=_ptr(anchor, "anchor"), temperature=_ptr(temperature, "temperature"),
+                  seed=int(seed), draft_tokens=_ptr(draft_tokens, "draft_tokens"),
+                  q_token=_ptr(q_token, "q_token"), q_stats=_ptr(q_stats, "q_stats"),
+                  workspace=_ptr(workspace, "workspace"),
+                  workspace_bytes=workspace.numel() * workspace.element_size(),
+                  status=_ptr(status, "status"))
+    return load().ds_draft_block(ctypes.byref(a), _stream(stream))
+
+
+def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp, sps, mode,
+                           conf, survival, sched_len, objective, status, threshold=0.0,
+                           workspace=None, stream=None):
+    B, K, d = h.shape
+    a = SchedArgs(B=B, K=K, d=d, r=E.shape[1], V=E.shape[0], dtype=_dtype_code(h),
+                  h=_ptr(h, "h"), E=_ptr(E, "E"), anchor=_ptr(anchor, "anchor"),
+                  draft_tokens=_ptr(draft_tokens, "draft_tokens"), w_h=_ptr(w_h, "w_h"),
+                  w_e=_ptr(w_e, "w_e"), bias=float(bias), sts_temp=_ptr(sts_temp, "sts_temp"),
+                  sps=_ptr(sps, "sps"), n_max=int(sps.shape[0]), mode=int(mode),
+                  threshold=float(threshold), conf=_ptr(conf, "conf"),
+                  survival=_ptr(survival, "survival"), sched_len=_ptr(sched_len, "sched_len"),
+                  objective=_ptr(objective, "objective"),
+                  workspace=_ptr(workspace, "workspace") if workspace is not None else None,
+                  workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                  status=_ptr(status, "status"))
+    return load().ds_confidence_schedule(ctypes.byref(a), _stream(stream))
+
+
+def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats, sched_len,
+              temperature, seed, out_tokens, accept_count, num_emitted, workspace, status,
+              stream=None):
+    B, K1, V = target_logits.shape
+    a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
+                   target_logits=_ptr(target_logits, "target_logits"),
+                   base_logits=_ptr(base_logits, "base_logits"), E=_ptr(E, "E"), P=_ptr(P, "P"),
+                   anchor=_ptr(anchor, "anchor"), draft_tokens=_ptr(draft_tokens, "draft_tokens"),
+                   q_token=_ptr(q_token, "q_token"), q_stats=_ptr(q_stats, "q_stats"),
+                   sched_len=_ptr(sched_len, "sched_len"), temperature=_ptr(temperature, "temperature"),
+                   seed=int(seed), out_tokens=_ptr(out_tokens, "out_tokens"),
+                   accept_count=_ptr(accept_count, "accept_count"),
+                   num_emitted=_ptr(num_emitted, "num_emitted"),
+                   workspace=_ptr(workspace, "workspace"),
+                   workspace_bytes=workspace.numel() * workspace.element_size(),
+                   status=_ptr(status, "status"))
+    return load().ds_verify(ctypes.byref(a), _stream(stream))
+
+
+def ds_check_status(status, stream=None):
+    return load().ds_check_status(_ptr(status, "status"), _stream(stream))
+
+
+def ds_status_string(code):
+    return load().ds_status_string(int(code)).decode()
+
+
+def ds_version():
+    return load().ds_version().decode()

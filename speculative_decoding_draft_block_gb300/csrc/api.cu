@@ -1,0 +1,297 @@
+// C-ABI layer: argument validation, workspace layout and kernel launches.
+// Declarations and the contract of every entry point are in include/ds_draft.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/ds_draft.h"
+#include "internal.h"
+#include "philox.h"
+
+using namespace ds;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
+
+// The kernels are built for sm_103a only; refuse other devices up front.
+ds_status device_supported() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
+  static std::mutex mu;
+  static int cached[64];
+  static bool init = false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (int i = 0; i < 64; ++i) cached[i] = -1;
+    init = true;
+  }
+  if (dev < 0 || dev >= 64) return DS_ERR_UNSUPPORTED;
+  if (cached[dev] < 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return DS_ERR_CUDA;
+    cached[dev] = (major == 10 && minor == 3) ? 1 : 0;
+  }
+  return cached[dev] ? DS_OK : DS_ERR_UNSUPPORTED;
+}
+
+bool shape_ok(int32_t B, int32_t K, int32_t V, int32_t r) {
+  if (B < 1 || K < 1 || K > 64 || V < 8 || (V % 8) != 0) return false;
+  if (r < 16 || r > 1024 || (r % 16) != 0) return false;
+  if ((int64_t)B * K > 16384) return false;
+  return true;
+}
+
+ds_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DS_OK : DS_ERR_CUDA; }
+
+size_t draft_ws(int32_t B, int32_t V) {
+  return align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
+}
+
+struct VerifyLayout {
+  size_t vrows, desc, chunks, total;
+};
+
+VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V) {
+  VerifyLayout l;
+  l.vrows = 0;
+  l.desc = l.vrows + align_up((size_t)B * (K + 1) * sizeof(VRow));
+  l.chunks = l.desc + align_up((size_t)B * sizeof(FinalDesc));
+  l.total = l.chunks + align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+void ds_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  const Philox4 r = philox4x32_10(ctr[0], ctr[1], ctr[2], ctr[3], key[0], key[1]);
+  memcpy(out, r.v, sizeof(r.v));
+}
+
+double ds_uniform(uint64_t seed, uint32_t request, uint32_t position, uint32_t stage) {
+  return uniform_from_word(philox_word(seed, request, position, stage));
+}
+
+ds_status ds_philox_fill(const uint32_t* ctr, uint32_t key0, uint32_t key1, uint32_t* out,
+                         int32_t n, ds_stream_t stream) {
+  if (n < 0 || (n > 0 && (!aligned16(ctr) || !aligned16(out)))) return DS_ERR_INVALID_ARG;
+  if (n == 0) return DS_OK;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  return from_cuda(launch_philox_fill(ctr, key0, key1, out, n, (cudaStream_t)stream));
+}
+
+size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r) {
+  if (!shape_ok(B, K, V, r)) return 0;
+  return draft_ws(B, V);
+}
+
+ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
+  if (a == nullptr) return DS_ERR_INVALID_ARG;
+  if (!shape_ok(a->B, a->K, a->V, a->r)) return DS_ERR_INVALID_ARG;
+  if (a->dtype != DS_F32 && a->dtype != DS_BF16) return DS_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->base_logits, a->E, a->P, a->anchor, a->temperature,
+                        a->draft_tokens, a->q_token, a->q_stats, a->status};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return DS_ERR_INVALID_ARG;
+  if (a->workspace == nullptr || !aligned16(a->workspace) ||
+      a->workspace_bytes < draft_ws(a->B, a->V))
+    return DS_ERR_WORKSPACE;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+
+  SampleParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = a->B;
+  p.K = a->K;
+  p.V = a->V;
+  p.r = a->r;
+  p.n_chunks = num_chunks(a->V);
+  p.src = 0;
+  p.dtype = a->dtype;
+  p.base_logits = a->base_logits;
+  p.E = a->E;
+  p.P = a->P;
+  p.anchor = a->anchor;
+  p.draft_tokens = a->draft_tokens;
+  p.temperature = a->temperature;
+  p.chunks = reinterpret_cast<ChunkRec*>(a->workspace);
+  p.seed = a->seed;
+  p.tokens_out = a->draft_tokens;
+  p.q_token = a->q_token;
+  p.q_stats = a->q_stats;
+  p.status = a->status;
+  const cudaStream_t s = (cudaStream_t)stream;
+  for (int k = 1; k <= a->K; ++k) {
+    p.step = k;
+    cudaError_t e = launch_sample_tile(p, s);
+    if (e != cudaSuccess) return DS_ERR_CUDA;
+    e = launch_sample_locate(p, s);
+    if (e != cudaSuccess) return DS_ERR_CUDA;
+  }
+  return DS_OK;
+}
+
+size_t ds_sched_workspace_bytes(int32_t B, int32_t K) {
+  (void)B;
+  (void)K;
+  return 0;
+}
+
+ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
+  if (a == nullptr) return DS_ERR_INVALID_ARG;
+  if (a->B < 1 || a->K < 1 || a->K > 64 || (int64_t)a->B * a->K > 16384) return DS_ERR_INVALID_ARG;
+  if (a->d < 8 || (a->d % 8) != 0 || a->r < 16 || (a->r % 16) != 0 || a->r > 1024 || a->V < 8 ||
+      (a->V % 8) != 0)
+    return DS_ERR_INVALID_ARG;
+  if (a->dtype != DS_F32 && a->dtype != DS_BF16) return DS_ERR_INVALID_ARG;
+  if (a->n_max < 1) return DS_ERR_INVALID_ARG;
+  if (a->mode != DS_SCHED_GREEDY_EARLYSTOP && a->mode != DS_SCHED_FIXED_K &&
+      a->mode != DS_SCHED_THRESHOLD)
+    return DS_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->h, a->E, a->anchor, a->draft_tokens, a->w_h, a->w_e, a->sts_temp,
+                        a->sps, a->conf, a->survival, a->sched_len, a->objective, a->status};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return DS_ERR_INVALID_ARG;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  SchedParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = a->B;
+  p.K = a->K;
+  p.d = a->d;
+  p.r = a->r;
+  p.V = a->V;
+  p.dtype = a->dtype;
+  p.n_max = a->n_max;
+  p.mode = a->mode;
+  p.bias = a->bias;
+  p.threshold = a->threshold;
+  p.h = a->h;
+  p.E = a->E;
+  p.anchor = a->anchor;
+  p.draft_tokens = a->draft_tokens;
+  p.w_h = a->w_h;
+  p.w_e = a->w_e;
+  p.sts_temp = a->sts_temp;
+  p.sps = a->sps;
+  p.conf = a->conf;
+  p.survival = a->survival;
+  p.sched_len = a->sched_len;
+  p.objective = a->objective;
+  p.status = a->status;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (launch_confidence(p, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_schedule(p, s) != cudaSuccess) return DS_ERR_CUDA;
+  return DS_OK;
+}
+
+size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r) {
+  if (!shape_ok(B, K, V, r)) return 0;
+  return verify_layout(B, K, V).total;
+}
+
+ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
+  if (a == nullptr) return DS_ERR_INVALID_ARG;
+  if (!shape_ok(a->B, a->K, a->V, a->r)) return DS_ERR_INVALID_ARG;
+  if (a->dtype != DS_F32 && a->dtype != DS_BF16) return DS_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->target_logits, a->base_logits, a->E, a->P, a->anchor,
+                        a->draft_tokens, a->q_token, a->q_stats, a->sched_len,
+                        a->temperature, a->out_tokens, a->accept_count, a->num_emitted,
+                        a->status};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return DS_ERR_INVALID_ARG;
+  const VerifyLayout l = verify_layout(a->B, a->K, a->V);
+  if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < l.total)
+    return DS_ERR_WORKSPACE;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  char* ws = reinterpret_cast<char*>(a->workspace);
+  VerifyParams v;
+  memset(&v, 0, sizeof(v));
+  v.B = a->B;
+  v.K = a->K;
+  v.V = a->V;
+  v.r = a->r;
+  v.n_chunks = num_chunks(a->V);
+  v.dtype = a->dtype;
+  v.target_logits = a->target_logits;
+  v.anchor = a->anchor;
+  v.draft_tokens = a->draft_tokens;
+  v.q_token = a->q_token;
+  v.q_stats = a->q_stats;
+  v.sched_len = a->sched_len;
+  v.temperature = a->temperature;
+  v.seed = a->seed;
+  v.vrows = reinterpret_cast<VRow*>(ws + l.vrows);
+  v.final_desc = reinterpret_cast<FinalDesc*>(ws + l.desc);
+  v.out_tokens = a->out_tokens;
+  v.accept_count = a->accept_count;
+  v.num_emitted = a->num_emitted;
+  v.status = a->status;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (launch_verify_rows(v, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_verify_finalize(v, s) != cudaSuccess) return DS_ERR_CUDA;
+
+  SampleParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = a->B;
+  p.K = a->K;
+  p.V = a->V;
+  p.r = a->r;
+  p.n_chunks = v.n_chunks;
+  p.src = 1;
+  p.dtype = a->dtype;
+  p.base_logits = a->base_logits;
+  p.target_logits = a->target_logits;
+  p.E = a->E;
+  p.P = a->P;
+  p.anchor = a->anchor;
+  p.draft_tokens = a->draft_tokens;
+  p.temperature = a->temperature;
+  p.final_desc = v.final_desc;
+  p.chunks = reinterpret_cast<ChunkRec*>(ws + l.chunks);
+  p.seed = a->seed;
+  p.tokens_out = a->out_tokens;
+  p.status = a->status;
+  if (launch_sample_tile(p, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_sample_locate(p, s) != cudaSuccess) return DS_ERR_CUDA;
+  return DS_OK;
+}
+
+ds_status ds_check_status(const int32_t* device_status, ds_stream_t stream) {
+  if (device_status == nullptr) return DS_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DS_ERR_CUDA;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, device_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DS_ERR_CUDA;
+  return (ds_status)h;
+}
+
+const char* ds_status_string(ds_status s) {
+  switch (s) {
+    case DS_OK: return "ok";
+    case DS_ERR_INVALID_ARG: return "invalid argument";
+    case DS_ERR_UNSUPPORTED: return "unsupported device or dtype";
+    case DS_ERR_WORKSPACE: return "workspace missing or too small";
+    case DS_ERR_CUDA: return "CUDA runtime error";
+    case DS_ERR_TIMEOUT: return "device wait timed out";
+    case DS_ERR_BOUNDS: return "token id out of range";
+    case DS_ERR_NONFINITE: return "non-finite logit or empty distribution";
+  }
+  return "unknown status";
+}
+
+const char* ds_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,157 @@
+// Shared device numerics for the sampling kernels.
+//
+// Sampling by inverse CDF over a ~152k-token vocabulary must agree with a
+// float64 reference on almost every draw. A per-token relative error delta in
+// the weights moves the CDF by a random walk whose mean absolute size is a few
+// hundred times delta at V ~ 1.5e5, so the kernels keep every weight within a
+// couple of float32 ulps and never round a running sum:
+//   * t = logit * log2(e) / T is carried as an unevaluated sum: the product of
+//     the logit with the high part of log2(e)/T is split exactly with an FMA
+//     (Dekker / Ogita-Rump-Oishi TwoProduct), the small terms are folded in.
+//   * t = k + f with k = rint(t_hi) (so t_hi - k is exact), w = 2^f * 2^(k-n),
+//     where n is a per-chunk integer reference: rescaling between chunks is a
+//     power of two and therefore exact.
+//   * Sums are double-float (Knuth's TwoSum), so accumulation adds no error
+//     beyond ~2^-48 relative.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "philox.h"
+
+namespace ds {
+
+#define kNegInf (-__int_as_float(0x7f800000))
+constexpr int kEmptyRef = -(1 << 29);  // reference of a chunk with no mass
+constexpr int kChunk = 32;             // tokens per partial-sum record
+
+enum DsStatusCode {
+  kOk = 0,
+  kErrInvalidArg = 1,
+  kErrUnsupported = 2,
+  kErrWorkspace = 3,
+  kErrCuda = 4,
+  kErrTimeout = 5,
+  kErrBounds = 6,
+  kErrNonfinite = 7
+};
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---- element loads ---------------------------------------------------------
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+// Load 8 consecutive elements (16-byte aligned for bf16, 32 for f32) as floats.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* o) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float* o) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+// ---- double-float ----------------------------------------------------------
+
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+// acc += x, keeping the rounding error of the high word in the low word.
+__device__ __forceinline__ void df_accumulate(DF& acc, float x) {
+  const DF t = two_sum(acc.hi, x);
+  acc.hi = t.hi;
+  acc.lo = __fadd_rn(acc.lo, t.lo);
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  DF s = two_sum(a.hi, b.hi);
+  s.lo = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  return fast_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ DF df_scale2(DF a, int e) {  // exact power-of-two scaling
+  return {ldexpf(a.hi, e), ldexpf(a.lo, e)};
+}
+
+__device__ __forceinline__ double df_to_double(DF a) { return (double)a.hi + (double)a.lo; }
+
+// ---- log2(e) / T as a double-float -----------------------------------------
+
+struct Gscale {
+  float hi, lo;
+};
+
+__device__ __forceinline__ Gscale make_gscale(float T) {
+  const double g = 1.4426950408889634073599246810019 / (double)T;
+  const float hi = (float)g;
+  return {hi, (float)(g - (double)hi)};
+}
+
+// t = (z + b) * g  as  k + f  with k integral (float), |f| <~ 0.5 + |b g|.
+__device__ __forceinline__ void exp2_split(float z, float b, Gscale g, float& k, float& f) {
+  const float a = __fmul_rn(z, g.hi);
+  const float ae = __fmaf_rn(z, g.hi, -a);  // z*g.hi - a, exact
+  float tl = __fmaf_rn(z, g.lo, ae);
+  tl = __fmaf_rn(b, g.hi, tl);
+  k = rintf(a);
+  f = __fadd_rn(__fsub_rn(a, k), tl);  // a - k is exact
+}
+
+// 2^(t - n) for t = (z + b) * g; 0 when z is -inf or the result is below 2^-140.
+__device__ __forceinline__ float exp2_rel(float z, float b, Gscale g, int n) {
+  if (z == kNegInf) return 0.f;
+  float k, f;
+  exp2_split(z, b, g, k, f);
+  const int e = (int)k - n;
+  if (e < -140) return 0.f;
+  return ldexpf(exp2f(f), e);
+}
+
+// Chunk reference: rint of the largest z*g.hi among finite entries.
+__device__ __forceinline__ float scaled_hi(float z, Gscale g) { return __fmul_rn(z, g.hi); }
+
+// ---- uniform ---------------------------------------------------------------
+
+__device__ __forceinline__ double uniform_dev(uint64_t seed, uint32_t request,
+                                              uint32_t position, uint32_t stage) {
+  return uniform_from_word(philox_word(seed, request, position, stage));
+}
+
+// Non-finite check for logits: NaN or +inf is an error; -inf is allowed.
+__device__ __forceinline__ bool bad_logit(float x) {
+  return !(x == x) || x == __int_as_float(0x7f800000);
+}
+
+}  // namespace ds

@@ -1,0 +1,120 @@
+// Internal types shared by the kernels and the C-ABI layer (not part of the ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds_draft.h"
+
+namespace ds {
+
+// One partial-sum record per (row, 32-token chunk).
+//   sampling rows: chunk sum (hi + lo) of 2^(t_i - ref), ref the chunk reference
+//   greedy rows:   the chunk's largest logit (hi + lo) and its token in `idx`
+struct ChunkRec {
+  float hi, lo;
+  int32_t ref;
+  int32_t idx;
+};
+
+enum RowMode : int32_t {
+  kSkip = 0,
+  kGreedyMarkov = 1,  // draft position with T = 0: argmax of z + bias
+  kSampleMarkov = 2,  // draft position with T > 0: inverse CDF of softmax((z + bias)/T)
+  kResidual = 3,      // verify, first rejection: inverse CDF of max(0, p - q)
+  kBonus = 4          // verify, all accepted: inverse CDF of p_{L+1}
+};
+
+// Final draw of one request in ds_verify (written by the finalize kernel).
+struct FinalDesc {
+  int32_t mode;     // kSkip, kResidual or kBonus
+  int32_t row;      // 0-based position index j of the target (and base) row
+  int32_t a_token;  // token whose E row forms the Markov bias (residual)
+  int32_t out_pos;  // where the drawn token goes in out_tokens[b]
+  int32_t Np, Nq;   // references of the target and draft rows
+  float Rhi, Rlo;   // S_p / S_q as a double-float
+};
+
+// Per (request, target row) results of the verify row pass.
+struct VRow {
+  float s_hi, s_lo;  // S_p = sum 2^(t_i - ref)
+  int32_t ref;
+  int32_t argmax;    // T = 0 rows
+  int32_t accept;    // 1 if the drafted token at this position passed
+  int32_t valid;
+  int32_t pad[2];
+};
+
+struct SampleParams {
+  int32_t B, K, V, r, n_chunks;
+  int32_t src;   // 0: draft step, 1: final draw of verify
+  int32_t step;  // draft: 1-based position k
+  int32_t dtype;
+  const void* base_logits;    // [B][K][V]
+  const void* target_logits;  // [B][K+1][V]
+  const void* E;
+  const void* P;
+  const int32_t* anchor;
+  const int32_t* draft_tokens;  // [B][K] (read: previous positions; written by locate)
+  const float* temperature;
+  const FinalDesc* final_desc;  // [B]
+  ChunkRec* chunks;             // [B][n_chunks]
+  uint64_t seed;
+  int32_t* tokens_out;        // draft: draft_tokens; final: out_tokens
+  float* q_token;             // draft only
+  ds_row_stats* q_stats;      // draft only
+  int32_t* status;
+};
+
+struct VerifyParams {
+  int32_t B, K, V, r, n_chunks, dtype;
+  const void* target_logits;
+  const int32_t* anchor;
+  const int32_t* draft_tokens;
+  const float* q_token;
+  const ds_row_stats* q_stats;
+  const int32_t* sched_len;
+  const float* temperature;
+  uint64_t seed;
+  VRow* vrows;  // [B][K+1]
+  FinalDesc* final_desc;
+  int32_t* out_tokens;
+  int32_t* accept_count;
+  int32_t* num_emitted;
+  int32_t* status;
+};
+
+struct SchedParams {
+  int32_t B, K, d, r, V, dtype, n_max, mode;
+  float bias, threshold;
+  const void* h;
+  const void* E;
+  const int32_t* anchor;
+  const int32_t* draft_tokens;
+  const void* w_h;
+  const void* w_e;
+  const float* sts_temp;
+  const float* sps;
+  float* conf;
+  float* survival;
+  int32_t* sched_len;
+  double* objective;
+  int32_t* status;
+};
+
+constexpr int kTileRows = 32;   // rows per sampling CTA
+constexpr int kTileCols = 256;  // tokens per sampling CTA (8 chunks of 32)
+
+inline int32_t num_chunks(int32_t V) { return (V + 31) / 32; }
+
+size_t sample_tile_smem_bytes(int32_t r);
+cudaError_t launch_sample_tile(const SampleParams& p, cudaStream_t s);
+cudaError_t launch_sample_locate(const SampleParams& p, cudaStream_t s);
+cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_confidence(const SchedParams& p, cudaStream_t s);
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
+size_t schedule_smem_bytes(int32_t B, int32_t K);
+cudaError_t launch_philox_fill(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_t* out,
+                               int32_t n, cudaStream_t s);
+
+}  // namespace ds

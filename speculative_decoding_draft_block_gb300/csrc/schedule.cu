@@ -1,0 +1,222 @@
+// Confidence head, survival and the hardware-aware prefix scheduler.
+//
+// DSpark summary page, 방법론 › 신뢰도 기반 검증:
+//   c_k = sigmoid((w_h . h_k + w_e . E[x_{k-1}] + b) / T_k)   (STS temperature T_k)
+//   s_k = c_1 * ... * c_k                                      (prefix survival)
+// The scheduler sorts all (request, position) candidates by survival and adds
+// them greedily while the expected throughput J = SPS(N) * A / N keeps rising,
+// stopping at the first candidate that does not raise it (non-anticipation).
+//
+//   confidence_kernel  one warp per (b, k): two dot products (d and r long,
+//                      16-byte loads, fp32 accumulation of exact bf16
+//                      products), sigmoid.
+//   schedule_kernel    one CTA: survival cumprod, bitonic sort of 64-bit keys
+//                      (survival descending, then k, then b) in shared memory,
+//                      double-precision prefix scan of A and J, first drop.
+#include <cuda_bf16.h>
+#include <float.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds {
+
+namespace {
+
+template <typename Tin>
+__device__ __forceinline__ float dot_warp(const Tin* a, const Tin* w, int n, int lane) {
+  float acc = 0.f;
+  for (int i = lane * 8; i < n; i += 32 * 8) {
+    float x[8], y[8];
+    load8(a + i, x);
+    load8(w + i, y);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc = __fmaf_rn(x[q], y[q], acc);
+  }
+  for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  return acc;
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) confidence_kernel(SchedParams p) {
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (item >= p.B * p.K) return;
+  const int b = item / p.K, k = item - b * p.K;
+  int prev = (k == 0) ? p.anchor[b] : p.draft_tokens[(size_t)b * p.K + k - 1];
+  if (prev < 0 || prev >= p.V) {
+    if (lane == 0) report(p.status, kErrBounds);
+    prev = 0;
+  }
+  const Tin* h = reinterpret_cast<const Tin*>(p.h) + (size_t)item * p.d;
+  const Tin* E = reinterpret_cast<const Tin*>(p.E) + (size_t)prev * p.r;
+  const float dh = dot_warp(h, reinterpret_cast<const Tin*>(p.w_h), p.d, lane);
+  const float de = dot_warp(E, reinterpret_cast<const Tin*>(p.w_e), p.r, lane);
+  if (lane == 0) {
+    const float Tk = p.sts_temp[k];
+    const float logit = (dh + de + p.bias) / Tk;
+    const float c = 1.f / (1.f + expf(-logit));
+    if (!(c == c) || !(Tk > 0.f)) report(p.status, kErrNonfinite);
+    p.conf[item] = c;
+  }
+}
+
+__device__ __forceinline__ double sps_at(const float* sps, int n_max, int n) {
+  return (double)sps[(n < n_max ? n : n_max) - 1];
+}
+
+constexpr int kSchedThreads = 1024;
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) {
+  extern __shared__ unsigned long long keys[];
+  __shared__ double wsum[32];
+  __shared__ int red[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int B = p.B, K = p.K, n = B * K;
+
+  // survival (sequential over k per request, fp32)
+  for (int b = tid; b < B; b += kSchedThreads) {
+    float s = 1.f;
+    int L = 0;
+    for (int k = 0; k < K; ++k) {
+      s = s * p.conf[(size_t)b * K + k];
+      p.survival[(size_t)b * K + k] = s;
+      if (p.mode == DS_SCHED_THRESHOLD && s >= p.threshold && L == k) L = k + 1;
+    }
+    p.sched_len[b] = (p.mode == DS_SCHED_FIXED_K) ? K : (p.mode == DS_SCHED_THRESHOLD ? L : 0);
+  }
+  __syncthreads();
+  if (p.mode != DS_SCHED_GREEDY_EARLYSTOP) {
+    if (tid == 0) {
+      long long nsum = B;
+      double a = B;
+      for (int b = 0; b < B; ++b) {
+        const int L = p.sched_len[b];
+        nsum += L;
+        for (int k = 0; k < L; ++k) a += (double)p.survival[(size_t)b * K + k];
+      }
+      p.objective[0] = sps_at(p.sps, p.n_max, (int)nsum) * a / (double)nsum;
+    }
+    return;
+  }
+
+  int n_pad = 1;
+  while (n_pad < n) n_pad <<= 1;
+  for (int i = tid; i < n_pad; i += kSchedThreads) {
+    unsigned long long key = ~0ull;
+    if (i < n) {
+      const int b = i / K, k = i - b * K;
+      const float s = p.survival[(size_t)b * K + k];
+      const uint32_t hi = 0xffffffffu - __float_as_uint(fmaxf(s, 0.f));
+      key = ((unsigned long long)hi << 32) | ((unsigned long long)k << 16) | (unsigned long long)b;
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  for (int size = 2; size <= n_pad; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < (n_pad >> 1); i += kSchedThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const unsigned long long a = keys[lo], c = keys[hi];
+        if ((a > c) == asc) {
+          keys[lo] = c;
+          keys[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // A_m = B + sum of the first m sorted survivals (double); each thread owns a
+  // contiguous run of sorted candidates.
+  const int per = (n + kSchedThreads - 1) / kSchedThreads;
+  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  double local = 0.0;
+  for (int i = i0; i < i1; ++i)
+    local += (double)__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
+  // block exclusive scan of `local`
+  double incl = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    const double v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    double v = wsum[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const double u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    wsum[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  double excl = incl - local + (wid > 0 ? wsum[wid - 1] : 0.0);
+
+  int first_drop = INT_MAX;
+  double a_prev = (double)B + excl;
+  double j_prev = sps_at(p.sps, p.n_max, B + i0) * a_prev / (double)(B + i0);
+  for (int i = i0; i < i1; ++i) {
+    const double s = (double)__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
+    const double a_new = a_prev + s;
+    const int nn = B + i + 1;
+    const double j_new = sps_at(p.sps, p.n_max, nn) * a_new / (double)nn;
+    if (!(j_new > j_prev)) {
+      first_drop = i;
+      break;
+    }
+    a_prev = a_new;
+    j_prev = j_new;
+  }
+  for (int o = 16; o > 0; o >>= 1) first_drop = min(first_drop, __shfl_xor_sync(0xffffffffu, first_drop, o));
+  if (lane == 0) red[wid] = first_drop;
+  __syncthreads();
+  int M = red[0];
+  for (int w = 1; w < kSchedThreads / 32; ++w) M = min(M, red[w]);
+  if (M == INT_MAX) M = n;
+
+  for (int i = tid; i < M; i += kSchedThreads) {
+    const unsigned long long key = keys[i];
+    const int k = (int)((key >> 16) & 0xffff), b = (int)(key & 0xffff);
+    atomicMax(&p.sched_len[b], k + 1);
+  }
+  // objective at the chosen set: thread owning item M-1 (or thread 0 for M = 0)
+  if (M == 0) {
+    if (tid == 0) p.objective[0] = sps_at(p.sps, p.n_max, B);
+  } else if (M - 1 >= i0 && M - 1 < i1) {
+    double a = (double)B + excl;
+    for (int i = i0; i < M; ++i) a += (double)__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
+    p.objective[0] = sps_at(p.sps, p.n_max, B + M) * a / (double)(B + M);
+  }
+}
+
+}  // namespace
+
+size_t schedule_smem_bytes(int32_t B, int32_t K) {
+  int n = B * K, n_pad = 1;
+  while (n_pad < n) n_pad <<= 1;
+  return (size_t)n_pad * sizeof(unsigned long long);
+}
+
+cudaError_t launch_confidence(const SchedParams& p, cudaStream_t s) {
+  const int items = p.B * p.K;
+  const int blocks = (items + 7) / 8;
+  if (p.dtype == DS_BF16)
+    confidence_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+  else
+    confidence_kernel<float><<<blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s) {
+  static cudaError_t attr = cudaFuncSetAttribute(
+      schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 8);
+  if (attr != cudaSuccess) return attr;
+  schedule_kernel<<<1, kSchedThreads, schedule_smem_bytes(p.B, p.K), s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ds

@@ -1,0 +1,218 @@
+// Verification kernels: target row statistics, accept tests and the final
+// draw's set-up.
+//
+// DSpark summary page, 배경: verification is left to right; the first rejection
+// discards everything after it, and the rejection rule keeps the target's
+// distribution exactly. Per (request b, scheduled position k <= L_b + 1):
+//
+//   verify_rows_kernel      one CTA per target row: streams the row once with
+//                           16-byte loads, builds S_p = sum 2^(t_i g - ref)
+//                           (per-thread power-of-two references merged
+//                           exactly, double-float sums), evaluates p(x_k) and
+//                           takes the accept decision u * q(x_k) < p(x_k) in
+//                           double (greedy rows: target argmax and exact match).
+//   verify_finalize_kernel  one thread per request: accepted prefix length,
+//                           emitted tokens, and the descriptor of the final
+//                           draw (residual at the first rejection, or bonus
+//                           from row L+1), drawn by the shared sampling kernels.
+#include <cuda_bf16.h>
+#include <float.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds {
+
+namespace {
+
+constexpr int kRowThreads = 512;
+
+template <typename Tin>
+__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p) {
+  __shared__ float sv[kRowThreads / 32];
+  __shared__ int si[kRowThreads / 32];
+  __shared__ int sref[kRowThreads / 32];
+  __shared__ DF sdf[kRowThreads];
+  const int j = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int lane = tid & 31, wid = tid >> 5;
+  int L = p.sched_len[b];
+  if (L < 0 || L > p.K) {
+    if (tid == 0) report(p.status, kErrInvalidArg);
+    L = L < 0 ? 0 : p.K;
+  }
+  if (j > L) return;
+  const float T = p.temperature[b];
+  const Tin* row = reinterpret_cast<const Tin*>(p.target_logits) + ((size_t)b * (p.K + 1) + j) * (size_t)p.V;
+  VRow out;
+  out.s_hi = out.s_lo = 0.f;
+  out.ref = 0;
+  out.argmax = -1;
+  out.accept = 0;
+  out.valid = 1;
+  out.pad[0] = out.pad[1] = 0;
+  bool bad = false;
+
+  if (T == 0.f) {
+    float best = kNegInf;
+    int bi = INT_MAX;
+    for (int i = tid * 8; i < p.V; i += kRowThreads * 8) {
+      float v[8];
+      load8(row + i, v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        bad |= bad_logit(v[q]);
+        if (v[q] > best || bi == INT_MAX) {
+          best = v[q];
+          bi = i + q;
+        }
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      sv[wid] = best;
+      si[wid] = bi;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float bb = sv[0];
+      int bx = si[0];
+      for (int w = 1; w < kRowThreads / 32; ++w)
+        if (sv[w] > bb || (sv[w] == bb && si[w] < bx)) {
+          bb = sv[w];
+          bx = si[w];
+        }
+      out.argmax = bx;
+      if (j < L) out.accept = (p.draft_tokens[(size_t)b * p.K + j] == bx) ? 1 : 0;
+    }
+  } else {
+    if (!(T >= 1e-3f && T <= 1e3f)) {
+      if (tid == 0) report(p.status, kErrInvalidArg);
+      return;
+    }
+    const Gscale g = make_gscale(T);
+    int nt = INT_MIN;
+    DF acc = {0.f, 0.f};
+    for (int i = tid * 8; i < p.V; i += kRowThreads * 8) {
+      float v[8];
+      load8(row + i, v);
+      float amax = kNegInf;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        bad |= bad_logit(v[q]);
+        if (v[q] != kNegInf) amax = fmaxf(amax, scaled_hi(v[q], g));
+      }
+      if (amax == kNegInf) continue;
+      const int ng = (int)rintf(amax);
+      if (ng > nt) {
+        if (nt != INT_MIN) acc = df_scale2(acc, max(nt - ng, -300));
+        nt = ng;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) df_accumulate(acc, exp2_rel(v[q], 0.f, g, nt));
+    }
+    int m = nt;
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) sref[wid] = m;
+    __syncthreads();
+    int N = sref[0];
+    for (int w = 1; w < kRowThreads / 32; ++w) N = max(N, sref[w]);
+    sdf[tid] = (nt == INT_MIN) ? DF{0.f, 0.f} : df_scale2(acc, max(nt - N, -300));
+    __syncthreads();
+    // fixed-order tree reduction
+    for (int s = kRowThreads / 2; s > 0; s >>= 1) {
+      if (tid < s) sdf[tid] = df_add(sdf[tid], sdf[tid + s]);
+      __syncthreads();
+    }
+    if (tid == 0) {
+      const DF S = sdf[0];
+      const double Sd = df_to_double(S);
+      out.s_hi = S.hi;
+      out.s_lo = S.lo;
+      out.ref = N;
+      if (!(Sd > 0.0)) bad = true;
+      if (j < L && Sd > 0.0) {
+        int x = p.draft_tokens[(size_t)b * p.K + j];
+        if (x < 0 || x >= p.V) {
+          report(p.status, kErrBounds);
+          x = 0;
+        }
+        const float tx = to_f32(row[x]);
+        const double px = (double)exp2_rel(tx, 0.f, g, N) / Sd;
+        const double qx = (double)p.q_token[(size_t)b * p.K + j];
+        const double u = uniform_dev(p.seed, (uint32_t)b, (uint32_t)(j + 1), DS_STAGE_ACCEPT);
+        out.accept = (u * qx < px) ? 1 : 0;
+      }
+    }
+  }
+  if (bad) report(p.status, kErrNonfinite);
+  if (tid == 0) p.vrows[(size_t)b * (p.K + 1) + j] = out;
+}
+
+__global__ void verify_finalize_kernel(VerifyParams p) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  const int K = p.K;
+  int L = p.sched_len[b];
+  L = L < 0 ? 0 : (L > K ? K : L);
+  const float T = p.temperature[b];
+  const VRow* vr = p.vrows + (size_t)b * (K + 1);
+  int a = 0;
+  while (a < L && vr[a].accept) ++a;
+  int32_t* out = p.out_tokens + (size_t)b * (K + 1);
+  for (int i = 0; i < a; ++i) out[i] = p.draft_tokens[(size_t)b * K + i];
+  for (int i = a; i <= K; ++i) out[i] = -1;
+  p.accept_count[b] = a;
+  p.num_emitted[b] = a + 1;
+  FinalDesc d;
+  d.mode = kSkip;
+  d.row = a;
+  d.a_token = -1;
+  d.out_pos = a;
+  d.Np = d.Nq = 0;
+  d.Rhi = d.Rlo = 0.f;
+  if (T == 0.f) {
+    out[a] = vr[a].argmax;
+  } else if (T >= 1e-3f && T <= 1e3f) {
+    d.Np = vr[a].ref;
+    if (a < L) {
+      d.mode = kResidual;
+      d.a_token = (a == 0) ? p.anchor[b] : p.draft_tokens[(size_t)b * K + (a - 1)];
+      const ds_row_stats qs = p.q_stats[(size_t)b * K + a];
+      d.Nq = qs.ref;
+      const double Sp = (double)vr[a].s_hi + (double)vr[a].s_lo;
+      const double Sq = (double)qs.sum_hi + (double)qs.sum_lo;
+      const double R = Sp / Sq;
+      d.Rhi = (float)R;
+      d.Rlo = (float)(R - (double)d.Rhi);
+    } else {
+      d.mode = kBonus;
+    }
+  }
+  p.final_desc[b] = d;
+}
+
+}  // namespace
+
+cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s) {
+  dim3 grid(p.K + 1, p.B);
+  if (p.dtype == DS_BF16)
+    verify_rows_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, s>>>(p);
+  else
+    verify_rows_kernel<float><<<grid, kRowThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s) {
+  verify_finalize_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ds

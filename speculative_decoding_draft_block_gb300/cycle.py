@@ -1,0 +1,117 @@
+"""One speculative cycle on the GPU through the C ABI: draft -> schedule -> verify.
+
+`DeviceCycle` owns the device buffers of one workload (PyTorch allocations used
+as plain device memory) and issues the three library calls on a stream. It does
+no arithmetic of its own.
+"""
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import check
+
+
+def _to_device(a, device):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def to_host_pinned(a):
+    """Pinned host copy of an input array (bf16 kept as bf16)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a)
+    return t.pin_memory()
+
+
+INPUT_KEYS = ("base_logits", "target_logits", "E", "P", "anchor", "temperature", "h", "w_h",
+              "w_e", "sts_temp", "sps")
+
+
+class DeviceCycle:
+    def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0):
+        self.inp = inp
+        self.device = torch.device(device)
+        self.mode = mode
+        self.threshold = threshold
+        B, K, V, r = inp["B"], inp["K"], inp["V"], inp["r"]
+        self.B, self.K, self.V, self.r, self.d = B, K, V, r, inp["d"]
+        dev = self.device
+        self.t = {k: _to_device(inp[k], dev) for k in INPUT_KEYS}
+        self.t["anchor"] = self.t["anchor"].to(torch.int32)
+        self.conf_bias = float(inp["conf_bias"])
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.draft_tokens = torch.zeros((B, K), **i32)
+        self.q_token = torch.zeros((B, K), **f32)
+        self.q_stats = torch.zeros((B, K, 4), **i32)
+        self.conf = torch.zeros((B, K), **f32)
+        self.survival = torch.zeros((B, K), **f32)
+        self.sched_len = torch.zeros((B,), **i32)
+        self.objective = torch.zeros((2,), dtype=torch.float64, device=dev)
+        self.out_tokens = torch.zeros((B, K + 1), **i32)
+        self.accept_count = torch.zeros((B,), **i32)
+        self.num_emitted = torch.zeros((B,), **i32)
+        self.status = torch.zeros((4,), **i32)
+        wd = _lib.ds_draft_workspace_bytes(B, K, V, r)
+        wv = _lib.ds_verify_workspace_bytes(B, K, V, r)
+        if wd == 0 or wv == 0:
+            raise ValueError("shape not supported by the library")
+        self.ws_draft = torch.empty((wd,), dtype=torch.uint8, device=dev)
+        self.ws_verify = torch.empty((wv,), dtype=torch.uint8, device=dev)
+
+    # -- the three calls ---------------------------------------------------------
+    def draft(self, seed, stream=None):
+        t = self.t
+        check(_lib.ds_draft_block(t["base_logits"], t["E"], t["P"], t["anchor"], t["temperature"],
+                                  seed, self.draft_tokens, self.q_token, self.q_stats,
+                                  self.ws_draft, self.status, stream), "ds_draft_block")
+
+    def schedule(self, stream=None):
+        t = self.t
+        check(_lib.ds_confidence_schedule(t["h"], t["E"], t["anchor"], self.draft_tokens, t["w_h"],
+                                          t["w_e"], self.conf_bias, t["sts_temp"], t["sps"],
+                                          self.mode, self.conf, self.survival, self.sched_len,
+                                          self.objective, self.status, threshold=self.threshold,
+                                          stream=stream), "ds_confidence_schedule")
+
+    def verify(self, seed, stream=None):
+        t = self.t
+        check(_lib.ds_verify(t["target_logits"], t["base_logits"], t["E"], t["P"], t["anchor"],
+                             self.draft_tokens, self.q_token, self.q_stats, self.sched_len,
+                             t["temperature"], seed, self.out_tokens, self.accept_count,
+                             self.num_emitted, self.ws_verify, self.status, stream), "ds_verify")
+
+    def run(self, seed, stream=None):
+        """Enqueue one cycle (three library calls); no host synchronisation."""
+        self.draft(seed, stream)
+        self.schedule(stream)
+        self.verify(seed, stream)
+
+    def check_status(self, stream=None):
+        code = _lib.ds_check_status(self.status, stream)
+        check(code, "device status")
+
+    def reset_status(self):
+        self.status.zero_()
+
+    def results(self):
+        st = self.q_stats.cpu().numpy()
+        return {
+            "tokens": self.draft_tokens.cpu().numpy().astype(np.int64),
+            "q_token": self.q_token.cpu().numpy().astype(np.float64),
+            "q_sum": st[..., 0].view(np.float32).astype(np.float64) + st[..., 1].view(np.float32),
+            "q_ref": st[..., 2].copy(),
+            "conf": self.conf.cpu().numpy().astype(np.float64),
+            "survival": self.survival.cpu().numpy().astype(np.float64),
+            "L": self.sched_len.cpu().numpy().astype(np.int64),
+            "objective": float(self.objective[0].item()),
+            "out_tokens": self.out_tokens.cpu().numpy().astype(np.int64),
+            "accept_count": self.accept_count.cpu().numpy().astype(np.int64),
+            "num_emitted": self.num_emitted.cpu().numpy().astype(np.int64),
+        }

@@ -1,0 +1,112 @@
+"""Comparison of a GPU cycle with the oracle on the same seeded inputs.
+
+Rules (from the parity specification):
+  * token ids, accept counts and scheduled lengths are compared exactly;
+  * a mismatch is allowed only at a near-tie -- a draw whose float64 CDF margin
+    to u is below 1e-6 (greedy choices: top-1/top-2 logit gap below 1e-6;
+    accept tests: |u - p/q| below 1e-6; schedule: relative objective change or
+    survival gap at the stop below 1e-5) -- and mismatched draws must stay
+    under 1e-4 of all draws;
+  * probabilities and confidences agree within 2e-3 relative.
+Every draw is checked on its own: the oracle is teacher-forced with the GPU's
+previous tokens, so one exempt mismatch does not cascade.
+"""
+import numpy as np
+
+import oracle
+
+NEAR_TIE = 1e-6
+SCHED_NEAR_TIE = 1e-5
+MISMATCH_BUDGET = 1e-4
+REL_TOL = 2e-3
+
+
+ROW_KEYS = ("base_logits", "target_logits", "anchor", "temperature", "h")
+GPU_ROW_KEYS = ("tokens", "q_token", "conf", "survival", "L", "out_tokens", "accept_count",
+                "num_emitted")
+
+
+def subset(inp, g, rows):
+    """Restrict inputs and GPU results to some requests (the RNG keeps global ids)."""
+    rows = np.asarray(rows)
+    si = dict(inp)
+    for k in ROW_KEYS:
+        si[k] = inp[k][rows]
+    sg = dict(g)
+    for k in GPU_ROW_KEYS:
+        sg[k] = g[k][rows]
+    return si, sg
+
+
+def compare_draft(inp, g, seed, request_ids=None):
+    o = oracle.draft_block(inp["base_logits"], inp["E"], inp["P"], inp["anchor"],
+                           inp["temperature"], seed, prev_tokens=g["tokens"],
+                           request_ids=request_ids)
+    mism = o["tokens"] != g["tokens"]
+    near = o["margin"] < NEAR_TIE
+    draws = mism.size
+    rep = {"draws": int(draws), "mismatches": int(mism.sum()), "near_ties": int(near.sum()),
+           "unexplained": int((mism & ~near).sum())}
+    ok = ~mism
+    rel = np.abs(g["q_token"][ok] - o["q_token"][ok]) / np.maximum(o["q_token"][ok], 1e-300)
+    rep["q_max_rel"] = float(rel.max()) if rel.size else 0.0
+    return rep, o
+
+
+def compare_schedule(inp, g):
+    c = oracle.confidence(inp["h"], inp["E"], inp["anchor"], g["tokens"], inp["w_h"], inp["w_e"],
+                          inp["conf_bias"], inp["sts_temp"])
+    s = oracle.survival(c)
+    sch = oracle.schedule(s, inp["sps"])
+    rep = {
+        "conf_max_rel": float(np.max(np.abs(g["conf"] - c) / c)),
+        "surv_max_rel": float(np.max(np.abs(g["survival"] - s) / s)),
+        "L_mismatch": int(np.sum(sch["L"] != g["L"])),
+        "near_tie": bool(min(sch["stop_rel_gain"], sch["survival_gap"]) < SCHED_NEAR_TIE),
+        "objective_rel": abs(g["objective"] - sch["objective"]) / abs(sch["objective"]),
+    }
+    return rep, sch
+
+
+def compare_verify(inp, g, seed, request_ids=None):
+    o = oracle.verify(inp["target_logits"], inp["base_logits"], inp["E"], inp["P"], inp["anchor"],
+                      g["tokens"], g["L"], inp["temperature"], seed, request_ids=request_ids)
+    bad_req = np.nonzero((o["accept_count"] != g["accept_count"]) |
+                         np.any(o["out_tokens"] != g["out_tokens"], axis=1))[0]
+    decisions = sum(len(d) for d in o["decisions"])
+    unexplained = []
+    for b in bad_req:
+        if not any(m < NEAR_TIE for _, m in o["decisions"][b]):
+            unexplained.append(int(b))
+    near = sum(1 for d in o["decisions"] for _, m in d if m < NEAR_TIE)
+    rep = {"requests": int(len(g["L"])), "decisions": int(decisions),
+           "mismatched_requests": int(len(bad_req)), "unexplained": unexplained,
+           "near_ties": int(near)}
+    return rep, o
+
+
+def assert_parity(inp, g, seed, check_schedule=True, check_verify=True, rows=None):
+    """Check a GPU cycle against the oracle; ``rows`` limits draft/verify to some requests."""
+    if check_schedule:
+        rs, _ = compare_schedule(inp, g)
+        assert rs["conf_max_rel"] < REL_TOL and rs["surv_max_rel"] < REL_TOL, rs
+        if not rs["near_tie"]:
+            assert rs["L_mismatch"] == 0, rs
+            assert rs["objective_rel"] < 1e-5, rs
+    rid = None
+    if rows is not None:
+        inp, g = subset(inp, g, rows)
+        rid = np.asarray(rows)
+    rd, od = compare_draft(inp, g, seed, request_ids=rid)
+    assert rd["unexplained"] == 0, rd
+    assert rd["mismatches"] <= MISMATCH_BUDGET * rd["draws"], rd
+    assert rd["q_max_rel"] < REL_TOL, rd
+    out = {"draft": rd}
+    if check_schedule:
+        out["schedule"] = rs
+    if check_verify:
+        rv, _ = compare_verify(inp, g, seed, request_ids=rid)
+        assert not rv["unexplained"], rv
+        assert rv["mismatched_requests"] <= MISMATCH_BUDGET * rv["decisions"], rv
+        out["verify"] = rv
+    return out

@@ -1,0 +1,76 @@
+"""The C-ABI library builds, loads and exports every declared symbol (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ds_draft.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_draft_block_gb300 import _lib, build
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_binding_exports():
+    from speculative_decoding_draft_block_gb300 import _lib
+    assert _declared() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True)
+    if out.returncode == 0:
+        syms = {l.split()[-1] for l in out.stdout.splitlines() if l.strip()}
+        for name in _declared():
+            assert name in syms, name
+
+
+def test_host_philox_matches_oracle(lib):
+    import numpy as np
+    from speculative_decoding_draft_block_gb300 import _lib
+    import oracle
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        v = [int(x) for x in rng.integers(0, 2**32, size=6, dtype=np.uint64)]
+        assert _lib.ds_philox4x32_10(v[:4], v[4:]) == oracle.philox4x32_10(v[:4], v[4:])
+    seed = (0xDEADBEEF << 32) | 0x5EED0000
+    for b in range(5):
+        for k in range(1, 6):
+            for s in range(3):
+                assert _lib.ds_uniform(seed, b, k, s) == oracle.uniform(seed, b, k, s)
+
+
+def test_workspace_sizes_and_limits(lib):
+    from speculative_decoding_draft_block_gb300 import _lib
+    assert _lib.ds_draft_workspace_bytes(128, 16, 151936, 256) >= 128 * 4748 * 16
+    assert _lib.ds_verify_workspace_bytes(128, 16, 151936, 256) > 0
+    assert _lib.ds_draft_workspace_bytes(128, 65, 151936, 256) == 0      # K > 64
+    assert _lib.ds_draft_workspace_bytes(128, 16, 151937, 256) == 0      # V % 8 != 0
+    assert _lib.ds_draft_workspace_bytes(1024, 17, 1024, 256) == 0       # B*K > 16384
+    assert _lib.ds_sched_workspace_bytes(128, 16) == 0
+
+
+def test_host_validation_rejects_without_launching(lib):
+    from speculative_decoding_draft_block_gb300 import _lib
+    # NULL args pointer and a zeroed struct are refused on the host
+    assert lib.ds_draft_block(None, None) == 1
+    a = _lib.DraftArgs()
+    assert lib.ds_draft_block(ctypes.byref(a), None) == 1
+    assert lib.ds_verify(ctypes.byref(_lib.VerifyArgs()), None) == 1
+    assert lib.ds_confidence_schedule(ctypes.byref(_lib.SchedArgs()), None) == 1
+    assert _lib.ds_status_string(7) == "non-finite logit or empty distribution"
+    assert _lib.ds_version() == "0.1.0"

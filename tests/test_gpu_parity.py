@@ -1,0 +1,194 @@
+"""GPU cycle vs the oracle, through the C ABI (needs a GB300).
+
+Sizes: the tiny workload and ragged multi-tile cases are compared in full; the
+full-size workloads are compared on every draw (B32, B128) or on a sample of
+requests (B512, B256), always with the oracle teacher-forced on the GPU's own
+prefix so every draw is checked on its own.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from tests import _parity
+
+pytestmark = pytest.mark.gpu
+
+SEED = 0x5EED0000
+
+
+@pytest.fixture(scope="module")
+def ds():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_draft_block_gb300 import _lib, build
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    _lib.load()
+    import speculative_decoding_draft_block_gb300 as pkg
+    return pkg
+
+
+def _run(inp, seed=SEED, **kw):
+    from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
+    cyc = DeviceCycle(inp, **kw)
+    cyc.reset_status()
+    cyc.run(seed)
+    cyc.check_status()
+    return cyc, cyc.results()
+
+
+def test_philox_device_words(ds):
+    import torch
+    import oracle
+    from speculative_decoding_draft_block_gb300 import _lib
+    n = 1 << 20
+    rng = np.random.default_rng(0)
+    ctr = rng.integers(0, 2**32, size=(n, 4), dtype=np.uint64).astype(np.uint32)
+    key = (0x89ABCDEF, 0x01234567)
+    ct = torch.from_numpy(ctr.view(np.int32)).cuda()
+    out = torch.zeros_like(ct)
+    assert _lib.ds_philox_fill(ct, key[0], key[1], out) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint32)
+    # vectorised Philox4x32-10 in NumPy (third implementation, for the bulk)
+    c = [ctr[:, i].astype(np.uint64) for i in range(4)]
+    k0, k1 = np.uint64(key[0]), np.uint64(key[1])
+    M = np.uint64(0xFFFFFFFF)
+    for rnd in range(10):
+        if rnd:
+            k0 = (k0 + np.uint64(0x9E3779B9)) & M
+            k1 = (k1 + np.uint64(0xBB67AE85)) & M
+        p0 = np.uint64(0xD2511F53) * c[0]
+        p1 = np.uint64(0xCD9E8D57) * c[2]
+        c = [((p1 >> np.uint64(32)) ^ c[1] ^ k0) & M, p1 & M, ((p0 >> np.uint64(32)) ^ c[3] ^ k1) & M, p0 & M]
+    want = np.stack(c, axis=1).astype(np.uint32)
+    assert np.array_equal(got, want)
+    for i in range(0, n, n // 500):
+        assert tuple(got[i]) == oracle.philox4x32_10(ctr[i], key)
+
+
+def test_tiny_cycle(ds):
+    from speculative_decoding_draft_block_gb300.workloads import TINY, make_inputs
+    inp = make_inputs(TINY)
+    _, g = _run(inp)
+    rep = _parity.assert_parity(inp, g, SEED)
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tiny_cycle.json")))
+    assert rep["draft"]["near_ties"] == 0
+    assert g["tokens"].tolist() == gold["draft_tokens"]
+    assert g["L"].tolist() == gold["sched_len"]
+    assert g["accept_count"].tolist() == gold["accept_count"]
+    assert g["out_tokens"].tolist() == gold["out_tokens"]
+
+
+def _ragged(bf16, temps, seed_in, B=37, K=5, V=3000, r=48, d=264, **kw):
+    from speculative_decoding_draft_block_gb300.workloads import B256, scaled, make_inputs
+    w = scaled(B256, name="ragged", B=B, K=K, V=V, r=r, d=d, bf16=bf16, temps=temps,
+               seed=seed_in, **kw)
+    return make_inputs(w)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_ragged_multitile_mixed_temperatures(ds, bf16):
+    inp = _ragged(bf16, (0.0, 0.6, 1.0), 7)
+    _, g = _run(inp)
+    rep = _parity.assert_parity(inp, g, SEED)
+    assert rep["draft"]["draws"] == 37 * 5
+
+
+def test_independent_cycle_matches_oracle_cycle(ds):
+    """No teacher forcing: the oracle's own cycle and the GPU's agree end to end."""
+    import oracle
+    inp = _ragged(True, (0.0, 1.0), 11, B=16, K=6, V=4096, r=64, d=128)
+    _, g = _run(inp)
+    o = oracle.cycle(inp, SEED)
+    if np.all(o["draft"]["margin"] > 1e-6):
+        assert np.array_equal(o["draft"]["tokens"], g["tokens"])
+        assert np.array_equal(o["schedule"]["L"], g["L"])
+        assert np.array_equal(o["verify"]["out_tokens"], g["out_tokens"])
+
+
+def test_masked_tokens_never_drawn(ds):
+    inp = _ragged(True, (1.0, 0.6), 13, B=8, K=4, V=2048, r=32, d=64)
+    mask = np.zeros(inp["V"], dtype=bool)
+    mask[::3] = True
+    ninf = np.uint16(0xFF80)                     # bfloat16 -inf
+    inp["base_logits"][:, :, mask] = ninf
+    inp["target_logits"][:, :, mask] = ninf
+    _, g = _run(inp)
+    assert not np.any(mask[g["tokens"]])
+    emitted = g["out_tokens"][g["out_tokens"] >= 0]
+    assert not np.any(mask[emitted])
+    _parity.assert_parity(inp, g, SEED)
+
+
+def test_schedule_modes(ds):
+    from speculative_decoding_draft_block_gb300 import _lib
+    import oracle
+    inp = _ragged(True, (1.0,), 17, B=12, K=5, V=1024, r=32, d=64)
+    _, g = _run(inp, mode=_lib.DS_SCHED_FIXED_K)
+    assert np.all(g["L"] == 5)
+    _parity.assert_parity(inp, g, SEED, check_schedule=False)
+    _, g = _run(inp, mode=_lib.DS_SCHED_THRESHOLD, threshold=0.5)
+    s = oracle.survival(oracle.confidence(inp["h"], inp["E"], inp["anchor"], g["tokens"], inp["w_h"],
+                                          inp["w_e"], inp["conf_bias"], inp["sts_temp"]))
+    want = oracle.schedule(s, inp["sps"], mode=oracle.SCHED_THRESHOLD, threshold=0.5)["L"]
+    assert np.array_equal(g["L"], want)
+    # threshold above every survival: nothing scheduled, bonus from row 1
+    _, g = _run(inp, mode=_lib.DS_SCHED_THRESHOLD, threshold=2.0)
+    assert np.all(g["L"] == 0) and np.all(g["num_emitted"] == 1)
+    _parity.assert_parity(inp, g, SEED, check_schedule=False)
+
+
+def test_minimal_shapes(ds):
+    inp = _ragged(True, (1.0,), 19, B=1, K=1, V=8, r=16, d=8)
+    _, g = _run(inp)
+    _parity.assert_parity(inp, g, SEED)
+
+
+def test_device_errors_are_reported(ds):
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
+    inp = _ragged(True, (1.0,), 23, B=4, K=3, V=512, r=16, d=16)
+    bad = dict(inp)
+    bad["base_logits"] = inp["base_logits"].copy()
+    bad["base_logits"][1, 0, 5] = np.uint16(0x7FC0)          # NaN
+    cyc = DeviceCycle(bad)
+    cyc.reset_status()
+    cyc.run(SEED)
+    assert _lib.ds_check_status(cyc.status) == 7
+    bad = dict(inp)
+    bad["anchor"] = inp["anchor"].copy()
+    bad["anchor"][2] = inp["V"] + 5
+    cyc = DeviceCycle(bad)
+    cyc.reset_status()
+    cyc.run(SEED)
+    assert _lib.ds_check_status(cyc.status) == 6
+    bad = dict(inp)
+    bad["temperature"] = np.array([1.0, -1.0, 1.0, 1.0], dtype=np.float32)
+    cyc = DeviceCycle(bad)
+    cyc.reset_status()
+    cyc.run(SEED)
+    assert _lib.ds_check_status(cyc.status) == 1
+    # the context is still usable: a clean cycle afterwards succeeds
+    _, g = _run(inp)
+    _parity.assert_parity(inp, g, SEED)
+
+
+@pytest.mark.parametrize("name,rows", [
+    ("B32_K8_V151936", None),
+    ("B128_K16_V151936", None),
+    ("B512_K16_V129280", 24),
+    ("B256_K32_V151936", 24),
+])
+def test_full_size_workloads(ds, name, rows):
+    from speculative_decoding_draft_block_gb300.workloads import WORKLOADS, make_inputs
+    inp = make_inputs(WORKLOADS[name])
+    _, g = _run(inp)
+    sel = None
+    if rows is not None:
+        sel = np.linspace(0, inp["B"] - 1, rows).astype(np.int64)
+    rep = _parity.assert_parity(inp, g, SEED, rows=sel)
+    print(name, json.dumps(rep))
