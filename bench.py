@@ -115,6 +115,14 @@ def verify_algorithmic(inp, L, n_final_residual, n_final_bonus):
     return by, 2.0 * n_final_residual * r * V
 
 
+def gpu_launches_per_cycle(w):
+    """Kernels one cycle launches: draft (A-staging prep + tile and locate per
+    position), schedule (confidence, scheduler), verify (rows, finalize, tile,
+    locate). The SIMT draft path (fp32 or r not a multiple of 64) has no prep."""
+    tc = w.bf16 and w.r % 64 == 0 and 64 <= w.r <= 256
+    return (1 if tc else 0) + 2 * w.K + 2 + 4
+
+
 # ---- CPU oracle timing ------------------------------------------------------------
 
 def oracle_sample(inp, seed, n_req):
@@ -336,7 +344,7 @@ def main():
         "mean_sched_len": float(res["L"].mean()), "mean_accepted": float(res["accept_count"].mean()),
         "cycle_roofline_us": cycle_roof_us, "cycle_roofline_frac": cycle_roof_us / (1e3 * cycle_ms.mean()),
         "roofline": roof,
-        "gpu_launches": K * (2 * Kb + 2 + 4),
+        "gpu_launches": K * (gpu_launches_per_cycle(w)),
         "wall_s": wall,
         "clocks": sampler.summary(),
     }

@@ -52,20 +52,36 @@ bool shape_ok(int32_t B, int32_t K, int32_t V, int32_t r) {
 
 ds_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DS_OK : DS_ERR_CUDA; }
 
-size_t draft_ws(int32_t B, int32_t V) {
-  return align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
-}
-
-struct VerifyLayout {
-  size_t vrows, desc, chunks, total;
+// Draft workspace: two record buffers (alternating steps, so a step's records
+// are never overwritten while the previous locate still reads them) and the
+// A-operand staging of the tensor-core path.
+struct DraftLayout {
+  size_t rec0, rec1, astage, total;
 };
 
-VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V) {
+DraftLayout draft_layout(int32_t B, int32_t V, int32_t r) {
+  DraftLayout l;
+  const size_t rec = align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
+  l.rec0 = 0;
+  l.rec1 = rec;
+  l.astage = 2 * rec;
+  l.total = l.astage + align_up(astage_bytes(B, r < 64 ? 64 : r));
+  return l;
+}
+
+size_t draft_ws(int32_t B, int32_t V, int32_t r) { return draft_layout(B, V, r).total; }
+
+struct VerifyLayout {
+  size_t vrows, desc, chunks, astage, total;
+};
+
+VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
   VerifyLayout l;
   l.vrows = 0;
   l.desc = l.vrows + align_up((size_t)B * (K + 1) * sizeof(VRow));
   l.chunks = l.desc + align_up((size_t)B * sizeof(FinalDesc));
-  l.total = l.chunks + align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
+  l.astage = l.chunks + align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
+  l.total = l.astage + align_up(astage_bytes(B, r < 64 ? 64 : r));
   return l;
 }
 
@@ -93,7 +109,7 @@ ds_status ds_philox_fill(const uint32_t* ctr, uint32_t key0, uint32_t key1, uint
 
 size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r) {
   if (!shape_ok(B, K, V, r)) return 0;
-  return draft_ws(B, V);
+  return draft_ws(B, V, r);
 }
 
 ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
@@ -105,7 +121,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
   if (a->workspace == nullptr || !aligned16(a->workspace) ||
-      a->workspace_bytes < draft_ws(a->B, a->V))
+      a->workspace_bytes < draft_ws(a->B, a->V, a->r))
     return DS_ERR_WORKSPACE;
   const ds_status st = device_supported();
   if (st != DS_OK) return st;
@@ -125,16 +141,22 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   p.anchor = a->anchor;
   p.draft_tokens = a->draft_tokens;
   p.temperature = a->temperature;
-  p.chunks = reinterpret_cast<ChunkRec*>(a->workspace);
+  const DraftLayout l = draft_layout(a->B, a->V, a->r);
+  char* ws = reinterpret_cast<char*>(a->workspace);
+  const bool tc = tc_path_supported(a->dtype, a->r);
+  p.astage = tc ? reinterpret_cast<uint8_t*>(ws + l.astage) : nullptr;
   p.seed = a->seed;
   p.tokens_out = a->draft_tokens;
   p.q_token = a->q_token;
   p.q_stats = a->q_stats;
   p.status = a->status;
   const cudaStream_t s = (cudaStream_t)stream;
+  if (tc && launch_draft_prep(a->anchor, a->E, a->B, a->V, a->r, p.astage, a->status, s) != cudaSuccess)
+    return DS_ERR_CUDA;
   for (int k = 1; k <= a->K; ++k) {
     p.step = k;
-    cudaError_t e = launch_sample_tile(p, s);
+    p.chunks = reinterpret_cast<ChunkRec*>(ws + ((k & 1) ? l.rec1 : l.rec0));
+    cudaError_t e = tc ? launch_tile_tc(p, p.astage, s) : launch_sample_tile(p, s);
     if (e != cudaSuccess) return DS_ERR_CUDA;
     e = launch_sample_locate(p, s);
     if (e != cudaSuccess) return DS_ERR_CUDA;
@@ -198,7 +220,7 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
 
 size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r) {
   if (!shape_ok(B, K, V, r)) return 0;
-  return verify_layout(B, K, V).total;
+  return verify_layout(B, K, V, r).total;
 }
 
 ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
@@ -211,7 +233,8 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
                         a->status};
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
-  const VerifyLayout l = verify_layout(a->B, a->K, a->V);
+  const VerifyLayout l = verify_layout(a->B, a->K, a->V, a->r);
+  const bool tc = tc_path_supported(a->dtype, a->r);
   if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < l.total)
     return DS_ERR_WORKSPACE;
   const ds_status st = device_supported();
@@ -226,6 +249,8 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   v.n_chunks = num_chunks(a->V);
   v.dtype = a->dtype;
   v.target_logits = a->target_logits;
+  v.E = a->E;
+  v.astage = tc ? reinterpret_cast<uint8_t*>(ws + l.astage) : nullptr;
   v.anchor = a->anchor;
   v.draft_tokens = a->draft_tokens;
   v.q_token = a->q_token;
@@ -261,10 +286,12 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   p.temperature = a->temperature;
   p.final_desc = v.final_desc;
   p.chunks = reinterpret_cast<ChunkRec*>(ws + l.chunks);
+  p.astage = nullptr;
   p.seed = a->seed;
   p.tokens_out = a->out_tokens;
   p.status = a->status;
-  if (launch_sample_tile(p, s) != cudaSuccess) return DS_ERR_CUDA;
+  if ((tc ? launch_tile_tc(p, v.astage, s) : launch_sample_tile(p, s)) != cudaSuccess)
+    return DS_ERR_CUDA;
   if (launch_sample_locate(p, s) != cudaSuccess) return DS_ERR_CUDA;
   return DS_OK;
 }

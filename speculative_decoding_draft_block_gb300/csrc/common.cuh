@@ -119,24 +119,31 @@ __device__ __forceinline__ Gscale make_gscale(float T) {
   return {hi, (float)(g - (double)hi)};
 }
 
-// t = (z + b) * g  as  k + f  with k integral (float), |f| <~ 0.5 + |b g|.
-__device__ __forceinline__ void exp2_split(float z, float b, Gscale g, float& k, float& f) {
-  const float a = __fmul_rn(z, g.hi);
-  const float ae = __fmaf_rn(z, g.hi, -a);  // z*g.hi - a, exact
-  float tl = __fmaf_rn(z, g.lo, ae);
-  tl = __fmaf_rn(b, g.hi, tl);
-  k = rintf(a);
-  f = __fadd_rn(__fsub_rn(a, k), tl);  // a - k is exact
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
-// 2^(t - n) for t = (z + b) * g; 0 when z is -inf or the result is below 2^-140.
-__device__ __forceinline__ float exp2_rel(float z, float b, Gscale g, int n) {
-  if (z == kNegInf) return 0.f;
-  float k, f;
-  exp2_split(z, b, g, k, f);
-  const int e = (int)k - n;
-  if (e < -140) return 0.f;
-  return ldexpf(exp2f(f), e);
+// 2^(t - n) for t = (z + b) * g and an integer reference n >= rint(z * g.hi).
+//   a = z*g.hi is split exactly from the product (FMA), the small terms
+//   z*g.lo and b*g.hi are folded into the fraction, k = rint(a) comes from the
+//   1.5*2^23 rounding trick (valid for |a| < 2^22), f = (a - k) + small lies
+//   within ~[-0.5 - |b g|, 0.5 + |b g|], and 2^(k - n) is built in the exponent
+//   field (flushed to 0 below 2^-126). z = -inf gives 0; NaN and +inf give NaN.
+__device__ __forceinline__ float weight_rel(float z, float b, Gscale g, int n) {
+  const float a = __fmul_rn(z, g.hi);
+  const float ae = __fmaf_rn(z, g.hi, -a);
+  float tl = __fmaf_rn(z, g.lo, ae);
+  tl = __fmaf_rn(b, g.hi, tl);
+  const float m = __fadd_rn(a, 12582912.f);
+  const float kf = __fsub_rn(m, 12582912.f);
+  const float f = __fadd_rn(__fsub_rn(a, kf), tl);
+  const float p = ex2_approx(f);
+  int e = (__float_as_int(m) - 0x4B400000) - n;
+  e = max(e, -127);
+  const float w = __fmul_rn(p, __int_as_float((e + 127) << 23));
+  return z == kNegInf ? 0.f : w;
 }
 
 // Chunk reference: rint of the largest z*g.hi among finite entries.

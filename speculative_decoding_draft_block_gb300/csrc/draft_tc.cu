@@ -1,0 +1,530 @@
+// Tensor-core tile kernel of the draft step and of the verify's final draw.
+//
+// DSpark summary page, 방법론 › 반자기회귀 생성: the Markov head's bias for a
+// block position is E[x_{k-1}] . P for every request at once -- a
+// [B x r] x [r x V] product -- and the position is then sampled from
+// softmax((z_k + bias) / T). This kernel computes that product on the 5th-gen
+// tensor cores and reduces it straight out of TMEM:
+//
+//   warp 0      producer: TMA loads of P tiles (r x 128 tokens, 128B-swizzled,
+//               MN-major, L2 evict-last: P is re-read every step) and of the
+//               base-logit tiles (128 rows x 128 tokens, evict-first), and one
+//               bulk copy of the A operand (E rows of the previous tokens,
+//               pre-swizzled by the previous locate kernel).
+//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> f32),
+//               M = 128 requests, N = 128 tokens, K = r in steps of 16, into one
+//               of two TMEM accumulators (double-buffered against the epilogue).
+//   warps 2-17  epilogue: tcgen05.ld of a 32-lane x 32-column slice each, add
+//               the base logits from shared memory, and reduce every
+//               (request, 32-token chunk) to its record: the double-float sum
+//               of 2^(t - ref) with an integer reference (sampling rows), or
+//               its largest logit (greedy rows). Nothing V-wide is stored.
+//
+// Tiles (M-tile of 128 requests, N-tile of 128 tokens) are split into
+// contiguous ranges, one range per CTA, one CTA per SM. Consecutive steps are
+// chained with programmatic dependent launch; every mbarrier wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sampling.cuh"
+#include "sm100.cuh"
+
+namespace ds {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kTcThreads = 576;  // 18 warps
+constexpr int kEpiWarps = 16;
+constexpr int kTileN = 128;
+constexpr int kPStages = 4;
+constexpr uint32_t kASize = 65536;   // up to r = 256
+constexpr uint32_t kPStage = 16384;  // 64 k-rows x 128 tokens
+constexpr uint32_t kZStage = 32768;  // 128 rows x 128 tokens
+constexpr uint32_t kOffP = kASize;
+constexpr uint32_t kOffZ = kOffP + kPStages * kPStage;
+constexpr uint32_t kSmemBytes = kOffZ + 2 * kZStage + 1024;
+constexpr uint32_t kTmemCols = 256;
+
+struct TcParams {
+  SampleParams sp;
+  const uint8_t* astage;
+  int32_t n_mt, n_nt, nkb, tiles;
+};
+
+struct Shared {
+  uint64_t a_full, a_empty;
+  uint64_t p_full[kPStages], p_empty[kPStages];
+  uint64_t z_full[2], z_empty[2];
+  uint64_t t_full[2], t_empty[2];
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int32_t* status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  report(status, kErrTimeout);
+  return false;
+}
+
+// What the epilogue keeps about its row (a trimmed RowCtx, to save registers).
+struct EpiRow {
+  int32_t mode;
+  Gscale g;
+  int32_t Np, Nq;
+  float Rhi, Rlo;
+};
+
+// Reduce this thread's (row, 32-token chunk) slice of a finished accumulator.
+// The bias is read from TMEM in two 16-column halves (tcgen05.ld is
+// warp-collective, so every lane loads even when its row has nothing to do).
+template <bool FULL>
+__device__ __forceinline__ void epi_chunk(const EpiRow& c, bool active, const uint32_t* zp,
+                                          const uint32_t* tp, uint32_t taddr, int n, int col0,
+                                          ChunkRec& rec, bool& bad) {
+  const Bf16Src z{zp}, t{tp};
+  int ref = 0;
+  if (active && c.mode == kSampleMarkov) {
+    float amax = kNegInf;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (FULL || j < n) amax = fmaxf(amax, scaled_hi(z(j), c.g));
+    ref = chunk_ref_from_max(amax);
+  }
+  DF s = {0.f, 0.f};
+  DF best = {kNegInf, 0.f};
+  int bi = -1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float bh[16];
+    tmem_ld16(taddr + h * 16, bh);
+    if (!active) continue;
+    if (c.mode == kSampleMarkov) {
+      if (ref != kEmptyRef) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (FULL || h * 16 + j < n) df_accumulate(s, weight_rel(z(h * 16 + j), bh[j], c.g, ref));
+      }
+    } else if (c.mode == kGreedyMarkov) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int jj = h * 16 + j;
+        if (FULL || jj < n) {
+          const float zj = z(jj);
+          bad |= bad_logit(zj) || !(bh[j] == bh[j]);
+          const DF l = (zj == kNegInf) ? DF{kNegInf, 0.f} : two_sum(zj, bh[j]);
+          if (bi < 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
+            best = l;
+            bi = col0 + jj;
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int jj = h * 16 + j;
+        if (FULL || jj < n) {
+          float w = weight_rel(t(jj), 0.f, c.g, c.Np);
+          if (c.mode == kResidual) {
+            const float wq = weight_rel(z(jj), bh[j], c.g, c.Nq);
+            float d = __fmaf_rn(-wq, c.Rhi, w);
+            d = __fmaf_rn(-wq, c.Rlo, d);
+            bad |= !(d == d);
+            w = fmaxf(d, 0.f);
+          }
+          df_accumulate(s, w);
+        }
+      }
+    }
+  }
+  rec.idx = -1;
+  if (c.mode == kGreedyMarkov) {
+    rec.hi = best.hi;
+    rec.lo = best.lo;
+    rec.ref = 0;
+    rec.idx = bi;
+  } else {
+    if (c.mode == kSampleMarkov && ref == kEmptyRef) {
+      bool any_nan = false;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (FULL || j < n) any_nan |= !(z(j) == z(j));
+      bad |= any_nan;
+    }
+    bad |= !isfinite(s.hi);
+    rec.hi = s.hi;
+    rec.lo = s.lo;
+    rec.ref = (c.mode == kSampleMarkov) ? ref : 0;
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tile_tc_kernel(const TcParams prm, const __grid_constant__ CUtensorMap tmP,
+                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmT) {
+  extern __shared__ uint8_t raw[];
+  __shared__ Shared sh;
+  const SampleParams& sp = prm.sp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base_addr = smem_u32(raw);
+  uint8_t* smem = raw + (((base_addr + 1023u) & ~1023u) - base_addr);
+  uint8_t* sA = smem;
+  uint8_t* sP = smem + kOffP;
+  uint8_t* sZ = smem + kOffZ;
+  const bool draft = (sp.src == 0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.a_full, 1);
+    mbar_init(&sh.a_empty, 1);
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(&sh.p_full[i], 1);
+      mbar_init(&sh.p_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.z_full[i], 1);
+      mbar_init(&sh.z_empty[i], kEpiWarps);
+      mbar_init(&sh.t_full[i], 1);
+      mbar_init(&sh.t_empty[i], kEpiWarps);
+    }
+    sh.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sh.tmem_slot, kTmemCols);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_slot;
+  pdl_launch_dependents();
+
+  const int G = gridDim.x;
+  const int t0 = (int)((long long)blockIdx.x * prm.tiles / G);
+  const int t1 = (int)((long long)(blockIdx.x + 1) * prm.tiles / G);
+  volatile int* abort_flag = &sh.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_p = policy_evict_last();
+    const uint64_t pol_z = policy_evict_first();
+    if (lane == 0) {
+      prefetch_tmap(&tmP);
+      prefetch_tmap(&tmZ);
+      if (!draft) prefetch_tmap(&tmT);
+    }
+    int cur_mt = -1;
+    uint32_t a_uses = 0, pc = 0;
+    bool waited = false;
+    for (int t = t0, i = 0; t < t1; ++t, ++i) {
+      const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
+      const int n0 = nt * kTileN;
+      bool ok = true;
+      for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
+        const uint32_t ps = pc % kPStages, ph = ((pc / kPStages) & 1) ^ 1;
+        if (lane == 0) {
+          ok = wait_bar(&sh.p_empty[ps], ph, abort_flag, sp.status);
+          if (ok) {
+            mbar_expect_tx(&sh.p_full[ps], kPStage);
+            tma_load_2d(sP + ps * kPStage, &tmP, &sh.p_full[ps], n0, c * 64, pol_p);
+            tma_load_2d(sP + ps * kPStage + 8192, &tmP, &sh.p_full[ps], n0 + 64, c * 64, pol_p);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      if (!ok) break;
+      if (!waited) {
+        pdl_wait();  // A staging, draft tokens and final descriptors come from earlier kernels
+        waited = true;
+      }
+      if (mt != cur_mt) {
+        if (lane == 0) {
+          if (cur_mt >= 0) ok = wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status);
+          if (ok) {
+            mbar_expect_tx(&sh.a_full, prm.nkb * 16384);
+            bulk_load(sA, prm.astage + (size_t)mt * prm.nkb * 16384, prm.nkb * 16384, &sh.a_full);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++a_uses;
+        cur_mt = mt;
+      }
+      if (draft) {
+        const uint32_t zs = i & 1, ph = ((i >> 1) & 1) ^ 1;
+        if (lane == 0) {
+          ok = wait_bar(&sh.z_empty[zs], ph, abort_flag, sp.status);
+          if (ok) {
+            mbar_expect_tx(&sh.z_full[zs], kZStage);
+            tma_load_3d(sZ + zs * kZStage, &tmZ, &sh.z_full[zs], n0, sp.step - 1, mt * 128, pol_z);
+            tma_load_3d(sZ + zs * kZStage + 16384, &tmZ, &sh.z_full[zs], n0 + 64, sp.step - 1,
+                        mt * 128, pol_z);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      } else {
+        // final draw: gather each request's own base / target row (one 128-byte box per row)
+        const uint32_t ph = (i & 1) ^ 1;
+        if (lane == 0) ok = wait_bar(&sh.z_empty[0], ph, abort_flag, sp.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        uint32_t bytes = 0;
+        int rows_z[4], rows_t[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rr = lane + 32 * u, b = mt * 128 + rr;
+          rows_z[u] = rows_t[u] = -1;
+          if (b < sp.B && sp.temperature[b] != 0.f) {
+            const FinalDesc d = sp.final_desc[b];
+            if (d.mode == kResidual) rows_z[u] = d.row;
+            if (d.mode == kResidual || d.mode == kBonus) rows_t[u] = d.row;
+          }
+          bytes += (rows_z[u] >= 0 ? 256u : 0u) + (rows_t[u] >= 0 ? 256u : 0u);
+        }
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        if (lane == 0) {
+          if (bytes)
+            mbar_expect_tx(&sh.z_full[0], bytes);
+          else
+            mbar_arrive(&sh.z_full[0]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rr = lane + 32 * u, b = mt * 128 + rr;
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            if (rows_z[u] >= 0)
+              tma_load_3d(sZ + nb * 16384 + rr * 128, &tmZ, &sh.z_full[0], n0 + nb * 64, rows_z[u], b,
+                          pol_z);
+            if (rows_t[u] >= 0)
+              tma_load_3d(sZ + kZStage + nb * 16384 + rr * 128, &tmT, &sh.z_full[0], n0 + nb * 64,
+                          rows_t[u], b, pol_z);
+          }
+        }
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, kTileN, false, true);
+      const uint64_t abits = smem_desc_bits(16, 1024, 2);
+      const uint64_t bbits = smem_desc_bits(8192, 1024, 2);
+      int cur_mt = -1;
+      uint32_t a_uses = 0, pc = 0;
+      bool ok = true;
+      for (int t = t0, i = 0; t < t1 && ok; ++t, ++i) {
+        const int mt = t / prm.n_nt;
+        if (mt != cur_mt) {
+          if (cur_mt >= 0) mma_commit(&sh.a_empty);
+          ok = wait_bar(&sh.a_full, a_uses & 1, abort_flag, sp.status);
+          if (!ok) break;
+          ++a_uses;
+          cur_mt = mt;
+          tc_fence_after();
+        }
+        const uint32_t buf = i & 1;
+        ok = wait_bar(&sh.t_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, sp.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kTileN;
+        for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
+          const uint32_t ps = pc % kPStages;
+          ok = wait_bar(&sh.p_full[ps], (pc / kPStages) & 1, abort_flag, sp.status);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(sA + c * 16384 + kk * 32, abits);
+            const uint64_t bd = smem_desc(sP + ps * kPStage + kk * 2048, bbits);
+            mma_bf16(d, ad, bd, idesc, (c | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&sh.p_empty[ps]);
+        }
+        if (ok) mma_commit(&sh.t_full[buf]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();
+    const int ew = warp - 2, q = warp & 3, cg = ew >> 2;
+    const int r_local = q * 32 + lane;
+    int cur_mt = -1;
+    EpiRow c;
+    c.mode = kSkip;
+    bool bad = false;
+    for (int t = t0, i = 0; t < t1; ++t, ++i) {
+      const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
+      const int row = mt * 128 + r_local;
+      if (mt != cur_mt) {
+        const RowCtx rc = make_row_ctx<__nv_bfloat16>(sp, row);
+        c.mode = rc.mode;
+        c.g = rc.g;
+        c.Np = rc.Np;
+        c.Nq = rc.Nq;
+        c.Rhi = rc.Rhi;
+        c.Rlo = rc.Rlo;
+        cur_mt = mt;
+      }
+      const uint32_t buf = i & 1;
+      const uint32_t zs = draft ? (i & 1) : 0;
+      const uint32_t zph = draft ? ((i >> 1) & 1) : (i & 1);
+      if (!wait_bar(&sh.z_full[zs], zph, abort_flag, sp.status)) break;
+      if (!wait_bar(&sh.t_full[buf], (i >> 1) & 1, abort_flag, sp.status)) break;
+      tc_fence_after();
+      uint32_t zp[16], tp[16];
+      const int nb = cg >> 1, ch0 = (cg & 1) * 4;
+      const bool need_z = (c.mode == kGreedyMarkov || c.mode == kSampleMarkov || c.mode == kResidual);
+      const bool need_t = (c.mode == kResidual || c.mode == kBonus);
+      if (need_z) {
+        const uint8_t* zb = sZ + zs * kZStage + nb * 16384 + r_local * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4*>(zb + (((ch0 + u) ^ (r_local & 7)) << 4));
+          zp[4 * u] = v.x;
+          zp[4 * u + 1] = v.y;
+          zp[4 * u + 2] = v.z;
+          zp[4 * u + 3] = v.w;
+        }
+      }
+      if (need_t) {
+        const uint8_t* tb = sZ + kZStage + nb * 16384 + r_local * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4*>(tb + (((ch0 + u) ^ (r_local & 7)) << 4));
+          tp[4 * u] = v.x;
+          tp[4 * u + 1] = v.y;
+          tp[4 * u + 2] = v.z;
+          tp[4 * u + 3] = v.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.z_empty[zs]);
+      const int col0 = nt * kTileN + cg * 32;
+      const bool active = row < sp.B && c.mode != kSkip && col0 < sp.V;
+      const int n = min(32, sp.V - col0);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kTileN + cg * 32;
+      ChunkRec rec;
+      if (n >= 32)
+        epi_chunk<true>(c, active, zp, tp, taddr, 32, col0, rec, bad);
+      else
+        epi_chunk<false>(c, active, zp, tp, taddr, n, col0, rec, bad);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
+      if (active) sp.chunks[(size_t)row * sp.n_chunks + (col0 >> 5)] = rec;
+    }
+    if (bad) report(sp.status, kErrNonfinite);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = get_encoder();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+bool tc_path_supported(int32_t dtype, int32_t r) {
+  return dtype == DS_BF16 && r % 64 == 0 && r >= 64 && r <= 256;
+}
+
+size_t astage_bytes(int32_t B, int32_t r) {
+  const size_t n_mt = (B + 127) / 128;
+  return n_mt * (size_t)(r / 64) * 16384;
+}
+
+cudaError_t launch_tile_tc(const SampleParams& p, const uint8_t* astage, cudaStream_t s) {
+  static cudaError_t attr = cudaFuncSetAttribute(
+      tile_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (attr != cudaSuccess) return attr;
+  TcParams prm;
+  prm.sp = p;
+  prm.astage = astage;
+  prm.n_mt = (p.B + 127) / 128;
+  prm.n_nt = (p.V + kTileN - 1) / kTileN;
+  prm.nkb = p.r / 64;
+  prm.tiles = prm.n_mt * prm.n_nt;
+
+  CUtensorMap mP, mZ, mT;
+  const cuuint64_t V = (cuuint64_t)p.V;
+  {
+    const cuuint64_t dims[2] = {V, (cuuint64_t)p.r};
+    const cuuint64_t str[1] = {V * 2};
+    const cuuint32_t box[2] = {64, 64};
+    if (!encode(&mP, p.P, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {V, (cuuint64_t)p.K, (cuuint64_t)p.B};
+    const cuuint64_t str[2] = {V * 2, V * 2 * (cuuint64_t)p.K};
+    const cuuint32_t box_draft[3] = {64, 1, 128};
+    const cuuint32_t box_row[3] = {64, 1, 1};
+    if (!encode(&mZ, p.base_logits, 3, dims, str, p.src == 0 ? box_draft : box_row))
+      return cudaErrorInvalidValue;
+  }
+  if (p.src == 0) {
+    mT = mZ;
+  } else {
+    const cuuint64_t dims[3] = {V, (cuuint64_t)(p.K + 1), (cuuint64_t)p.B};
+    const cuuint64_t str[2] = {V * 2, V * 2 * (cuuint64_t)(p.K + 1)};
+    const cuuint32_t box[3] = {64, 1, 1};
+    if (!encode(&mT, p.target_logits, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  static int sms = num_sms();
+  const int grid = prm.tiles < sms ? prm.tiles : sms;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tile_tc_kernel, prm, mP, mZ, mT);
+}
+
+}  // namespace ds

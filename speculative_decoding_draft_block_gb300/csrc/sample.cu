@@ -27,6 +27,8 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sampling.cuh"
+#include "sm100.cuh"
 
 namespace ds {
 
@@ -34,160 +36,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kPsStride = 8 * 36;  // 8 chunks of 32 floats padded to 36 (bank spread)
-
-// Everything a kernel needs to know about one row of the batch being sampled.
-struct RowCtx {
-  int32_t mode;
-  int32_t a_token;  // E row of the bias; -1 when the row needs no bias
-  const void* zrow;
-  const void* trow;
-  Gscale g;
-  int32_t Np, Nq;
-  float Rhi, Rlo;
-  uint32_t upos, ustage;  // Philox position and stage of the row's draw
-  int32_t out_index;      // flat index of the drawn token in tokens_out
-};
-
-template <typename Tin>
-__device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
-  RowCtx c;
-  c.mode = kSkip;
-  c.a_token = -1;
-  c.zrow = nullptr;
-  c.trow = nullptr;
-  c.g = {0.f, 0.f};
-  c.Np = c.Nq = 0;
-  c.Rhi = c.Rlo = 0.f;
-  c.upos = 0;
-  c.ustage = 0;
-  c.out_index = 0;
-  if (b >= p.B) return c;
-  const Tin* base = reinterpret_cast<const Tin*>(p.base_logits);
-  const Tin* tgt = reinterpret_cast<const Tin*>(p.target_logits);
-  const float T = p.temperature[b];
-  const bool greedy = (T == 0.f);
-  if (!greedy && !(T >= 1e-3f && T <= 1e3f)) {
-    report(p.status, kErrInvalidArg);
-    return c;
-  }
-  if (!greedy) c.g = make_gscale(T);
-  if (p.src == 0) {
-    const int k = p.step;  // 1-based
-    int tok = (k == 1) ? p.anchor[b] : p.draft_tokens[(size_t)b * p.K + (k - 2)];
-    if (tok < 0 || tok >= p.V) {
-      report(p.status, kErrBounds);
-      tok = 0;
-    }
-    c.a_token = tok;
-    c.mode = greedy ? kGreedyMarkov : kSampleMarkov;
-    c.zrow = base + ((size_t)b * p.K + (k - 1)) * (size_t)p.V;
-    c.upos = (uint32_t)k;
-    c.ustage = DS_STAGE_DRAFT;
-    c.out_index = b * p.K + (k - 1);
-  } else {
-    const FinalDesc d = p.final_desc[b];
-    if (greedy || d.mode == kSkip) return c;
-    c.mode = d.mode;
-    c.trow = tgt + ((size_t)b * (p.K + 1) + d.row) * (size_t)p.V;
-    c.Np = d.Np;
-    c.upos = (uint32_t)(d.row + 1);
-    c.ustage = DS_STAGE_RESAMPLE;
-    c.out_index = b * (p.K + 1) + d.out_pos;
-    if (d.mode == kResidual) {
-      int tok = d.a_token;
-      if (tok < 0 || tok >= p.V) {
-        report(p.status, kErrBounds);
-        tok = 0;
-      }
-      c.a_token = tok;
-      c.zrow = base + ((size_t)b * p.K + d.row) * (size_t)p.V;
-      c.Nq = d.Nq;
-      c.Rhi = d.Rhi;
-      c.Rlo = d.Rlo;
-    }
-  }
-  return c;
-}
-
-// Reduce one chunk of n (<= 32) tokens starting at token col0 to its record.
-// z, bias, t hold the chunk's base logits, Markov bias and target logits.
-// If w_out is given, the per-token weights (relative to rec.ref) and the
-// running double-float prefix after each token are written too.
-__device__ __forceinline__ void chunk_record(const RowCtx& c, const float* z, const float* bias,
-                                             const float* t, int n, int col0, ChunkRec& rec,
-                                             int32_t* status, float* w_out = nullptr,
-                                             DF* prefix_out = nullptr) {
-  rec.hi = 0.f;
-  rec.lo = 0.f;
-  rec.ref = 0;
-  rec.idx = -1;
-  bool bad = false;
-  if (c.mode == kGreedyMarkov) {
-    DF best = {kNegInf, 0.f};
-    int bi = -1;
-    for (int j = 0; j < n; ++j) {
-      bad |= bad_logit(z[j]) || !(bias[j] == bias[j]);
-      DF l = (z[j] == kNegInf) ? DF{kNegInf, 0.f} : two_sum(z[j], bias[j]);
-      if (bi < 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
-        best = l;
-        bi = col0 + j;
-      }
-    }
-    rec.hi = best.hi;
-    rec.lo = best.lo;
-    rec.idx = bi;
-  } else if (c.mode == kSampleMarkov) {
-    float amax = kNegInf;
-    for (int j = 0; j < n; ++j) {
-      bad |= bad_logit(z[j]) || !(bias[j] == bias[j]);
-      if (z[j] != kNegInf) amax = fmaxf(amax, scaled_hi(z[j], c.g));
-    }
-    if (amax == kNegInf) {
-      rec.ref = kEmptyRef;
-      if (w_out)
-        for (int j = 0; j < n; ++j) {
-          w_out[j] = 0.f;
-          prefix_out[j] = {0.f, 0.f};
-        }
-    } else {
-      const int ref = (int)rintf(amax);
-      DF s = {0.f, 0.f};
-      for (int j = 0; j < n; ++j) {
-        const float w = exp2_rel(z[j], bias[j], c.g, ref);
-        df_accumulate(s, w);
-        if (w_out) {
-          w_out[j] = w;
-          prefix_out[j] = s;
-        }
-      }
-      rec.hi = s.hi;
-      rec.lo = s.lo;
-      rec.ref = ref;
-    }
-  } else {  // kResidual / kBonus: weights on the row's global scale
-    DF s = {0.f, 0.f};
-    for (int j = 0; j < n; ++j) {
-      bad |= bad_logit(t[j]);
-      float w = exp2_rel(t[j], 0.f, c.g, c.Np);
-      if (c.mode == kResidual) {
-        bad |= bad_logit(z[j]) || !(bias[j] == bias[j]);
-        const float wq = exp2_rel(z[j], bias[j], c.g, c.Nq);
-        float d = __fmaf_rn(-wq, c.Rhi, w);
-        d = __fmaf_rn(-wq, c.Rlo, d);
-        w = fmaxf(d, 0.f);
-      }
-      df_accumulate(s, w);
-      if (w_out) {
-        w_out[j] = w;
-        prefix_out[j] = s;
-      }
-    }
-    rec.hi = s.hi;
-    rec.lo = s.lo;
-    rec.ref = 0;
-  }
-  if (bad) report(status, kErrNonfinite);
-}
 
 template <typename Tin>
 __device__ __forceinline__ void load_chunk(const void* row, int col0, int n, float* out) {
@@ -214,6 +62,8 @@ __global__ void __launch_bounds__(kThreads) sample_tile_kernel(SampleParams p) {
   const Tin* E = reinterpret_cast<const Tin*>(p.E);
   const Tin* P = reinterpret_cast<const Tin*>(p.P);
 
+  sm100::pdl_launch_dependents();
+  sm100::pdl_wait();
   if (tid == 0) any_bias = 0;
   __syncthreads();
   if (tid < kTileRows) {
@@ -269,135 +119,171 @@ __global__ void __launch_bounds__(kThreads) sample_tile_kernel(SampleParams p) {
   if (c.zrow) load_chunk<Tin>(c.zrow, col0, n, z);
   if (c.trow) load_chunk<Tin>(c.trow, col0, n, t);
   ChunkRec rec;
-  chunk_record(c, z, acc, t, n, col0, rec, p.status);
+  if (n == 32)
+    chunk_record<true>(c, F32Src{z}, acc, F32Src{t}, 32, col0, rec, p.status);
+  else
+    chunk_record<false>(c, F32Src{z}, acc, F32Src{t}, n, col0, rec, p.status);
   p.chunks[(size_t)row * p.n_chunks + chunk] = rec;
 }
 
-// ---- block helpers --------------------------------------------------------
+// ---- locate ------------------------------------------------------------------
 
-__device__ __forceinline__ int block_max_int(int v, int* red) {
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) red[w] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : INT_MIN;
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (threadIdx.x == 0) red[0] = v;
-  }
-  __syncthreads();
-  return red[0];
+__device__ __forceinline__ DF shfl_up_df(DF v, int o) {
+  return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }
 
-__device__ __forceinline__ int block_min_int(int v, int* red) {
-  return -block_max_int(-v, red);
+__device__ __forceinline__ DF scaled_rec(const ChunkRec& r, int N) {
+  const int e = (r.ref == kEmptyRef) ? -300 : max(r.ref - N, -300);
+  return df_scale2(DF{r.hi, r.lo}, e);
 }
 
+// One CTA per row: combine the row's chunk records, locate the chunk where the
+// CDF crosses u*S, recompute its 32 weights and pick the token. In draft mode
+// it also stages E[x_k] as the next step's tensor-core A operand.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p) {
-  __shared__ int red[32];
-  __shared__ DF tot_s[kThreads];
-  __shared__ DF excl_s[kThreads];
-  __shared__ float arow[1024];
-  __shared__ float zs[32], bs[32], ts[32];
-  __shared__ int found_s;
-  __shared__ DF found_excl;
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x;
+  extern __shared__ ChunkRec srec[];
+  __shared__ int s_int[kThreads / 32];
+  __shared__ DF s_df[kThreads / 32];
+  __shared__ float s_arow[1024];
+  __shared__ float s_part[kThreads / 32][32];
+  __shared__ float s_z[32], s_b[32], s_t[32], s_w[32];
+  __shared__ int s_found, s_ref;
+  __shared__ DF s_excl;
+  sm100::pdl_launch_dependents();
+  sm100::pdl_wait();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const RowCtx c = make_row_ctx<Tin>(p, b);
-  if (c.mode == kSkip) return;
-  const ChunkRec* rec = p.chunks + (size_t)b * p.n_chunks;
+  const bool stage_next = (p.src == 0) && (p.astage != nullptr) && (p.step < p.K);
+  if (c.mode == kSkip) {
+    if (stage_next && wid == 0)
+      write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, 0, lane);
+    return;
+  }
   const int nc = p.n_chunks;
+  const ChunkRec* rec = p.chunks + (size_t)b * nc;
+  for (int i = tid; i < nc; i += kThreads) srec[i] = rec[i];
+  __syncthreads();
   const int seg = (nc + kThreads - 1) / kThreads;
   const int c0 = min(nc, tid * seg), c1 = min(nc, c0 + seg);
 
   if (c.mode == kGreedyMarkov) {
-    // argmax over chunk records, lowest token on ties
     DF best = {kNegInf, 0.f};
     int bi = INT_MAX;
     for (int i = c0; i < c1; ++i) {
-      const ChunkRec r = rec[i];
+      const ChunkRec r = srec[i];
+      if (r.idx < 0) continue;
       if (bi == INT_MAX || r.hi > best.hi || (r.hi == best.hi && r.lo > best.lo)) {
         best = {r.hi, r.lo};
         bi = r.idx;
       }
     }
-    tot_s[tid] = best;
-    red[0] = 0;
-    __shared__ int idx_s[kThreads];
-    idx_s[tid] = bi;
+    for (int o = 16; o > 0; o >>= 1) {
+      const DF ov = {__shfl_xor_sync(0xffffffffu, best.hi, o), __shfl_xor_sync(0xffffffffu, best.lo, o)};
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const bool take = (oi != INT_MAX) &&
+                        (bi == INT_MAX || ov.hi > best.hi || (ov.hi == best.hi && ov.lo > best.lo) ||
+                         (ov.hi == best.hi && ov.lo == best.lo && oi < bi));
+      if (take) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      s_df[wid] = best;
+      s_int[wid] = bi;
+    }
     __syncthreads();
-    if (tid == 0) {
+    if (wid == 0) {
       DF bb = {kNegInf, 0.f};
       int bx = INT_MAX;
-      for (int i = 0; i < kThreads; ++i) {
-        if (idx_s[i] == INT_MAX) continue;
-        const DF v = tot_s[i];
+      for (int w = 0; w < kThreads / 32; ++w) {
+        const DF v = s_df[w];
+        const int iw = s_int[w];
+        if (iw == INT_MAX) continue;
         if (bx == INT_MAX || v.hi > bb.hi || (v.hi == bb.hi && v.lo > bb.lo) ||
-            (v.hi == bb.hi && v.lo == bb.lo && idx_s[i] < bx)) {
+            (v.hi == bb.hi && v.lo == bb.lo && iw < bx)) {
           bb = v;
-          bx = idx_s[i];
+          bx = iw;
         }
       }
-      if (bx == INT_MAX || bx < 0) bx = 0;
-      p.tokens_out[c.out_index] = bx;
-      if (p.src == 0) {
-        p.q_token[c.out_index] = 1.f;
-        ds_row_stats st;
-        st.sum_hi = 1.f;
-        st.sum_lo = 0.f;
-        st.ref = 0;
-        st.argmax = bx;
-        p.q_stats[c.out_index] = st;
+      if (bx == INT_MAX) {
+        bx = 0;
+        if (lane == 0) report(p.status, kErrNonfinite);
       }
+      if (lane == 0) {
+        p.tokens_out[c.out_index] = bx;
+        if (p.src == 0) {
+          p.q_token[c.out_index] = 1.f;
+          ds_row_stats st;
+          st.sum_hi = 1.f;
+          st.sum_lo = 0.f;
+          st.ref = 0;
+          st.argmax = bx;
+          p.q_stats[c.out_index] = st;
+        }
+      }
+      if (stage_next)
+        write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, bx, lane);
     }
     return;
   }
 
-  // ---- sampling rows: global reference, prefix sums, crossing chunk ----
-  int local_max = INT_MIN;
+  // ---- sampling rows ----
+  int lm = INT_MIN;
   if (c.mode == kSampleMarkov)
-    for (int i = c0; i < c1; ++i) local_max = max(local_max, rec[i].ref);
-  const int N = (c.mode == kSampleMarkov) ? block_max_int(local_max, red) : 0;
-
+    for (int i = c0; i < c1; ++i) lm = max(lm, srec[i].ref);
+  for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, o));
+  if (lane == 0) s_int[wid] = lm;
+  __syncthreads();
+  int N = 0;
+  if (c.mode == kSampleMarkov) {
+    N = s_int[0];
+    for (int w = 1; w < kThreads / 32; ++w) N = max(N, s_int[w]);
+  }
   DF tot = {0.f, 0.f};
-  for (int i = c0; i < c1; ++i) {
-    const ChunkRec r = rec[i];
-    const int e = (r.ref == kEmptyRef) ? -1000 : r.ref - N;
-    tot = df_add(tot, df_scale2(DF{r.hi, r.lo}, max(e, -300)));
+  for (int i = c0; i < c1; ++i) tot = df_add(tot, scaled_rec(srec[i], N));
+  // block exclusive scan of the per-thread totals (fixed tree order)
+  DF inc = tot;
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF v = shfl_up_df(inc, o);
+    if (lane >= o) inc = df_add(v, inc);
   }
-  tot_s[tid] = tot;
+  DF prev = shfl_up_df(inc, 1);
+  if (lane == 0) prev = DF{0.f, 0.f};
   __syncthreads();
-  if (tid == 0) {
-    DF run = {0.f, 0.f};
-    for (int i = 0; i < kThreads; ++i) {
-      excl_s[i] = run;
-      run = df_add(run, tot_s[i]);
+  if (lane == 31) s_df[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    DF wv = lane < kThreads / 32 ? s_df[lane] : DF{0.f, 0.f};
+    for (int o = 1; o < 32; o <<= 1) {
+      const DF v = shfl_up_df(wv, o);
+      if (lane >= o) wv = df_add(v, wv);
     }
-    tot_s[0] = run;  // total S
-    found_s = INT_MAX;
+    if (lane < kThreads / 32) s_df[lane] = wv;
+    if (lane == 0) s_found = INT_MAX;
   }
   __syncthreads();
-  const DF S = tot_s[0];
+  const DF wexcl = wid > 0 ? s_df[wid - 1] : DF{0.f, 0.f};
+  const DF excl = df_add(wexcl, prev);
+  const DF S = s_df[kThreads / 32 - 1];
   const double Sd = df_to_double(S);
-  if (!(Sd > 0.0)) {
+  if (!(Sd > 0.0) || !isfinite(Sd)) {
     if (tid == 0) {
       report(p.status, kErrNonfinite);
       p.tokens_out[c.out_index] = 0;
     }
+    if (stage_next && wid == 0)
+      write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, 0, lane);
     return;
   }
   const double u = uniform_dev(p.seed, (uint32_t)b, c.upos, c.ustage);
   const double theta = u * Sd;
-
-  DF run = excl_s[tid];
+  DF run = excl;
   int my_found = INT_MAX;
   DF my_excl = {0.f, 0.f};
   for (int i = c0; i < c1; ++i) {
-    const ChunkRec r = rec[i];
-    const int e = (r.ref == kEmptyRef) ? -1000 : r.ref - N;
-    const DF incl = df_add(run, df_scale2(DF{r.hi, r.lo}, max(e, -300)));
+    const DF incl = df_add(run, scaled_rec(srec[i], N));
     if (df_to_double(incl) > theta) {
       my_found = i;
       my_excl = run;
@@ -405,74 +291,106 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
     }
     run = incl;
   }
-  const int cfound = block_min_int(my_found, red);
-  if (my_found == cfound && cfound != INT_MAX) found_excl = my_excl;
+  if (my_found != INT_MAX) atomicMin(&s_found, my_found);
   __syncthreads();
-
-  int chunk = cfound;
-  if (chunk == INT_MAX) {  // rounding left u*S at the very top: take the last chunk with mass
-    if (tid == 0) {
-      chunk = nc - 1;
-      while (chunk > 0 && rec[chunk].hi == 0.f) --chunk;
-      found_s = chunk;
-      found_excl = df_add(S, DF{-rec[chunk].hi, -rec[chunk].lo});
-    }
-    __syncthreads();
-    chunk = found_s;
+  if (my_found != INT_MAX && my_found == s_found) s_excl = my_excl;
+  if (tid == 0 && s_found == INT_MAX) {  // u*S at the very top: last chunk with mass
+    int ch = nc - 1;
+    while (ch > 0 && !(srec[ch].hi > 0.f)) --ch;
+    s_found = ch;
+    const DF sc = scaled_rec(srec[ch], N);
+    s_excl = df_add(S, DF{-sc.hi, -sc.lo});
   }
-
-  // ---- recompute the crossing chunk with the tile kernel's arithmetic ----
+  __syncthreads();
+  const int chunk = s_found;
   const int col0 = chunk * 32;
   const int n = min(32, p.V - col0);
+
+  // ---- recompute the crossing chunk: bias (k split over warps), logits, weights ----
   if (c.a_token >= 0) {
-    const Tin* E = reinterpret_cast<const Tin*>(p.E);
-    for (int k = tid; k < p.r; k += kThreads) arow[k] = to_f32(E[(size_t)c.a_token * p.r + k]);
+    const Tin* E = reinterpret_cast<const Tin*>(p.E) + (size_t)c.a_token * p.r;
+    for (int k = tid; k < p.r; k += kThreads) s_arow[k] = to_f32(E[k]);
   }
   __syncthreads();
-  if (tid < 32) {
-    const int col = col0 + tid;
+  {
     float acc = 0.f;
-    if (c.a_token >= 0 && tid < n) {
-      const Tin* P = reinterpret_cast<const Tin*>(p.P);
-      for (int k = 0; k < p.r; ++k) acc = __fmaf_rn(arow[k], to_f32(P[(size_t)k * p.V + col]), acc);
-    }
-    bs[tid] = acc;
-    zs[tid] = (c.zrow && tid < n) ? to_f32(reinterpret_cast<const Tin*>(c.zrow)[col]) : 0.f;
-    ts[tid] = (c.trow && tid < n) ? to_f32(reinterpret_cast<const Tin*>(c.trow)[col]) : 0.f;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float w[32];
-    DF pre[32];
-    ChunkRec chk;
-    RowCtx cc = c;
-    chunk_record(cc, zs, bs, ts, n, col0, chk, p.status, w, pre);
-    const int e = (chk.ref == kEmptyRef) ? -1000 : chk.ref - N;
-    const DF ex = found_excl;
-    int x = -1;
-    int last_pos = -1;
-    for (int j = 0; j < n; ++j) {
-      if (w[j] > 0.f) last_pos = j;
-      const DF incl = df_add(ex, df_scale2(pre[j], max(e, -300)));
-      if (w[j] > 0.f && df_to_double(incl) > theta) {
-        x = j;
-        break;
+    if (c.a_token >= 0 && lane < n) {
+      const int per = p.r / (kThreads / 32);
+      const int k0 = wid * per;
+      const Tin* P = reinterpret_cast<const Tin*>(p.P) + (size_t)k0 * p.V + col0 + lane;
+      float pv[8];
+      for (int k = 0; k < per; k += 8) {
+#pragma unroll
+        for (int u8 = 0; u8 < 8; ++u8) pv[u8] = (k + u8 < per) ? to_f32(P[(size_t)(k + u8) * p.V]) : 0.f;
+#pragma unroll
+        for (int u8 = 0; u8 < 8; ++u8)
+          if (k + u8 < per) acc = __fmaf_rn(s_arow[k0 + k + u8], pv[u8], acc);
       }
     }
-    if (x < 0) x = last_pos >= 0 ? last_pos : 0;  // recompute drifted from the record
-    const int tok = col0 + x;
-    p.tokens_out[c.out_index] = tok;
-    if (p.src == 0) {
-      const double q = ldexp((double)w[x], e) / Sd;
-      p.q_token[c.out_index] = (float)q;
-      ds_row_stats st;
-      st.sum_hi = S.hi;
-      st.sum_lo = S.lo;
-      st.ref = N;
-      st.argmax = -1;
-      p.q_stats[c.out_index] = st;
+    s_part[wid][lane] = acc;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    float bsum = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) bsum = __fadd_rn(bsum, s_part[w][lane]);
+    s_b[lane] = bsum;
+    s_z[lane] = (c.zrow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.zrow)[col0 + lane]) : 0.f;
+    s_t[lane] = (c.trow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.trow)[col0 + lane]) : 0.f;
+    __syncwarp();
+    if (lane == 0) {
+      ChunkRec chk;
+      chunk_record<false>(c, F32Src{s_z}, s_b, F32Src{s_t}, n, col0, chk, p.status, s_w);
+      s_ref = (c.mode == kSampleMarkov) ? chk.ref : 0;
+    }
+    __syncwarp();
+    const int e = (c.mode == kSampleMarkov) ? max(s_ref - N, -300) : 0;
+    const float w = lane < n ? s_w[lane] : 0.f;
+    DF pre = {ldexpf(w, e), 0.f};
+    for (int o = 1; o < 32; o <<= 1) {
+      const DF v = shfl_up_df(pre, o);
+      if (lane >= o) pre = df_add(v, pre);
+    }
+    const DF incl = df_add(s_excl, pre);
+    const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && df_to_double(incl) > theta);
+    const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
+    int xl = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+    const float wx = __shfl_sync(0xffffffffu, w, xl);
+    const int x = col0 + xl;
+    if (lane == 0) {
+      if (!pos) report(p.status, kErrNonfinite);
+      p.tokens_out[c.out_index] = x;
+      if (p.src == 0) {
+        p.q_token[c.out_index] = (float)(ldexp((double)wx, e) / Sd);
+        ds_row_stats st;
+        st.sum_hi = S.hi;
+        st.sum_lo = S.lo;
+        st.ref = N;
+        st.argmax = -1;
+        p.q_stats[c.out_index] = st;
+      }
+    }
+    if (stage_next) write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, x, lane);
+  }
+}
+
+// Stage E[anchor] rows as the first step's A operand (rows beyond B zeroed).
+__global__ void __launch_bounds__(128) draft_prep_kernel(const int32_t* anchor,
+                                                         const __nv_bfloat16* E, int B, int V,
+                                                         int r, uint8_t* astage, int rows,
+                                                         int32_t* status) {
+  sm100::pdl_launch_dependents();
+  sm100::pdl_wait();
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  int tok = -1;
+  if (row < B) {
+    tok = anchor[row];
+    if (tok < 0 || tok >= V) {
+      if (lane == 0) report(status, kErrBounds);
+      tok = 0;
     }
   }
+  write_a_row(astage, E, r, row, tok, lane);
 }
 
 }  // namespace
@@ -498,12 +416,44 @@ cudaError_t launch_sample_tile(const SampleParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+size_t locate_smem_bytes(int32_t V) { return (size_t)num_chunks(V) * sizeof(ChunkRec); }
+
+template <typename K, typename... Args>
+static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_sample_locate(const SampleParams& p, cudaStream_t s) {
-  if (p.dtype == DS_BF16)
-    sample_locate_kernel<__nv_bfloat16><<<p.B, kThreads, 0, s>>>(p);
-  else
-    sample_locate_kernel<float><<<p.B, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  const size_t smem = locate_smem_bytes(p.V);
+  if (p.dtype == DS_BF16) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        sample_locate_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (attr != cudaSuccess) return attr;
+    return launch_pdl(sample_locate_kernel<__nv_bfloat16>, dim3(p.B), dim3(kThreads), smem, s, p);
+  }
+  static cudaError_t attr = cudaFuncSetAttribute(
+      sample_locate_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (attr != cudaSuccess) return attr;
+  return launch_pdl(sample_locate_kernel<float>, dim3(p.B), dim3(kThreads), smem, s, p);
+}
+
+cudaError_t launch_draft_prep(const int32_t* anchor, const void* E, int32_t B, int32_t V, int32_t r,
+                              uint8_t* astage, int32_t* status, cudaStream_t s) {
+  const int rows = ((B + 127) / 128) * 128;
+  return launch_pdl(draft_prep_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, anchor,
+                    reinterpret_cast<const __nv_bfloat16*>(E), (int)B, (int)V, (int)r, astage, rows,
+                    status);
 }
 
 }  // namespace ds

@@ -1,0 +1,220 @@
+// Per-row sampling context and the per-chunk reductions shared by the tile
+// kernels (tensor-core and SIMT) and the locate kernel.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ds {
+namespace {
+
+// Everything a kernel needs to know about one row of the batch being sampled.
+struct RowCtx {
+  int32_t mode;
+  int32_t a_token;  // E row of the bias; -1 when the row needs no bias
+  const void* zrow;
+  const void* trow;
+  Gscale g;
+  int32_t Np, Nq;
+  float Rhi, Rlo;
+  uint32_t upos, ustage;  // Philox position and stage of the row's draw
+  int32_t out_index;      // flat index of the drawn token in tokens_out
+  int32_t zk;             // draft: 0-based position of the base row; final: row index j
+};
+
+template <typename Tin>
+__device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
+  RowCtx c;
+  c.mode = kSkip;
+  c.a_token = -1;
+  c.zrow = nullptr;
+  c.trow = nullptr;
+  c.g = {0.f, 0.f};
+  c.Np = c.Nq = 0;
+  c.Rhi = c.Rlo = 0.f;
+  c.upos = 0;
+  c.ustage = 0;
+  c.out_index = 0;
+  c.zk = 0;
+  if (b >= p.B) return c;
+  const Tin* base = reinterpret_cast<const Tin*>(p.base_logits);
+  const Tin* tgt = reinterpret_cast<const Tin*>(p.target_logits);
+  const float T = p.temperature[b];
+  const bool greedy = (T == 0.f);
+  if (!greedy && !(T >= 1e-3f && T <= 1e3f)) {
+    report(p.status, kErrInvalidArg);
+    return c;
+  }
+  if (!greedy) c.g = make_gscale(T);
+  if (p.src == 0) {
+    const int k = p.step;  // 1-based
+    int tok = (k == 1) ? p.anchor[b] : p.draft_tokens[(size_t)b * p.K + (k - 2)];
+    if (tok < 0 || tok >= p.V) {
+      report(p.status, kErrBounds);
+      tok = 0;
+    }
+    c.a_token = tok;
+    c.mode = greedy ? kGreedyMarkov : kSampleMarkov;
+    c.zrow = base + ((size_t)b * p.K + (k - 1)) * (size_t)p.V;
+    c.upos = (uint32_t)k;
+    c.ustage = DS_STAGE_DRAFT;
+    c.out_index = b * p.K + (k - 1);
+    c.zk = k - 1;
+  } else {
+    const FinalDesc d = p.final_desc[b];
+    if (greedy || d.mode == kSkip) return c;
+    c.mode = d.mode;
+    c.trow = tgt + ((size_t)b * (p.K + 1) + d.row) * (size_t)p.V;
+    c.Np = d.Np;
+    c.upos = (uint32_t)(d.row + 1);
+    c.ustage = DS_STAGE_RESAMPLE;
+    c.out_index = b * (p.K + 1) + d.out_pos;
+    c.zk = d.row;
+    if (d.mode == kResidual) {
+      int tok = d.a_token;
+      if (tok < 0 || tok >= p.V) {
+        report(p.status, kErrBounds);
+        tok = 0;
+      }
+      c.a_token = tok;
+      c.zrow = base + ((size_t)b * p.K + d.row) * (size_t)p.V;
+      c.Nq = d.Nq;
+      c.Rhi = d.Rhi;
+      c.Rlo = d.Rlo;
+    }
+  }
+  return c;
+}
+
+// Chunk reference n = rint(max_j z_j * g.hi) over finite z; kEmptyRef if none.
+__device__ __forceinline__ int chunk_ref_from_max(float amax) {
+  return amax == kNegInf ? kEmptyRef : (int)rintf(amax);
+}
+
+// Element sources for chunk_record: plain floats, or bf16 pairs packed in
+// 32-bit words (the tensor-core epilogue keeps its logits packed to save
+// registers; unpacking is a shift or a mask).
+struct F32Src {
+  const float* p;
+  __device__ __forceinline__ float operator()(int j) const { return p[j]; }
+};
+struct Bf16Src {
+  const uint32_t* p;
+  __device__ __forceinline__ float operator()(int j) const {
+    const uint32_t w = p[j >> 1];
+    return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+};
+
+// Reduce one chunk of n (<= 32) tokens starting at token col0 to its record.
+// z, bias, t give the chunk's base logits, Markov bias and target logits.
+// If w_out is given, per-token weights (relative to rec.ref) are written too.
+template <bool FULL, typename ZS, typename TS>
+__device__ __forceinline__ void chunk_record(const RowCtx& c, ZS z, const float* bias, TS t, int n,
+                                             int col0, ChunkRec& rec, int32_t* status,
+                                             float* w_out = nullptr) {
+  constexpr int NMAX = 32;
+  rec.hi = 0.f;
+  rec.lo = 0.f;
+  rec.ref = 0;
+  rec.idx = -1;
+  bool bad = false;
+  if (c.mode == kGreedyMarkov) {
+    DF best = {kNegInf, 0.f};
+    int bi = -1;
+#pragma unroll
+    for (int j = 0; j < NMAX; ++j) {
+      if (FULL || j < n) {
+        const float zj = z(j);
+        bad |= bad_logit(zj) || !(bias[j] == bias[j]);
+        DF l = (zj == kNegInf) ? DF{kNegInf, 0.f} : two_sum(zj, bias[j]);
+        if (bi < 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
+          best = l;
+          bi = col0 + j;
+        }
+      }
+    }
+    rec.hi = best.hi;
+    rec.lo = best.lo;
+    rec.idx = bi;
+  } else if (c.mode == kSampleMarkov) {
+    // NaN / +inf logits or biases make the sum non-finite; -inf weighs 0.
+    float amax = kNegInf;
+#pragma unroll
+    for (int j = 0; j < NMAX; ++j)
+      if (FULL || j < n) amax = fmaxf(amax, scaled_hi(z(j), c.g));
+    const int ref = chunk_ref_from_max(amax);
+    DF s = {0.f, 0.f};
+    if (ref != kEmptyRef) {
+#pragma unroll
+      for (int j = 0; j < NMAX; ++j) {
+        if (FULL || j < n) {
+          const float w = weight_rel(z(j), bias[j], c.g, ref);
+          df_accumulate(s, w);
+          if (w_out) w_out[j] = w;
+        } else if (w_out) {
+          w_out[j] = 0.f;
+        }
+      }
+    } else {
+      bool any_nan = false;
+#pragma unroll
+      for (int j = 0; j < NMAX; ++j)
+        if (FULL || j < n) any_nan |= !(z(j) == z(j));
+      bad |= any_nan;
+      if (w_out)
+#pragma unroll
+        for (int j = 0; j < NMAX; ++j) w_out[j] = 0.f;
+    }
+    bad |= !isfinite(s.hi);
+    rec.hi = s.hi;
+    rec.lo = s.lo;
+    rec.ref = ref;
+  } else {  // kResidual / kBonus: weights on the row's global scale
+    DF s = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NMAX; ++j) {
+      if (FULL || j < n) {
+        float w = weight_rel(t(j), 0.f, c.g, c.Np);
+        if (c.mode == kResidual) {
+          const float wq = weight_rel(z(j), bias[j], c.g, c.Nq);
+          float d = __fmaf_rn(-wq, c.Rhi, w);
+          d = __fmaf_rn(-wq, c.Rlo, d);
+          bad |= !(d == d);
+          w = fmaxf(d, 0.f);
+        }
+        df_accumulate(s, w);
+        if (w_out) w_out[j] = w;
+      } else if (w_out) {
+        w_out[j] = 0.f;
+      }
+    }
+    bad |= !isfinite(s.hi);
+    rec.hi = s.hi;
+    rec.lo = s.lo;
+    rec.ref = 0;
+  }
+  if (bad) report(status, kErrNonfinite);
+}
+
+// Write E[tok] (r bf16 values, r % 64 == 0) into the 128B-swizzled K-major
+// A-operand staging of its M-tile: [kb][row/8][row%8][chunk ^ (row%8)][16 B].
+// One warp; lane i copies 16-byte chunks i, i+32, ...
+__device__ __forceinline__ void write_a_row(uint8_t* astage, const __nv_bfloat16* E, int r, int b,
+                                            int tok, int lane) {
+  const int mt = b >> 7, m = b & 127;
+  const int nkb = r >> 6;
+  uint8_t* tile = astage + (size_t)mt * nkb * 16384;
+  for (int q = lane; q < nkb * 8; q += 32) {
+    const int kb = q >> 3, ch = q & 7;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tok >= 0) v = __ldg(reinterpret_cast<const uint4*>(E + (size_t)tok * r + kb * 64 + ch * 8));
+    uint8_t* dst = tile + kb * 16384 + (m >> 3) * 1024 + (m & 7) * 128 + ((ch ^ (m & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst) = v;
+  }
+}
+
+}  // namespace
+}  // namespace ds

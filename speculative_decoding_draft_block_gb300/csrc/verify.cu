@@ -21,6 +21,8 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sampling.cuh"
+#include "sm100.cuh"
 
 namespace ds {
 
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
         nt = ng;
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) df_accumulate(acc, exp2_rel(v[q], 0.f, g, nt));
+      for (int q = 0; q < 8; ++q) df_accumulate(acc, weight_rel(v[q], 0.f, g, nt));
     }
     int m = nt;
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
           x = 0;
         }
         const float tx = to_f32(row[x]);
-        const double px = (double)exp2_rel(tx, 0.f, g, N) / Sd;
+        const double px = (double)weight_rel(tx, 0.f, g, N) / Sd;
         const double qx = (double)p.q_token[(size_t)b * p.K + j];
         const double u = uniform_dev(p.seed, (uint32_t)b, (uint32_t)(j + 1), DS_STAGE_ACCEPT);
         out.accept = (u * qx < px) ? 1 : 0;
@@ -156,9 +158,17 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
   if (tid == 0) p.vrows[(size_t)b * (p.K + 1) + j] = out;
 }
 
-__global__ void verify_finalize_kernel(VerifyParams p) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= p.B) return;
+// One warp per request: lane 0 walks the accept flags; the warp then stages
+// the A-operand row of the final draw (E[x_{k-1}] for a residual draw).
+__global__ void __launch_bounds__(128) verify_finalize_kernel(VerifyParams p) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int rows = ((p.B + 127) / 128) * 128;
+  if (b >= rows) return;
+  if (b >= p.B) {
+    if (p.astage) write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, -1, lane);
+    return;
+  }
   const int K = p.K;
   int L = p.sched_len[b];
   L = L < 0 ? 0 : (L > K ? K : L);
@@ -167,10 +177,7 @@ __global__ void verify_finalize_kernel(VerifyParams p) {
   int a = 0;
   while (a < L && vr[a].accept) ++a;
   int32_t* out = p.out_tokens + (size_t)b * (K + 1);
-  for (int i = 0; i < a; ++i) out[i] = p.draft_tokens[(size_t)b * K + i];
-  for (int i = a; i <= K; ++i) out[i] = -1;
-  p.accept_count[b] = a;
-  p.num_emitted[b] = a + 1;
+  for (int i = lane; i <= K; i += 32) out[i] = i < a ? p.draft_tokens[(size_t)b * K + i] : -1;
   FinalDesc d;
   d.mode = kSkip;
   d.row = a;
@@ -179,7 +186,8 @@ __global__ void verify_finalize_kernel(VerifyParams p) {
   d.Np = d.Nq = 0;
   d.Rhi = d.Rlo = 0.f;
   if (T == 0.f) {
-    out[a] = vr[a].argmax;
+    __syncwarp();
+    if (lane == 0) out[a] = vr[a].argmax;
   } else if (T >= 1e-3f && T <= 1e3f) {
     d.Np = vr[a].ref;
     if (a < L) {
@@ -196,7 +204,16 @@ __global__ void verify_finalize_kernel(VerifyParams p) {
       d.mode = kBonus;
     }
   }
-  p.final_desc[b] = d;
+  if (lane == 0) {
+    p.accept_count[b] = a;
+    p.num_emitted[b] = a + 1;
+    p.final_desc[b] = d;
+  }
+  if (p.astage) {
+    int tok = d.a_token;
+    if (tok >= p.V) tok = 0;
+    write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, tok, lane);
+  }
 }
 
 }  // namespace
@@ -211,7 +228,8 @@ cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s) {
-  verify_finalize_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p);
+  const int rows = ((p.B + 127) / 128) * 128;
+  verify_finalize_kernel<<<(rows + 3) / 4, 128, 0, s>>>(p);
   return cudaGetLastError();
 }
 
