@@ -52,27 +52,26 @@ bool shape_ok(int32_t B, int32_t K, int32_t V, int32_t r) {
 
 ds_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DS_OK : DS_ERR_CUDA; }
 
-// Draft workspace: two record buffers (alternating steps, so a step's records
-// are never overwritten while the previous locate still reads them) and the
-// A-operand staging of the tensor-core path.
+// Draft workspace: two record buffers, used by alternating steps so that a
+// step's records are never overwritten while the previous locate still reads them.
 struct DraftLayout {
-  size_t rec0, rec1, astage, total;
+  size_t rec0, rec1, total;
 };
 
 DraftLayout draft_layout(int32_t B, int32_t V, int32_t r) {
+  (void)r;
   DraftLayout l;
   const size_t rec = align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
   l.rec0 = 0;
   l.rec1 = rec;
-  l.astage = 2 * rec;
-  l.total = l.astage + align_up(astage_bytes(B, r < 64 ? 64 : r));
+  l.total = 2 * rec;
   return l;
 }
 
 size_t draft_ws(int32_t B, int32_t V, int32_t r) { return draft_layout(B, V, r).total; }
 
 struct VerifyLayout {
-  size_t vrows, desc, chunks, astage, total;
+  size_t vrows, desc, chunks, total;
 };
 
 VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
@@ -80,8 +79,8 @@ VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
   l.vrows = 0;
   l.desc = l.vrows + align_up((size_t)B * (K + 1) * sizeof(VRow));
   l.chunks = l.desc + align_up((size_t)B * sizeof(FinalDesc));
-  l.astage = l.chunks + align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
-  l.total = l.astage + align_up(astage_bytes(B, r < 64 ? 64 : r));
+  (void)r;
+  l.total = l.chunks + align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
   return l;
 }
 
@@ -144,19 +143,16 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   const DraftLayout l = draft_layout(a->B, a->V, a->r);
   char* ws = reinterpret_cast<char*>(a->workspace);
   const bool tc = tc_path_supported(a->dtype, a->r);
-  p.astage = tc ? reinterpret_cast<uint8_t*>(ws + l.astage) : nullptr;
   p.seed = a->seed;
   p.tokens_out = a->draft_tokens;
   p.q_token = a->q_token;
   p.q_stats = a->q_stats;
   p.status = a->status;
   const cudaStream_t s = (cudaStream_t)stream;
-  if (tc && launch_draft_prep(a->anchor, a->E, a->B, a->V, a->r, p.astage, a->status, s) != cudaSuccess)
-    return DS_ERR_CUDA;
   for (int k = 1; k <= a->K; ++k) {
     p.step = k;
     p.chunks = reinterpret_cast<ChunkRec*>(ws + ((k & 1) ? l.rec1 : l.rec0));
-    cudaError_t e = tc ? launch_tile_tc(p, p.astage, s) : launch_sample_tile(p, s);
+    cudaError_t e = tc ? launch_tile_tc(p, s) : launch_sample_tile(p, s);
     if (e != cudaSuccess) return DS_ERR_CUDA;
     e = launch_sample_locate(p, s);
     if (e != cudaSuccess) return DS_ERR_CUDA;
@@ -249,8 +245,6 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   v.n_chunks = num_chunks(a->V);
   v.dtype = a->dtype;
   v.target_logits = a->target_logits;
-  v.E = a->E;
-  v.astage = tc ? reinterpret_cast<uint8_t*>(ws + l.astage) : nullptr;
   v.anchor = a->anchor;
   v.draft_tokens = a->draft_tokens;
   v.q_token = a->q_token;
@@ -286,11 +280,10 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   p.temperature = a->temperature;
   p.final_desc = v.final_desc;
   p.chunks = reinterpret_cast<ChunkRec*>(ws + l.chunks);
-  p.astage = nullptr;
   p.seed = a->seed;
   p.tokens_out = a->out_tokens;
   p.status = a->status;
-  if ((tc ? launch_tile_tc(p, v.astage, s) : launch_sample_tile(p, s)) != cudaSuccess)
+  if ((tc ? launch_tile_tc(p, s) : launch_sample_tile(p, s)) != cudaSuccess)
     return DS_ERR_CUDA;
   if (launch_sample_locate(p, s) != cudaSuccess) return DS_ERR_CUDA;
   return DS_OK;

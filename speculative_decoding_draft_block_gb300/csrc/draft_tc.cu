@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "fastpath.cuh"
 #include "sampling.cuh"
 #include "sm100.cuh"
 
@@ -45,26 +46,27 @@ using namespace sm100;
 constexpr int kTcThreads = 576;  // 18 warps
 constexpr int kEpiWarps = 16;
 constexpr int kTileN = 128;
-constexpr int kPStages = 4;
-constexpr uint32_t kASize = 65536;   // up to r = 256
-constexpr uint32_t kPStage = 16384;  // 64 k-rows x 128 tokens
-constexpr uint32_t kZStage = 32768;  // 128 rows x 128 tokens
+constexpr int kPStages = 6;           // 64 k-rows x 128 tokens of P each
+constexpr int kZSlots = 4;            // 128 rows x 64 tokens of logits each
+constexpr int kAccum = 2;             // TMEM accumulators (128 columns each)
+constexpr uint32_t kASize = 65536;    // up to r = 256
+constexpr uint32_t kPStage = 16384;
+constexpr uint32_t kZSlot = 16384;
 constexpr uint32_t kOffP = kASize;
 constexpr uint32_t kOffZ = kOffP + kPStages * kPStage;
-constexpr uint32_t kSmemBytes = kOffZ + 2 * kZStage + 1024;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSmemBytes = kOffZ + kZSlots * kZSlot + 1024;
+constexpr uint32_t kTmemCols = kAccum * kTileN;
 
 struct TcParams {
   SampleParams sp;
-  const uint8_t* astage;
   int32_t n_mt, n_nt, nkb, tiles;
 };
 
 struct Shared {
   uint64_t a_full, a_empty;
   uint64_t p_full[kPStages], p_empty[kPStages];
-  uint64_t z_full[2], z_empty[2];
-  uint64_t t_full[2], t_empty[2];
+  uint64_t z_full[kZSlots], z_empty[kZSlots];
+  uint64_t t_full[kAccum], t_empty[kAccum];
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -84,73 +86,111 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 struct EpiRow {
   int32_t mode;
   Gscale g;
+  G16 g16;
   int32_t Np, Nq;
   float Rhi, Rlo;
 };
 
+// General path for one 16-column half (every mode; ragged chunks; chunks with
+// -inf, out-of-range or non-finite logits).
+__device__ __forceinline__ void slow_half(const EpiRow& c, int h, const uint32_t* zp,
+                                          const uint32_t* tp, const float* bh, int n, int col0,
+                                          int ref, DF& s, DF& best, int& bi, bool& bad) {
+  const Bf16Src z{zp}, t{tp};
+  if (c.mode == kSampleMarkov) {
+    if (ref == kEmptyRef) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (h * 16 + j < n) df_accumulate(s, weight_rel(z(h * 16 + j), bh[j], c.g, ref));
+  } else if (c.mode == kGreedyMarkov) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int jj = h * 16 + j;
+      if (jj < n) {
+        const float zj = z(jj);
+        bad |= bad_logit(zj) || !(bh[j] == bh[j]);
+        const DF l = (zj == kNegInf) ? DF{kNegInf, 0.f} : two_sum(zj, bh[j]);
+        if (bi < 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
+          best = l;
+          bi = col0 + jj;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int jj = h * 16 + j;
+      if (jj < n) {
+        float w = weight_rel(t(jj), 0.f, c.g, c.Np);
+        if (c.mode == kResidual) {
+          const float wq = weight_rel(z(jj), bh[j], c.g, c.Nq);
+          float d = __fmaf_rn(-wq, c.Rhi, w);
+          d = __fmaf_rn(-wq, c.Rlo, d);
+          bad |= !(d == d);
+          w = fmaxf(d, 0.f);
+        }
+        df_accumulate(s, w);
+      }
+    }
+  }
+}
+
 // Reduce this thread's (row, 32-token chunk) slice of a finished accumulator.
-// The bias is read from TMEM in two 16-column halves (tcgen05.ld is
-// warp-collective, so every lane loads even when its row has nothing to do).
-template <bool FULL>
+// The bias is read from TMEM in two 16-column halves; tcgen05.ld is
+// warp-collective, so every lane of the warp issues the same loads.
 __device__ __forceinline__ void epi_chunk(const EpiRow& c, bool active, const uint32_t* zp,
                                           const uint32_t* tp, uint32_t taddr, int n, int col0,
                                           ChunkRec& rec, bool& bad) {
-  const Bf16Src z{zp}, t{tp};
+  const bool sample = active && c.mode == kSampleMarkov;
+  int fref = 0;
+  bool fast = (n == 32) && sample && fast_chunk_ok(zp, c.g16, fref);
+  bool done = false;
+  if (__any_sync(0xffffffffu, fast)) {
+    const FastConsts k = make_fast_consts(c.g16, fref);
+    float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float bh[16];
+      tmem_ld16(taddr + h * 16, bh);
+      if (fast) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) fast_pair(zp[h * 8 + i], bh[2 * i], bh[2 * i + 1], k, shi, slo);
+      }
+    }
+    if (fast) {
+      const float hi = __fadd_rn(shi.x, shi.y);  // exact: multiples of 2^-15 below 1024
+      const float lo = __fadd_rn(slo.x, slo.y);
+      if (shi.x >= 0.f && shi.x < kFastHiLimit && shi.y >= 0.f && shi.y < kFastHiLimit &&
+          isfinite(lo)) {
+        const DF r = fast_two_sum(hi, lo);
+        rec.hi = r.hi;
+        rec.lo = r.lo;
+        rec.ref = fref;
+        rec.idx = -2;  // fast-path record
+        done = true;
+      }
+    }
+  }
+  const bool slow = active && !done;
+  if (!__any_sync(0xffffffffu, slow)) return;
   int ref = 0;
-  if (active && c.mode == kSampleMarkov) {
+  if (slow && c.mode == kSampleMarkov) {
+    const Bf16Src z{zp};
     float amax = kNegInf;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (FULL || j < n) amax = fmaxf(amax, scaled_hi(z(j), c.g));
+      if (j < n) amax = fmaxf(amax, scaled_hi(z(j), c.g));
     ref = chunk_ref_from_max(amax);
   }
-  DF s = {0.f, 0.f};
-  DF best = {kNegInf, 0.f};
+  DF s = {0.f, 0.f}, best = {kNegInf, 0.f};
   int bi = -1;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float bh[16];
     tmem_ld16(taddr + h * 16, bh);
-    if (!active) continue;
-    if (c.mode == kSampleMarkov) {
-      if (ref != kEmptyRef) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (FULL || h * 16 + j < n) df_accumulate(s, weight_rel(z(h * 16 + j), bh[j], c.g, ref));
-      }
-    } else if (c.mode == kGreedyMarkov) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int jj = h * 16 + j;
-        if (FULL || jj < n) {
-          const float zj = z(jj);
-          bad |= bad_logit(zj) || !(bh[j] == bh[j]);
-          const DF l = (zj == kNegInf) ? DF{kNegInf, 0.f} : two_sum(zj, bh[j]);
-          if (bi < 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
-            best = l;
-            bi = col0 + jj;
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int jj = h * 16 + j;
-        if (FULL || jj < n) {
-          float w = weight_rel(t(jj), 0.f, c.g, c.Np);
-          if (c.mode == kResidual) {
-            const float wq = weight_rel(z(jj), bh[j], c.g, c.Nq);
-            float d = __fmaf_rn(-wq, c.Rhi, w);
-            d = __fmaf_rn(-wq, c.Rlo, d);
-            bad |= !(d == d);
-            w = fmaxf(d, 0.f);
-          }
-          df_accumulate(s, w);
-        }
-      }
-    }
+    if (slow) slow_half(c, h, zp, tp, bh, n, col0, ref, s, best, bi, bad);
   }
-  rec.idx = -1;
+  if (!slow) return;
   if (c.mode == kGreedyMarkov) {
     rec.hi = best.hi;
     rec.lo = best.lo;
@@ -158,22 +198,36 @@ __device__ __forceinline__ void epi_chunk(const EpiRow& c, bool active, const ui
     rec.idx = bi;
   } else {
     if (c.mode == kSampleMarkov && ref == kEmptyRef) {
-      bool any_nan = false;
+      const Bf16Src z{zp};
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (FULL || j < n) any_nan |= !(z(j) == z(j));
-      bad |= any_nan;
+        if (j < n) bad |= !(z(j) == z(j));
     }
     bad |= !isfinite(s.hi);
     rec.hi = s.hi;
     rec.lo = s.lo;
     rec.ref = (c.mode == kSampleMarkov) ? ref : 0;
+    rec.idx = -1;
   }
+}
+
+// Token whose E row forms A-operand row b of this launch (0 for padding rows).
+__device__ __forceinline__ int a_token_for_row(const SampleParams& sp, int b) {
+  if (b >= sp.B) return 0;
+  int tok = 0;
+  if (sp.src == 0) {
+    tok = (sp.step == 1) ? sp.anchor[b] : sp.draft_tokens[(size_t)b * sp.K + (sp.step - 2)];
+  } else {
+    const FinalDesc d = sp.final_desc[b];
+    tok = (d.mode == kResidual && sp.temperature[b] != 0.f) ? d.a_token : 0;
+  }
+  return (tok >= 0 && tok < sp.V) ? tok : 0;  // out-of-range ids are reported by the epilogue
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     tile_tc_kernel(const TcParams prm, const __grid_constant__ CUtensorMap tmP,
-                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmT) {
+                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmT,
+                   const __grid_constant__ CUtensorMap tmE) {
   extern __shared__ uint8_t raw[];
   __shared__ Shared sh;
   const SampleParams& sp = prm.sp;
@@ -192,9 +246,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sh.p_full[i], 1);
       mbar_init(&sh.p_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kZSlots; ++i) {
       mbar_init(&sh.z_full[i], 1);
-      mbar_init(&sh.z_empty[i], kEpiWarps);
+      mbar_init(&sh.z_empty[i], kEpiWarps / 2);
+    }
+    for (int i = 0; i < kAccum; ++i) {
       mbar_init(&sh.t_full[i], 1);
       mbar_init(&sh.t_empty[i], kEpiWarps);
     }
@@ -219,19 +275,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tmP);
       prefetch_tmap(&tmZ);
+      prefetch_tmap(&tmE);
       if (!draft) prefetch_tmap(&tmT);
     }
     int cur_mt = -1;
-    uint32_t a_uses = 0, pc = 0;
-    bool waited = false;
-    for (int t = t0, i = 0; t < t1; ++t, ++i) {
+    uint32_t a_uses = 0, pc = 0, zc = 0;
+    bool waited = false, ok = true;
+    for (int t = t0, i = 0; t < t1 && ok; ++t, ++i) {
       const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
       const int n0 = nt * kTileN;
-      bool ok = true;
+      // P: independent of earlier kernels, so the first tile's loads precede the PDL wait
       for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
-        const uint32_t ps = pc % kPStages, ph = ((pc / kPStages) & 1) ^ 1;
+        const uint32_t ps = pc % kPStages;
         if (lane == 0) {
-          ok = wait_bar(&sh.p_empty[ps], ph, abort_flag, sp.status);
+          ok = wait_bar(&sh.p_empty[ps], ((pc / kPStages) & 1) ^ 1, abort_flag, sp.status);
           if (ok) {
             mbar_expect_tx(&sh.p_full[ps], kPStage);
             tma_load_2d(sP + ps * kPStage, &tmP, &sh.p_full[ps], n0, c * 64, pol_p);
@@ -242,59 +299,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) break;
       if (!waited) {
-        pdl_wait();  // A staging, draft tokens and final descriptors come from earlier kernels
+        pdl_wait();  // tokens and final-draw descriptors come from earlier kernels
         waited = true;
       }
       if (mt != cur_mt) {
+        // A operand: gather E rows of this M-tile's conditioning tokens (128B-swizzled TMA rows)
         if (lane == 0) {
           if (cur_mt >= 0) ok = wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status);
-          if (ok) {
-            mbar_expect_tx(&sh.a_full, prm.nkb * 16384);
-            bulk_load(sA, prm.astage + (size_t)mt * prm.nkb * 16384, prm.nkb * 16384, &sh.a_full);
-          }
+          if (ok) mbar_expect_tx(&sh.a_full, 128u * prm.nkb * 128u);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rr = lane + 32 * u;
+          const int tok = a_token_for_row(sp, mt * 128 + rr);
+          for (int kb = 0; kb < prm.nkb; ++kb)
+            tma_load_2d(sA + kb * 16384 + rr * 128, &tmE, &sh.a_full, kb * 64, tok, pol_p);
+        }
         ++a_uses;
         cur_mt = mt;
       }
       if (draft) {
-        const uint32_t zs = i & 1, ph = ((i >> 1) & 1) ^ 1;
-        if (lane == 0) {
-          ok = wait_bar(&sh.z_empty[zs], ph, abort_flag, sp.status);
-          if (ok) {
-            mbar_expect_tx(&sh.z_full[zs], kZStage);
-            tma_load_3d(sZ + zs * kZStage, &tmZ, &sh.z_full[zs], n0, sp.step - 1, mt * 128, pol_z);
-            tma_load_3d(sZ + zs * kZStage + 16384, &tmZ, &sh.z_full[zs], n0 + 64, sp.step - 1,
-                        mt * 128, pol_z);
+        for (int nb = 0; nb < 2 && ok; ++nb, ++zc) {
+          const uint32_t zs = zc % kZSlots;
+          if (lane == 0) {
+            ok = wait_bar(&sh.z_empty[zs], ((zc / kZSlots) & 1) ^ 1, abort_flag, sp.status);
+            if (ok) {
+              mbar_expect_tx(&sh.z_full[zs], kZSlot);
+              tma_load_3d(sZ + zs * kZSlot, &tmZ, &sh.z_full[zs], n0 + nb * 64, sp.step - 1,
+                          mt * 128, pol_z);
+            }
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       } else {
-        // final draw: gather each request's own base / target row (one 128-byte box per row)
-        const uint32_t ph = (i & 1) ^ 1;
-        if (lane == 0) ok = wait_bar(&sh.z_empty[0], ph, abort_flag, sp.status);
+        // final draw: each request's own base and target rows, one 128-byte box per row
+        // and half; slots 0/1 hold the base-logit halves, slots 2/3 the target halves
+        if (lane == 0)
+          for (int s = 0; s < kZSlots && ok; ++s)
+            ok = wait_bar(&sh.z_empty[s], (i & 1) ^ 1, abort_flag, sp.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        uint32_t bytes = 0;
         int rows_z[4], rows_t[4];
+        uint32_t nz = 0, ntr = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int rr = lane + 32 * u, b = mt * 128 + rr;
+          const int b = mt * 128 + lane + 32 * u;
           rows_z[u] = rows_t[u] = -1;
           if (b < sp.B && sp.temperature[b] != 0.f) {
             const FinalDesc d = sp.final_desc[b];
             if (d.mode == kResidual) rows_z[u] = d.row;
             if (d.mode == kResidual || d.mode == kBonus) rows_t[u] = d.row;
           }
-          bytes += (rows_z[u] >= 0 ? 256u : 0u) + (rows_t[u] >= 0 ? 256u : 0u);
+          nz += rows_z[u] >= 0;
+          ntr += rows_t[u] >= 0;
         }
-        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        for (int o = 16; o > 0; o >>= 1) {
+          nz += __shfl_xor_sync(0xffffffffu, nz, o);
+          ntr += __shfl_xor_sync(0xffffffffu, ntr, o);
+        }
         if (lane == 0) {
-          if (bytes)
-            mbar_expect_tx(&sh.z_full[0], bytes);
-          else
-            mbar_arrive(&sh.z_full[0]);
+          for (int s = 0; s < kZSlots; ++s) {
+            const uint32_t bytes = 128u * (s < 2 ? nz : ntr);
+            if (bytes)
+              mbar_expect_tx(&sh.z_full[s], bytes);
+            else
+              mbar_arrive(&sh.z_full[s]);
+          }
         }
         __syncwarp();
 #pragma unroll
@@ -303,15 +376,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int nb = 0; nb < 2; ++nb) {
             if (rows_z[u] >= 0)
-              tma_load_3d(sZ + nb * 16384 + rr * 128, &tmZ, &sh.z_full[0], n0 + nb * 64, rows_z[u], b,
-                          pol_z);
+              tma_load_3d(sZ + nb * kZSlot + rr * 128, &tmZ, &sh.z_full[nb], n0 + nb * 64,
+                          rows_z[u], b, pol_z);
             if (rows_t[u] >= 0)
-              tma_load_3d(sZ + kZStage + nb * 16384 + rr * 128, &tmT, &sh.z_full[0], n0 + nb * 64,
+              tma_load_3d(sZ + (2 + nb) * kZSlot + rr * 128, &tmT, &sh.z_full[2 + nb], n0 + nb * 64,
                           rows_t[u], b, pol_z);
           }
         }
       }
-      if (!ok) break;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -332,8 +404,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cur_mt = mt;
           tc_fence_after();
         }
-        const uint32_t buf = i & 1;
-        ok = wait_bar(&sh.t_empty[buf], ((i >> 1) & 1) ^ 1, abort_flag, sp.status);
+        const uint32_t buf = i % kAccum;
+        ok = wait_bar(&sh.t_empty[buf], ((i / kAccum) & 1) ^ 1, abort_flag, sp.status);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kTileN;
@@ -357,7 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     pdl_wait();
-    const int ew = warp - 2, q = warp & 3, cg = ew >> 2;
+    const int ew = warp - 2, q = warp & 3, cg = ew >> 2, nb = cg >> 1;
     const int r_local = q * 32 + lane;
     int cur_mt = -1;
     EpiRow c;
@@ -370,24 +442,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const RowCtx rc = make_row_ctx<__nv_bfloat16>(sp, row);
         c.mode = rc.mode;
         c.g = rc.g;
+        c.g16 = (rc.mode == kSampleMarkov) ? make_g16(sp.temperature[row]) : G16{0.f, 0.f, 0.f};
         c.Np = rc.Np;
         c.Nq = rc.Nq;
         c.Rhi = rc.Rhi;
         c.Rlo = rc.Rlo;
         cur_mt = mt;
       }
-      const uint32_t buf = i & 1;
-      const uint32_t zs = draft ? (i & 1) : 0;
-      const uint32_t zph = draft ? ((i >> 1) & 1) : (i & 1);
+      const uint32_t buf = i % kAccum;
+      const uint32_t zc = 2u * i + nb;
+      const uint32_t zs = draft ? zc % kZSlots : nb;
+      const uint32_t zph = draft ? (zc / kZSlots) & 1 : (i & 1);
       if (!wait_bar(&sh.z_full[zs], zph, abort_flag, sp.status)) break;
-      if (!wait_bar(&sh.t_full[buf], (i >> 1) & 1, abort_flag, sp.status)) break;
+      if (!draft && !wait_bar(&sh.z_full[2 + nb], zph, abort_flag, sp.status)) break;
+      if (!wait_bar(&sh.t_full[buf], (i / kAccum) & 1, abort_flag, sp.status)) break;
       tc_fence_after();
       uint32_t zp[16], tp[16];
-      const int nb = cg >> 1, ch0 = (cg & 1) * 4;
+      const int ch0 = (cg & 1) * 4;
       const bool need_z = (c.mode == kGreedyMarkov || c.mode == kSampleMarkov || c.mode == kResidual);
       const bool need_t = (c.mode == kResidual || c.mode == kBonus);
       if (need_z) {
-        const uint8_t* zb = sZ + zs * kZStage + nb * 16384 + r_local * 128;
+        const uint8_t* zb = sZ + zs * kZSlot + r_local * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint4 v = *reinterpret_cast<const uint4*>(zb + (((ch0 + u) ^ (r_local & 7)) << 4));
@@ -398,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (need_t) {
-        const uint8_t* tb = sZ + kZStage + nb * 16384 + r_local * 128;
+        const uint8_t* tb = sZ + (2 + nb) * kZSlot + r_local * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint4 v = *reinterpret_cast<const uint4*>(tb + (((ch0 + u) ^ (r_local & 7)) << 4));
@@ -409,16 +484,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.z_empty[zs]);
+      if (lane == 0) {
+        mbar_arrive(&sh.z_empty[zs]);
+        if (!draft) mbar_arrive(&sh.z_empty[2 + nb]);
+      }
       const int col0 = nt * kTileN + cg * 32;
       const bool active = row < sp.B && c.mode != kSkip && col0 < sp.V;
       const int n = min(32, sp.V - col0);
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kTileN + cg * 32;
       ChunkRec rec;
-      if (n >= 32)
-        epi_chunk<true>(c, active, zp, tp, taddr, 32, col0, rec, bad);
-      else
-        epi_chunk<false>(c, active, zp, tp, taddr, n, col0, rec, bad);
+      epi_chunk(c, active, zp, tp, taddr, n, col0, rec, bad);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
@@ -470,30 +545,30 @@ bool tc_path_supported(int32_t dtype, int32_t r) {
   return dtype == DS_BF16 && r % 64 == 0 && r >= 64 && r <= 256;
 }
 
-size_t astage_bytes(int32_t B, int32_t r) {
-  const size_t n_mt = (B + 127) / 128;
-  return n_mt * (size_t)(r / 64) * 16384;
-}
-
-cudaError_t launch_tile_tc(const SampleParams& p, const uint8_t* astage, cudaStream_t s) {
+cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(
       tile_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (attr != cudaSuccess) return attr;
   TcParams prm;
   prm.sp = p;
-  prm.astage = astage;
   prm.n_mt = (p.B + 127) / 128;
   prm.n_nt = (p.V + kTileN - 1) / kTileN;
   prm.nkb = p.r / 64;
   prm.tiles = prm.n_mt * prm.n_nt;
 
-  CUtensorMap mP, mZ, mT;
+  CUtensorMap mP, mZ, mT, mE;
   const cuuint64_t V = (cuuint64_t)p.V;
   {
     const cuuint64_t dims[2] = {V, (cuuint64_t)p.r};
     const cuuint64_t str[1] = {V * 2};
     const cuuint32_t box[2] = {64, 64};
     if (!encode(&mP, p.P, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.r, V};
+    const cuuint64_t str[1] = {(cuuint64_t)p.r * 2};
+    const cuuint32_t box[2] = {64, 1};
+    if (!encode(&mE, p.E, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {V, (cuuint64_t)p.K, (cuuint64_t)p.B};
@@ -524,7 +599,7 @@ cudaError_t launch_tile_tc(const SampleParams& p, const uint8_t* astage, cudaStr
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tile_tc_kernel, prm, mP, mZ, mT);
+  return cudaLaunchKernelEx(&cfg, tile_tc_kernel, prm, mP, mZ, mT, mE);
 }
 
 }  // namespace ds

@@ -58,7 +58,6 @@ struct SampleParams {
   const float* temperature;
   const FinalDesc* final_desc;  // [B]
   ChunkRec* chunks;             // [B][n_chunks]
-  uint8_t* astage;              // tensor-core A operand staging (bf16 path) or nullptr
   uint64_t seed;
   int32_t* tokens_out;        // draft: draft_tokens; final: out_tokens
   float* q_token;             // draft only
@@ -69,8 +68,6 @@ struct SampleParams {
 struct VerifyParams {
   int32_t B, K, V, r, n_chunks, dtype;
   const void* target_logits;
-  const void* E;
-  uint8_t* astage;  // A operand staging of the final draw (bf16 tensor-core path) or nullptr
   const int32_t* anchor;
   const int32_t* draft_tokens;
   const float* q_token;
@@ -112,10 +109,7 @@ inline int32_t num_chunks(int32_t V) { return (V + 31) / 32; }
 size_t sample_tile_smem_bytes(int32_t r);
 size_t locate_smem_bytes(int32_t V);
 bool tc_path_supported(int32_t dtype, int32_t r);
-size_t astage_bytes(int32_t B, int32_t r);
-cudaError_t launch_tile_tc(const SampleParams& p, const uint8_t* astage, cudaStream_t s);
-cudaError_t launch_draft_prep(const int32_t* anchor, const void* E, int32_t B, int32_t V, int32_t r,
-                              uint8_t* astage, int32_t* status, cudaStream_t s);
+cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_sample_tile(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_sample_locate(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s);

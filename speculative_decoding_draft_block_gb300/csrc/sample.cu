@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "fastpath.cuh"
 #include "sampling.cuh"
 #include "sm100.cuh"
 
@@ -132,14 +133,20 @@ __device__ __forceinline__ DF shfl_up_df(DF v, int o) {
   return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }
 
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
 __device__ __forceinline__ DF scaled_rec(const ChunkRec& r, int N) {
   const int e = (r.ref == kEmptyRef) ? -300 : max(r.ref - N, -300);
   return df_scale2(DF{r.hi, r.lo}, e);
 }
 
 // One CTA per row: combine the row's chunk records, locate the chunk where the
-// CDF crosses u*S, recompute its 32 weights and pick the token. In draft mode
-// it also stages E[x_k] as the next step's tensor-core A operand.
+// CDF crosses u*S, recompute its 32 weights and pick the token. The records
+// are staged once with independent 16-byte loads; the E row of the bias is
+// prefetched alongside, and the P column loads of the crossing chunk are all
+// issued before they are consumed, so the row costs few dependent round trips.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p) {
   extern __shared__ ChunkRec srec[];
@@ -147,22 +154,44 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
   __shared__ DF s_df[kThreads / 32];
   __shared__ float s_arow[1024];
   __shared__ float s_part[kThreads / 32][32];
-  __shared__ float s_z[32], s_b[32], s_t[32], s_w[32];
-  __shared__ int s_found, s_ref;
+  __shared__ int s_found;
   __shared__ DF s_excl;
   sm100::pdl_launch_dependents();
   sm100::pdl_wait();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const RowCtx c = make_row_ctx<Tin>(p, b);
-  const bool stage_next = (p.src == 0) && (p.astage != nullptr) && (p.step < p.K);
-  if (c.mode == kSkip) {
-    if (stage_next && wid == 0)
-      write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, 0, lane);
-    return;
-  }
+  if (c.mode == kSkip) return;
   const int nc = p.n_chunks;
-  const ChunkRec* rec = p.chunks + (size_t)b * nc;
-  for (int i = tid; i < nc; i += kThreads) srec[i] = rec[i];
+  const int r = p.r;
+  const Tin* Erow = reinterpret_cast<const Tin*>(p.E) + (size_t)(c.a_token >= 0 ? c.a_token : 0) * r;
+  float erow[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int k = tid + q * kThreads;
+    erow[q] = (c.a_token >= 0 && k < r) ? to_f32(Erow[k]) : 0.f;
+  }
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(p.chunks + (size_t)b * nc);
+    uint4* dst = reinterpret_cast<uint4*>(srec);
+    for (int i0 = 0; i0 < nc; i0 += kThreads * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < nc) v[u] = __ldcg(src + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < nc) dst[i] = v[u];
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int k = tid + q * kThreads;
+    if (k < r) s_arow[k] = erow[q];
+  }
   __syncthreads();
   const int seg = (nc + kThreads - 1) / kThreads;
   const int c0 = min(nc, tid * seg), c1 = min(nc, c0 + seg);
@@ -171,11 +200,11 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
     DF best = {kNegInf, 0.f};
     int bi = INT_MAX;
     for (int i = c0; i < c1; ++i) {
-      const ChunkRec r = srec[i];
-      if (r.idx < 0) continue;
-      if (bi == INT_MAX || r.hi > best.hi || (r.hi == best.hi && r.lo > best.lo)) {
-        best = {r.hi, r.lo};
-        bi = r.idx;
+      const ChunkRec rr = srec[i];
+      if (rr.idx < 0) continue;
+      if (bi == INT_MAX || rr.hi > best.hi || (rr.hi == best.hi && rr.lo > best.lo)) {
+        best = {rr.hi, rr.lo};
+        bi = rr.idx;
       }
     }
     for (int o = 16; o > 0; o >>= 1) {
@@ -194,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
       s_int[wid] = bi;
     }
     __syncthreads();
-    if (wid == 0) {
+    if (tid == 0) {
       DF bb = {kNegInf, 0.f};
       int bx = INT_MAX;
       for (int w = 0; w < kThreads / 32; ++w) {
@@ -209,27 +238,23 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
       }
       if (bx == INT_MAX) {
         bx = 0;
-        if (lane == 0) report(p.status, kErrNonfinite);
+        report(p.status, kErrNonfinite);
       }
-      if (lane == 0) {
-        p.tokens_out[c.out_index] = bx;
-        if (p.src == 0) {
-          p.q_token[c.out_index] = 1.f;
-          ds_row_stats st;
-          st.sum_hi = 1.f;
-          st.sum_lo = 0.f;
-          st.ref = 0;
-          st.argmax = bx;
-          p.q_stats[c.out_index] = st;
-        }
+      p.tokens_out[c.out_index] = bx;
+      if (p.src == 0) {
+        p.q_token[c.out_index] = 1.f;
+        ds_row_stats st;
+        st.sum_hi = 1.f;
+        st.sum_lo = 0.f;
+        st.ref = 0;
+        st.argmax = bx;
+        p.q_stats[c.out_index] = st;
       }
-      if (stage_next)
-        write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, bx, lane);
     }
     return;
   }
 
-  // ---- sampling rows ----
+  // ---- sampling rows: global reference, prefix sums, crossing chunk ----
   int lm = INT_MIN;
   if (c.mode == kSampleMarkov)
     for (int i = c0; i < c1; ++i) lm = max(lm, srec[i].ref);
@@ -243,7 +268,6 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
   }
   DF tot = {0.f, 0.f};
   for (int i = c0; i < c1; ++i) tot = df_add(tot, scaled_rec(srec[i], N));
-  // block exclusive scan of the per-thread totals (fixed tree order)
   DF inc = tot;
   for (int o = 1; o < 32; o <<= 1) {
     const DF v = shfl_up_df(inc, o);
@@ -251,7 +275,6 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
   }
   DF prev = shfl_up_df(inc, 1);
   if (lane == 0) prev = DF{0.f, 0.f};
-  __syncthreads();
   if (lane == 31) s_df[wid] = inc;
   __syncthreads();
   if (wid == 0) {
@@ -273,18 +296,18 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
       report(p.status, kErrNonfinite);
       p.tokens_out[c.out_index] = 0;
     }
-    if (stage_next && wid == 0)
-      write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, 0, lane);
     return;
   }
   const double u = uniform_dev(p.seed, (uint32_t)b, c.upos, c.ustage);
-  const double theta = u * Sd;
+  const double theta_d = u * Sd;
+  const float th_hi = (float)theta_d;
+  const DF theta = {th_hi, (float)(theta_d - (double)th_hi)};
   DF run = excl;
   int my_found = INT_MAX;
   DF my_excl = {0.f, 0.f};
   for (int i = c0; i < c1; ++i) {
     const DF incl = df_add(run, scaled_rec(srec[i], N));
-    if (df_to_double(incl) > theta) {
+    if (df_gt(incl, theta)) {
       my_found = i;
       my_excl = run;
       break;
@@ -306,25 +329,25 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
   const int col0 = chunk * 32;
   const int n = min(32, p.V - col0);
 
-  // ---- recompute the crossing chunk: bias (k split over warps), logits, weights ----
-  if (c.a_token >= 0) {
-    const Tin* E = reinterpret_cast<const Tin*>(p.E) + (size_t)c.a_token * p.r;
-    for (int k = tid; k < p.r; k += kThreads) s_arow[k] = to_f32(E[k]);
+  // ---- recompute the crossing chunk: logits first, then the bias (k split over warps) ----
+  float zl = 0.f, tl = 0.f;
+  if (wid == 0) {
+    zl = (c.zrow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.zrow)[col0 + lane]) : 0.f;
+    tl = (c.trow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.trow)[col0 + lane]) : 0.f;
   }
-  __syncthreads();
   {
     float acc = 0.f;
-    if (c.a_token >= 0 && lane < n) {
-      const int per = p.r / (kThreads / 32);
+    if (c.a_token >= 0) {
+      const int per = r / (kThreads / 32);
       const int k0 = wid * per;
-      const Tin* P = reinterpret_cast<const Tin*>(p.P) + (size_t)k0 * p.V + col0 + lane;
-      float pv[8];
-      for (int k = 0; k < per; k += 8) {
+      const Tin* P = reinterpret_cast<const Tin*>(p.P) + (size_t)k0 * p.V + col0 + (lane < n ? lane : 0);
+      for (int kb = 0; kb < per; kb += 32) {
+        float pv[32];
 #pragma unroll
-        for (int u8 = 0; u8 < 8; ++u8) pv[u8] = (k + u8 < per) ? to_f32(P[(size_t)(k + u8) * p.V]) : 0.f;
+        for (int u8 = 0; u8 < 32; ++u8) pv[u8] = (kb + u8 < per) ? to_f32(P[(size_t)(kb + u8) * p.V]) : 0.f;
 #pragma unroll
-        for (int u8 = 0; u8 < 8; ++u8)
-          if (k + u8 < per) acc = __fmaf_rn(s_arow[k0 + k + u8], pv[u8], acc);
+        for (int u8 = 0; u8 < 32; ++u8)
+          if (kb + u8 < per) acc = __fmaf_rn(s_arow[k0 + kb + u8], pv[u8], acc);
       }
     }
     s_part[wid][lane] = acc;
@@ -333,32 +356,42 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
   if (wid == 0) {
     float bsum = 0.f;
     for (int w = 0; w < kThreads / 32; ++w) bsum = __fadd_rn(bsum, s_part[w][lane]);
-    s_b[lane] = bsum;
-    s_z[lane] = (c.zrow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.zrow)[col0 + lane]) : 0.f;
-    s_t[lane] = (c.trow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.trow)[col0 + lane]) : 0.f;
-    __syncwarp();
-    if (lane == 0) {
-      ChunkRec chk;
-      chunk_record<false>(c, F32Src{s_z}, s_b, F32Src{s_t}, n, col0, chk, p.status, s_w);
-      s_ref = (c.mode == kSampleMarkov) ? chk.ref : 0;
+    // weights with the arithmetic of the chunk's record (idx -2: tensor-core fast path)
+    float w = 0.f;
+    int e = 0;
+    if (c.mode == kSampleMarkov) {
+      const ChunkRec cr = srec[chunk];
+      const int ref = cr.ref;
+      if (lane < n && ref != kEmptyRef) {
+        if (cr.idx == -2)
+          w = fast_w1(zl, bsum, make_g16(p.temperature[b]), (uint32_t)ref << 23);
+        else
+          w = weight_rel(zl, bsum, c.g, ref);
+      }
+      e = (ref == kEmptyRef) ? -300 : max(ref - N, -300);
+    } else if (lane < n) {
+      w = weight_rel(tl, 0.f, c.g, c.Np);
+      if (c.mode == kResidual) {
+        const float wq = weight_rel(zl, bsum, c.g, c.Nq);
+        float d = __fmaf_rn(-wq, c.Rhi, w);
+        d = __fmaf_rn(-wq, c.Rlo, d);
+        w = fmaxf(d, 0.f);
+      }
     }
-    __syncwarp();
-    const int e = (c.mode == kSampleMarkov) ? max(s_ref - N, -300) : 0;
-    const float w = lane < n ? s_w[lane] : 0.f;
+    if (!(w >= 0.f) || !isfinite(w)) w = 0.f;
     DF pre = {ldexpf(w, e), 0.f};
     for (int o = 1; o < 32; o <<= 1) {
       const DF v = shfl_up_df(pre, o);
       if (lane >= o) pre = df_add(v, pre);
     }
     const DF incl = df_add(s_excl, pre);
-    const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && df_to_double(incl) > theta);
+    const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && df_gt(incl, theta));
     const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
-    int xl = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+    const int xl = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
     const float wx = __shfl_sync(0xffffffffu, w, xl);
-    const int x = col0 + xl;
     if (lane == 0) {
       if (!pos) report(p.status, kErrNonfinite);
-      p.tokens_out[c.out_index] = x;
+      p.tokens_out[c.out_index] = col0 + xl;
       if (p.src == 0) {
         p.q_token[c.out_index] = (float)(ldexp((double)wx, e) / Sd);
         ds_row_stats st;
@@ -369,28 +402,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
         p.q_stats[c.out_index] = st;
       }
     }
-    if (stage_next) write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, x, lane);
   }
-}
-
-// Stage E[anchor] rows as the first step's A operand (rows beyond B zeroed).
-__global__ void __launch_bounds__(128) draft_prep_kernel(const int32_t* anchor,
-                                                         const __nv_bfloat16* E, int B, int V,
-                                                         int r, uint8_t* astage, int rows,
-                                                         int32_t* status) {
-  sm100::pdl_launch_dependents();
-  sm100::pdl_wait();
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  int tok = -1;
-  if (row < B) {
-    tok = anchor[row];
-    if (tok < 0 || tok >= V) {
-      if (lane == 0) report(status, kErrBounds);
-      tok = 0;
-    }
-  }
-  write_a_row(astage, E, r, row, tok, lane);
 }
 
 }  // namespace
@@ -446,14 +458,6 @@ cudaError_t launch_sample_locate(const SampleParams& p, cudaStream_t s) {
       sample_locate_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (attr != cudaSuccess) return attr;
   return launch_pdl(sample_locate_kernel<float>, dim3(p.B), dim3(kThreads), smem, s, p);
-}
-
-cudaError_t launch_draft_prep(const int32_t* anchor, const void* E, int32_t B, int32_t V, int32_t r,
-                              uint8_t* astage, int32_t* status, cudaStream_t s) {
-  const int rows = ((B + 127) / 128) * 128;
-  return launch_pdl(draft_prep_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, anchor,
-                    reinterpret_cast<const __nv_bfloat16*>(E), (int)B, (int)V, (int)r, astage, rows,
-                    status);
 }
 
 }  // namespace ds

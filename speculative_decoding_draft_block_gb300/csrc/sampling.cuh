@@ -199,22 +199,5 @@ __device__ __forceinline__ void chunk_record(const RowCtx& c, ZS z, const float*
   if (bad) report(status, kErrNonfinite);
 }
 
-// Write E[tok] (r bf16 values, r % 64 == 0) into the 128B-swizzled K-major
-// A-operand staging of its M-tile: [kb][row/8][row%8][chunk ^ (row%8)][16 B].
-// One warp; lane i copies 16-byte chunks i, i+32, ...
-__device__ __forceinline__ void write_a_row(uint8_t* astage, const __nv_bfloat16* E, int r, int b,
-                                            int tok, int lane) {
-  const int mt = b >> 7, m = b & 127;
-  const int nkb = r >> 6;
-  uint8_t* tile = astage + (size_t)mt * nkb * 16384;
-  for (int q = lane; q < nkb * 8; q += 32) {
-    const int kb = q >> 3, ch = q & 7;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (tok >= 0) v = __ldg(reinterpret_cast<const uint4*>(E + (size_t)tok * r + kb * 64 + ch * 8));
-    uint8_t* dst = tile + kb * 16384 + (m >> 3) * 1024 + (m & 7) * 128 + ((ch ^ (m & 7)) << 4);
-    *reinterpret_cast<uint4*>(dst) = v;
-  }
-}
-
 }  // namespace
 }  // namespace ds

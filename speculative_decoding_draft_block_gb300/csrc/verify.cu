@@ -158,17 +158,12 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
   if (tid == 0) p.vrows[(size_t)b * (p.K + 1) + j] = out;
 }
 
-// One warp per request: lane 0 walks the accept flags; the warp then stages
-// the A-operand row of the final draw (E[x_{k-1}] for a residual draw).
+// One warp per request: lane 0 walks the accept flags and writes the final
+// draw's descriptor; the warp writes the emitted-token row.
 __global__ void __launch_bounds__(128) verify_finalize_kernel(VerifyParams p) {
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int rows = ((p.B + 127) / 128) * 128;
-  if (b >= rows) return;
-  if (b >= p.B) {
-    if (p.astage) write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, -1, lane);
-    return;
-  }
+  if (b >= p.B) return;
   const int K = p.K;
   int L = p.sched_len[b];
   L = L < 0 ? 0 : (L > K ? K : L);
@@ -209,11 +204,6 @@ __global__ void __launch_bounds__(128) verify_finalize_kernel(VerifyParams p) {
     p.num_emitted[b] = a + 1;
     p.final_desc[b] = d;
   }
-  if (p.astage) {
-    int tok = d.a_token;
-    if (tok >= p.V) tok = 0;
-    write_a_row(p.astage, reinterpret_cast<const __nv_bfloat16*>(p.E), p.r, b, tok, lane);
-  }
 }
 
 }  // namespace
@@ -228,8 +218,7 @@ cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s) {
-  const int rows = ((p.B + 127) / 128) * 128;
-  verify_finalize_kernel<<<(rows + 3) / 4, 128, 0, s>>>(p);
+  verify_finalize_kernel<<<(p.B + 3) / 4, 128, 0, s>>>(p);
   return cudaGetLastError();
 }
 

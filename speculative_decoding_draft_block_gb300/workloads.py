@@ -80,7 +80,13 @@ B256 = _cfg("B256_K32_V151936", B=256, K=32, V=151936, r=256, d=4096, bf16=True,
             bump0=6.0, bump_decay=0.2, sigma_b=(0.2, 1.0), sts=(0.8, 1.5), temps=(0.0, 0.6, 1.0),
             sps_kind="hyperbolic", sps_nmax=256 * 33, conf_bias=3.0, seed=1004)
 
-WORKLOADS = {w.name: w for w in (TINY, B32, B128, B512, B256)}
+# Same per-step shape as the B=128 workload with fewer block positions: for
+# profiler captures, which replay each kernel many times and must stay small.
+B128_K4 = _cfg("B128_K4_V151936", B=128, K=4, V=151936, r=256, d=4096, bf16=True, sigma_z=1.5,
+               bump0=5.0, bump_decay=0.25, sigma_b=(0.3, 1.2), sts=(0.8, 1.5), temps=(1.0,),
+               sps_kind="hyperbolic", sps_nmax=128 * 5, conf_bias=3.0, seed=1005)
+
+WORKLOADS = {w.name: w for w in (TINY, B32, B128, B512, B256, B128_K4)}
 
 
 def scaled(w, **changes):
