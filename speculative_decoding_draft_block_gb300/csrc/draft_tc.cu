@@ -6,16 +6,17 @@
 // softmax((z_k + bias) / T). This kernel computes that product on the 5th-gen
 // tensor cores and reduces it straight out of TMEM:
 //
-//   warp 0      producer: TMA loads of P tiles (r x 128 tokens, 128B-swizzled,
-//               MN-major, L2 evict-last: P is re-read every step) and of the
-//               base-logit tiles (128 rows x 128 tokens, evict-first), and one
-//               bulk copy of the A operand (E rows of the previous tokens,
-//               pre-swizzled by the previous locate kernel).
+//   warp 0      producer: TMA loads of P tiles (64 k-rows x 128 tokens per
+//               stage, 128B-swizzled, MN-major, L2 evict-last: P is re-read
+//               every step) and of the base-logit tiles (128 rows x 64 tokens
+//               per slot, evict-first).
 //   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> f32),
 //               M = 128 requests, N = 128 tokens, K = r in steps of 16, into one
 //               of two TMEM accumulators (double-buffered against the epilogue).
-//   warps 2-17  epilogue: tcgen05.ld of a 32-lane x 32-column slice each, add
-//               the base logits from shared memory, and reduce every
+//   warps 2..   epilogue (kEpiWarps warps): gather the A operand (E rows of the
+//               conditioning tokens, stored 128B-swizzled K-major) with 16-byte
+//               loads at each M-tile; then per tile tcgen05.ld of their TMEM
+//               slice, add the base logits from shared memory, and reduce every
 //               (request, 32-token chunk) to its record: the double-float sum
 //               of 2^(t - ref) with an integer reference (sampling rows), or
 //               its largest logit (greedy rows). Nothing V-wide is stored.
@@ -43,8 +44,10 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcThreads = 576;  // 18 warps
-constexpr int kEpiWarps = 16;
+constexpr int kEpiWarps = 8;                    // multiple of 4 (TMEM lane quadrants)
+constexpr int kColGroups = kEpiWarps / 4;       // column groups per lane quadrant
+constexpr int kChunks = 4 / kColGroups;         // 32-token chunks per thread per tile
+constexpr int kTcThreads = 64 + 32 * kEpiWarps;
 constexpr int kTileN = 128;
 constexpr int kPStages = 6;           // 64 k-rows x 128 tokens of P each
 constexpr int kZSlots = 4;            // 128 rows x 64 tokens of logits each
@@ -69,17 +72,28 @@ struct Shared {
   uint64_t t_full[kAccum], t_empty[kAccum];
   uint32_t tmem_slot;
   int abort_flag;
+  int tok[128];
 };
 
+// Bounded wait (about a second at most): the thread sleeps in try_wait with a
+// 20 us hint (it wakes as soon as the phase completes), so waiting warps do
+// not take issue slots from the epilogue.
+constexpr uint32_t kWaitPolls = 1u << 16;
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          int32_t* status) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 255 && *abort_flag) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((i & 15) == 15 && *abort_flag) return false;
   }
   *abort_flag = 1;
   report(status, kErrTimeout);
   return false;
+}
+
+// Named barrier over the epilogue warps only.
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
 }
 
 // What the epilogue keeps about its row (a trimmed RowCtx, to save registers).
@@ -91,124 +105,96 @@ struct EpiRow {
   float Rhi, Rlo;
 };
 
-// General path for one 16-column half (every mode; ragged chunks; chunks with
-// -inf, out-of-range or non-finite logits).
-__device__ __forceinline__ void slow_half(const EpiRow& c, int h, const uint32_t* zp,
-                                          const uint32_t* tp, const float* bh, int n, int col0,
-                                          int ref, DF& s, DF& best, int& bi, bool& bad) {
-  const Bf16Src z{zp}, t{tp};
-  if (c.mode == kSampleMarkov) {
-    if (ref == kEmptyRef) return;
+// Fast path of a full sampling chunk (bf16 logits; see fastpath.cuh). False
+// when the chunk needs the general path.
+__device__ __forceinline__ bool sample_chunk_fast(const G16& g16, const uint32_t* zp,
+                                                  const uint32_t* braw, ChunkRec& rec) {
+  int fref = 0;
+  if (!fast_chunk_ok(zp, g16, fref)) return false;
+  const FastConsts k = make_fast_consts(g16, fref);
+  float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (h * 16 + j < n) df_accumulate(s, weight_rel(z(h * 16 + j), bh[j], c.g, ref));
-  } else if (c.mode == kGreedyMarkov) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int jj = h * 16 + j;
-      if (jj < n) {
-        const float zj = z(jj);
-        bad |= bad_logit(zj) || !(bh[j] == bh[j]);
-        const DF l = (zj == kNegInf) ? DF{kNegInf, 0.f} : two_sum(zj, bh[j]);
-        if (bi < 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
-          best = l;
-          bi = col0 + jj;
-        }
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int jj = h * 16 + j;
-      if (jj < n) {
-        float w = weight_rel(t(jj), 0.f, c.g, c.Np);
-        if (c.mode == kResidual) {
-          const float wq = weight_rel(z(jj), bh[j], c.g, c.Nq);
-          float d = __fmaf_rn(-wq, c.Rhi, w);
-          d = __fmaf_rn(-wq, c.Rlo, d);
-          bad |= !(d == d);
-          w = fmaxf(d, 0.f);
-        }
-        df_accumulate(s, w);
-      }
-    }
-  }
+  for (int i = 0; i < 16; ++i)
+    fast_pair(zp[i], __uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1]), k, shi, slo);
+  const float hi = __fadd_rn(shi.x, shi.y);  // exact: multiples of 2^-15 below 1024
+  const float lo = __fadd_rn(slo.x, slo.y);
+  if (!(shi.x >= 0.f && shi.x < kFastHiLimit && shi.y >= 0.f && shi.y < kFastHiLimit &&
+        isfinite(lo)))
+    return false;
+  const DF r = fast_two_sum(hi, lo);
+  rec.hi = r.hi;
+  rec.lo = r.lo;
+  rec.ref = fref;
+  rec.idx = -2;  // fast-path record
+  return true;
 }
 
-// Reduce this thread's (row, 32-token chunk) slice of a finished accumulator.
-// The bias is read from TMEM in two 16-column halves; tcgen05.ld is
-// warp-collective, so every lane of the warp issues the same loads.
-__device__ __forceinline__ void epi_chunk(const EpiRow& c, bool active, const uint32_t* zp,
-                                          const uint32_t* tp, uint32_t taddr, int n, int col0,
-                                          ChunkRec& rec, bool& bad) {
-  const bool sample = active && c.mode == kSampleMarkov;
-  int fref = 0;
-  bool fast = (n == 32) && sample && fast_chunk_ok(zp, c.g16, fref);
-  bool done = false;
-  if (__any_sync(0xffffffffu, fast)) {
-    const FastConsts k = make_fast_consts(c.g16, fref);
-    float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
+// Greedy chunk: the largest z + bias as a double-float and its first token.
+// Same ordering as the general path; false on a NaN/+inf input, which the
+// general path then reports.
+__device__ __forceinline__ bool greedy_chunk_fast(const uint32_t* zp, const uint32_t* braw,
+                                                  int col0, ChunkRec& rec) {
+  DF best = {kNegInf, 0.f};
+  int bj = 0;
+  bool bad = false;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float bh[16];
-      tmem_ld16(taddr + h * 16, bh);
-      if (fast) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) fast_pair(zp[h * 8 + i], bh[2 * i], bh[2 * i + 1], k, shi, slo);
-      }
-    }
-    if (fast) {
-      const float hi = __fadd_rn(shi.x, shi.y);  // exact: multiples of 2^-15 below 1024
-      const float lo = __fadd_rn(slo.x, slo.y);
-      if (shi.x >= 0.f && shi.x < kFastHiLimit && shi.y >= 0.f && shi.y < kFastHiLimit &&
-          isfinite(lo)) {
-        const DF r = fast_two_sum(hi, lo);
-        rec.hi = r.hi;
-        rec.lo = r.lo;
-        rec.ref = fref;
-        rec.idx = -2;  // fast-path record
-        done = true;
-      }
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t w = zp[j >> 1];
+    const float zj = __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+    const float bb = __uint_as_float(braw[j]);
+    bad |= bad_logit(zj) || !(bb == bb);
+    const DF l = (zj == kNegInf) ? DF{kNegInf, 0.f} : two_sum(zj, bb);
+    if (j == 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
+      best = l;
+      bj = j;
     }
   }
-  const bool slow = active && !done;
-  if (!__any_sync(0xffffffffu, slow)) return;
-  int ref = 0;
-  if (slow && c.mode == kSampleMarkov) {
-    const Bf16Src z{zp};
-    float amax = kNegInf;
+  rec.hi = best.hi;
+  rec.lo = best.lo;
+  rec.ref = 0;
+  rec.idx = col0 + bj;
+  return !bad;
+}
+
+// The general path for the lanes with need set (greedy and sampling chunks
+// the fast paths decline, ragged chunks, residual/bonus draws). Called by the
+// whole warp: it reloads the bias from TMEM (a warp-collective load) and the
+// logits from shared memory, so that the fast paths keep everything in
+// registers. zb / tb: this row's 128-byte logit rows in the (swizzled) slots.
+__device__ __noinline__ void slow_chunk_warp(EpiRow c, bool need, uint32_t taddr,
+                                             const uint8_t* zb, const uint8_t* tb, int ch0, int sw,
+                                             int n, int col0, ChunkRec* out, int32_t* status) {
+  uint32_t braw[32];
+  tmem_ld32_issue(taddr, braw);
+  tmem_ld_wait(braw);
+  if (!need) return;
+  float bias[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < n) amax = fmaxf(amax, scaled_hi(z(j), c.g));
-    ref = chunk_ref_from_max(amax);
-  }
-  DF s = {0.f, 0.f}, best = {kNegInf, 0.f};
-  int bi = -1;
+  for (int e = 0; e < 32; ++e) bias[e] = __uint_as_float(braw[e]);
+  uint32_t zp[16], tp[16];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float bh[16];
-    tmem_ld16(taddr + h * 16, bh);
-    if (slow) slow_half(c, h, zp, tp, bh, n, col0, ref, s, best, bi, bad);
+  for (int u = 0; u < 4; ++u) {
+    const int off = ((ch0 + u) ^ sw) << 4;
+    const uint4 v = *reinterpret_cast<const uint4*>(zb + off);
+    const uint4 t = *reinterpret_cast<const uint4*>(tb + off);
+    zp[4 * u] = v.x; zp[4 * u + 1] = v.y; zp[4 * u + 2] = v.z; zp[4 * u + 3] = v.w;
+    tp[4 * u] = t.x; tp[4 * u + 1] = t.y; tp[4 * u + 2] = t.z; tp[4 * u + 3] = t.w;
   }
-  if (!slow) return;
-  if (c.mode == kGreedyMarkov) {
-    rec.hi = best.hi;
-    rec.lo = best.lo;
-    rec.ref = 0;
-    rec.idx = bi;
-  } else {
-    if (c.mode == kSampleMarkov && ref == kEmptyRef) {
-      const Bf16Src z{zp};
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < n) bad |= !(z(j) == z(j));
-    }
-    bad |= !isfinite(s.hi);
-    rec.hi = s.hi;
-    rec.lo = s.lo;
-    rec.ref = (c.mode == kSampleMarkov) ? ref : 0;
-    rec.idx = -1;
-  }
+  RowCtx rc;
+  rc.mode = c.mode;
+  rc.a_token = -1;
+  rc.zrow = nullptr;
+  rc.trow = nullptr;
+  rc.g = c.g;
+  rc.Np = c.Np;
+  rc.Nq = c.Nq;
+  rc.Rhi = c.Rhi;
+  rc.Rlo = c.Rlo;
+  rc.upos = rc.ustage = 0;
+  rc.out_index = rc.zk = 0;
+  ChunkRec r;
+  chunk_record<false>(rc, Bf16Src{zp}, bias, Bf16Src{tp}, n, col0, r, status);
+  *out = r;
 }
 
 // Token whose E row forms A-operand row b of this launch (0 for padding rows).
@@ -221,13 +207,12 @@ __device__ __forceinline__ int a_token_for_row(const SampleParams& sp, int b) {
     const FinalDesc d = sp.final_desc[b];
     tok = (d.mode == kResidual && sp.temperature[b] != 0.f) ? d.a_token : 0;
   }
-  return (tok >= 0 && tok < sp.V) ? tok : 0;  // out-of-range ids are reported by the epilogue
+  return (tok >= 0 && tok < sp.V) ? tok : 0;  // out-of-range ids are reported by make_row_ctx
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     tile_tc_kernel(const TcParams prm, const __grid_constant__ CUtensorMap tmP,
-                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmT,
-                   const __grid_constant__ CUtensorMap tmE) {
+                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmT) {
   extern __shared__ uint8_t raw[];
   __shared__ Shared sh;
   const SampleParams& sp = prm.sp;
@@ -240,7 +225,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool draft = (sp.src == 0);
 
   if (threadIdx.x == 0) {
-    mbar_init(&sh.a_full, 1);
+    mbar_init(&sh.a_full, kEpiWarps);
     mbar_init(&sh.a_empty, 1);
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&sh.p_full[i], 1);
@@ -275,16 +260,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tmP);
       prefetch_tmap(&tmZ);
-      prefetch_tmap(&tmE);
       if (!draft) prefetch_tmap(&tmT);
     }
-    int cur_mt = -1;
-    uint32_t a_uses = 0, pc = 0, zc = 0;
-    bool waited = false, ok = true;
+    uint32_t pc = 0, zc = 0;
+    bool waited = draft, ok = true;  // a draft step's P and logits are inputs, not results
     for (int t = t0, i = 0; t < t1 && ok; ++t, ++i) {
       const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
       const int n0 = nt * kTileN;
-      // P: independent of earlier kernels, so the first tile's loads precede the PDL wait
       for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
         const uint32_t ps = pc % kPStages;
         if (lane == 0) {
@@ -298,29 +280,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (!ok) break;
-      if (!waited) {
-        pdl_wait();  // tokens and final-draw descriptors come from earlier kernels
-        waited = true;
-      }
-      if (mt != cur_mt) {
-        // A operand: gather E rows of this M-tile's conditioning tokens (128B-swizzled TMA rows)
-        if (lane == 0) {
-          if (cur_mt >= 0) ok = wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status);
-          if (ok) mbar_expect_tx(&sh.a_full, 128u * prm.nkb * 128u);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int rr = lane + 32 * u;
-          const int tok = a_token_for_row(sp, mt * 128 + rr);
-          for (int kb = 0; kb < prm.nkb; ++kb)
-            tma_load_2d(sA + kb * 16384 + rr * 128, &tmE, &sh.a_full, kb * 64, tok, pol_p);
-        }
-        ++a_uses;
-        cur_mt = mt;
-      }
       if (draft) {
         for (int nb = 0; nb < 2 && ok; ++nb, ++zc) {
           const uint32_t zs = zc % kZSlots;
@@ -335,8 +294,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
       } else {
-        // final draw: each request's own base and target rows, one 128-byte box per row
-        // and half; slots 0/1 hold the base-logit halves, slots 2/3 the target halves
+        if (!waited) {
+          pdl_wait();  // final-draw descriptors come from the finalize kernel
+          waited = true;
+        }
+        // each request's own base and target rows, one 128-byte box per row and
+        // half; slots 0/1 hold the base-logit halves, slots 2/3 the target halves
         if (lane == 0)
           for (int s = 0; s < kZSlots && ok; ++s)
             ok = wait_bar(&sh.z_empty[s], (i & 1) ^ 1, abort_flag, sp.status);
@@ -428,17 +391,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    pdl_wait();
-    const int ew = warp - 2, q = warp & 3, cg = ew >> 2, nb = cg >> 1;
+    pdl_wait();  // tokens and final-draw descriptors come from earlier kernels
+    const int ew = warp - 2, et = threadIdx.x - 64;
+    const int q = warp & 3, cg = ew >> 2;
     const int r_local = q * 32 + lane;
     int cur_mt = -1;
+    uint32_t a_uses = 0;
     EpiRow c;
     c.mode = kSkip;
-    bool bad = false;
     for (int t = t0, i = 0; t < t1; ++t, ++i) {
       const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
       const int row = mt * 128 + r_local;
       if (mt != cur_mt) {
+        // A operand of this M-tile: E rows of its conditioning tokens, written
+        // 128B-swizzled (16-byte chunk c of row m at c ^ (m & 7)) for the MMA.
+        if (a_uses > 0 && !wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status)) break;
+        if (et < 128) sh.tok[et] = a_token_for_row(sp, mt * 128 + et);
+        epi_sync();
+        const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(sp.E);
+        const int per_row = prm.nkb * 8;
+        const int n_a = 128 * per_row;
+        for (int base = 0; base < n_a; base += 8 * 32 * kEpiWarps) {
+          uint4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * 32 * kEpiWarps + et;
+            if (idx < n_a) {
+              const int m = idx / per_row, rem = idx - m * per_row;
+              v[u] = __ldg(reinterpret_cast<const uint4*>(E + (size_t)sh.tok[m] * sp.r + rem * 8));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * 32 * kEpiWarps + et;
+            if (idx < n_a) {
+              const int m = idx / per_row, rem = idx - m * per_row;
+              const int kb = rem >> 3, ch = rem & 7;
+              *reinterpret_cast<uint4*>(sA + kb * 16384 + m * 128 + ((ch ^ (m & 7)) << 4)) = v[u];
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.a_full);
+        ++a_uses;
+        epi_sync();  // the token list is rewritten at the next M-tile
         const RowCtx rc = make_row_ctx<__nv_bfloat16>(sp, row);
         c.mode = rc.mode;
         c.g = rc.g;
@@ -450,6 +447,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cur_mt = mt;
       }
       const uint32_t buf = i % kAccum;
+      // this thread's chunks: cg * kChunks .. + kChunks - 1, all in logit box nb
+      const int nb = (cg * kChunks) >> 1;
       const uint32_t zc = 2u * i + nb;
       const uint32_t zs = draft ? zc % kZSlots : nb;
       const uint32_t zph = draft ? (zc / kZSlots) & 1 : (i & 1);
@@ -457,49 +456,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!draft && !wait_bar(&sh.z_full[2 + nb], zph, abort_flag, sp.status)) break;
       if (!wait_bar(&sh.t_full[buf], (i / kAccum) & 1, abort_flag, sp.status)) break;
       tc_fence_after();
-      uint32_t zp[16], tp[16];
-      const int ch0 = (cg & 1) * 4;
-      const bool need_z = (c.mode == kGreedyMarkov || c.mode == kSampleMarkov || c.mode == kResidual);
-      const bool need_t = (c.mode == kResidual || c.mode == kBonus);
-      if (need_z) {
-        const uint8_t* zb = sZ + zs * kZSlot + r_local * 128;
+      __syncwarp();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * kTileN;
+      // bias of every chunk first (one wait for all TMEM loads)
+      uint32_t braw[kChunks][32];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 v = *reinterpret_cast<const uint4*>(zb + (((ch0 + u) ^ (r_local & 7)) << 4));
-          zp[4 * u] = v.x;
-          zp[4 * u + 1] = v.y;
-          zp[4 * u + 2] = v.z;
-          zp[4 * u + 3] = v.w;
-        }
-      }
-      if (need_t) {
-        const uint8_t* tb = sZ + (2 + nb) * kZSlot + r_local * 128;
+      for (int j = 0; j < kChunks; ++j) tmem_ld32_issue(tbase + (cg * kChunks + j) * 32, braw[j]);
+      tmem_ld_wait(braw[0]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 v = *reinterpret_cast<const uint4*>(tb + (((ch0 + u) ^ (r_local & 7)) << 4));
-          tp[4 * u] = v.x;
-          tp[4 * u + 1] = v.y;
-          tp[4 * u + 2] = v.z;
-          tp[4 * u + 3] = v.w;
+      for (int j = 1; j < kChunks; ++j) reg_dep32(braw[j]);
+      const uint8_t* zb = sZ + zs * kZSlot + r_local * 128;
+      const uint8_t* tb = sZ + (draft ? zs : 2 + nb) * kZSlot + r_local * 128;
+      const int sw = r_local & 7;
+#pragma unroll
+      for (int j = 0; j < kChunks; ++j) {
+        const int ch0 = ((cg * kChunks + j) & 1) * 4;
+        const int col0 = nt * kTileN + (cg * kChunks + j) * 32;
+        const bool active = row < sp.B && c.mode != kSkip && col0 < sp.V;
+        const int n = min(32, sp.V - col0);
+        ChunkRec* out = sp.chunks + (size_t)row * sp.n_chunks + (col0 >> 5);
+        bool done = !active;
+        if (active && n == 32 && (c.mode == kSampleMarkov || c.mode == kGreedyMarkov)) {
+          uint32_t zp[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 v = *reinterpret_cast<const uint4*>(zb + (((ch0 + u) ^ sw) << 4));
+            zp[4 * u] = v.x;
+            zp[4 * u + 1] = v.y;
+            zp[4 * u + 2] = v.z;
+            zp[4 * u + 3] = v.w;
+          }
+          ChunkRec rec;
+          done = (c.mode == kSampleMarkov) ? sample_chunk_fast(c.g16, zp, braw[j], rec)
+                                           : greedy_chunk_fast(zp, braw[j], col0, rec);
+          if (done) *out = rec;
         }
+        if (__any_sync(0xffffffffu, !done))
+          slow_chunk_warp(c, !done, tbase + (cg * kChunks + j) * 32, zb, tb, ch0, sw, n, col0, out,
+                          sp.status);
       }
+      // this warp is done with the tile's accumulator and logit slots
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&sh.t_empty[buf]);
         mbar_arrive(&sh.z_empty[zs]);
         if (!draft) mbar_arrive(&sh.z_empty[2 + nb]);
       }
-      const int col0 = nt * kTileN + cg * 32;
-      const bool active = row < sp.B && c.mode != kSkip && col0 < sp.V;
-      const int n = min(32, sp.V - col0);
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kTileN + cg * 32;
-      ChunkRec rec;
-      epi_chunk(c, active, zp, tp, taddr, n, col0, rec, bad);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
-      if (active) sp.chunks[(size_t)row * sp.n_chunks + (col0 >> 5)] = rec;
     }
-    if (bad) report(sp.status, kErrNonfinite);
   }
   __syncthreads();
   if (warp == 1) {
@@ -556,19 +560,13 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   prm.nkb = p.r / 64;
   prm.tiles = prm.n_mt * prm.n_nt;
 
-  CUtensorMap mP, mZ, mT, mE;
+  CUtensorMap mP, mZ, mT;
   const cuuint64_t V = (cuuint64_t)p.V;
   {
     const cuuint64_t dims[2] = {V, (cuuint64_t)p.r};
     const cuuint64_t str[1] = {V * 2};
     const cuuint32_t box[2] = {64, 64};
     if (!encode(&mP, p.P, 2, dims, str, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.r, V};
-    const cuuint64_t str[1] = {(cuuint64_t)p.r * 2};
-    const cuuint32_t box[2] = {64, 1};
-    if (!encode(&mE, p.E, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {V, (cuuint64_t)p.K, (cuuint64_t)p.B};
@@ -599,7 +597,7 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tile_tc_kernel, prm, mP, mZ, mT, mE);
+  return cudaLaunchKernelEx(&cfg, tile_tc_kernel, prm, mP, mZ, mT);
 }
 
 }  // namespace ds

@@ -58,22 +58,12 @@ __device__ __forceinline__ float fast_w1(float z, float b, G16 g, uint32_t ref23
 }
 
 struct FastConsts {
-  float2 G2, GL2, GF2, MG2, NMG2, NEG1, C2, NC2;
+  float G, gl, gf;
   uint32_t ref23;
 };
 
 __device__ __forceinline__ FastConsts make_fast_consts(G16 g, int ref) {
-  FastConsts k;
-  k.G2 = make_float2(g.G, g.G);
-  k.GL2 = make_float2(g.gl, g.gl);
-  k.GF2 = make_float2(g.gf, g.gf);
-  k.MG2 = make_float2(kMagic, kMagic);
-  k.NMG2 = make_float2(-kMagic, -kMagic);
-  k.NEG1 = make_float2(-1.0f, -1.0f);
-  k.C2 = make_float2(kGrid, kGrid);
-  k.NC2 = make_float2(-kGrid, -kGrid);
-  k.ref23 = (uint32_t)ref << 23;
-  return k;
+  return {g.G, g.gl, g.gf, (uint32_t)ref << 23};
 }
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
@@ -84,20 +74,20 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
 __device__ __forceinline__ void fast_pair(uint32_t zw, float b0, float b1, const FastConsts& k,
                                           float2& shi, float2& slo) {
   const float2 z2 = unpack_bf16x2(zw);
-  const float2 a2 = __fmul2_rn(z2, k.G2);
-  const float2 t2 = __fmul2_rn(make_float2(b0, b1), k.GF2);
-  const float2 tl2 = __ffma2_rn(z2, k.GL2, t2);
-  const float2 m2 = __fadd2_rn(a2, k.MG2);
-  const float2 kf2 = __fadd2_rn(m2, k.NMG2);
-  const float2 d2 = __ffma2_rn(kf2, k.NEG1, a2);
+  const float2 a2 = __fmul2_rn(z2, make_float2(k.G, k.G));
+  const float2 t2 = __fmul2_rn(make_float2(b0, b1), make_float2(k.gf, k.gf));
+  const float2 tl2 = __ffma2_rn(z2, make_float2(k.gl, k.gl), t2);
+  const float2 m2 = __fadd2_rn(a2, make_float2(kMagic, kMagic));
+  const float2 kf2 = __fadd2_rn(m2, make_float2(-kMagic, -kMagic));
+  const float2 d2 = __ffma2_rn(kf2, make_float2(-1.0f, -1.0f), a2);
   const float2 f2 = __fadd2_rn(d2, tl2);
   const float p0 = ex2_approx(f2.x), p1 = ex2_approx(f2.y);
   const float2 w2 =
       make_float2(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(m2.x) << 23) - k.ref23),
                   __uint_as_float(__float_as_uint(p1) + (__float_as_uint(m2.y) << 23) - k.ref23));
-  const float2 tt = __fadd2_rn(w2, k.C2);
-  const float2 wh = __fadd2_rn(tt, k.NC2);
-  const float2 wl = __ffma2_rn(wh, k.NEG1, w2);
+  const float2 tt = __fadd2_rn(w2, make_float2(kGrid, kGrid));
+  const float2 wh = __fadd2_rn(tt, make_float2(-kGrid, -kGrid));
+  const float2 wl = __ffma2_rn(wh, make_float2(-1.0f, -1.0f), w2);
   shi = __fadd2_rn(shi, wh);
   slo = __fadd2_rn(slo, wl);
 }
