@@ -52,26 +52,30 @@ bool shape_ok(int32_t B, int32_t K, int32_t V, int32_t r) {
 
 ds_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DS_OK : DS_ERR_CUDA; }
 
-// Draft workspace: two record buffers, used by alternating steps so that a
-// step's records are never overwritten while the previous locate still reads them.
+// Draft workspace: two sets of chunk and group records, used by alternating
+// steps so that a step's records are never overwritten while the previous
+// locate still reads them.
 struct DraftLayout {
-  size_t rec0, rec1, total;
+  size_t rec[2], sup[2], total;
 };
 
 DraftLayout draft_layout(int32_t B, int32_t V, int32_t r) {
   (void)r;
   DraftLayout l;
   const size_t rec = align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
-  l.rec0 = 0;
-  l.rec1 = rec;
-  l.total = 2 * rec;
+  const size_t sup = align_up((size_t)B * sup_stride_for(V) * sizeof(ChunkRec));
+  l.rec[0] = 0;
+  l.rec[1] = rec;
+  l.sup[0] = 2 * rec;
+  l.sup[1] = 2 * rec + sup;
+  l.total = 2 * rec + 2 * sup;
   return l;
 }
 
 size_t draft_ws(int32_t B, int32_t V, int32_t r) { return draft_layout(B, V, r).total; }
 
 struct VerifyLayout {
-  size_t vrows, desc, chunks, total;
+  size_t vrows, desc, chunks, supers, total;
 };
 
 VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
@@ -80,7 +84,8 @@ VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
   l.desc = l.vrows + align_up((size_t)B * (K + 1) * sizeof(VRow));
   l.chunks = l.desc + align_up((size_t)B * sizeof(FinalDesc));
   (void)r;
-  l.total = l.chunks + align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
+  l.supers = l.chunks + align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
+  l.total = l.supers + align_up((size_t)B * sup_stride_for(V) * sizeof(ChunkRec));
   return l;
 }
 
@@ -148,10 +153,15 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   p.q_token = a->q_token;
   p.q_stats = a->q_stats;
   p.status = a->status;
+  if (tc)
+    tc_group_layout(p);
+  else
+    simt_group_layout(p);
   const cudaStream_t s = (cudaStream_t)stream;
   for (int k = 1; k <= a->K; ++k) {
     p.step = k;
-    p.chunks = reinterpret_cast<ChunkRec*>(ws + ((k & 1) ? l.rec1 : l.rec0));
+    p.chunks = reinterpret_cast<ChunkRec*>(ws + l.rec[k & 1]);
+    p.supers = reinterpret_cast<ChunkRec*>(ws + l.sup[k & 1]);
     cudaError_t e = tc ? launch_tile_tc(p, s) : launch_sample_tile(p, s);
     if (e != cudaSuccess) return DS_ERR_CUDA;
     e = launch_sample_locate(p, s);
@@ -280,6 +290,11 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   p.temperature = a->temperature;
   p.final_desc = v.final_desc;
   p.chunks = reinterpret_cast<ChunkRec*>(ws + l.chunks);
+  p.supers = reinterpret_cast<ChunkRec*>(ws + l.supers);
+  if (tc)
+    tc_group_layout(p);
+  else
+    simt_group_layout(p);
   p.seed = a->seed;
   p.tokens_out = a->out_tokens;
   p.status = a->status;

@@ -105,18 +105,46 @@ __device__ __forceinline__ DF df_scale2(DF a, int e) {  // exact power-of-two sc
   return {ldexpf(a.hi, e), ldexpf(a.lo, e)};
 }
 
-__device__ __forceinline__ double df_to_double(DF a) { return (double)a.hi + (double)a.lo; }
+// a * b as a double-float (TwoProduct of the high words, cross terms added).
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  float e = __fmaf_rn(a.hi, b.hi, -p);
+  e = __fmaf_rn(a.hi, b.lo, e);
+  e = __fmaf_rn(a.lo, b.hi, e);
+  return fast_two_sum(p, e);
+}
+
+// a < b for double-floats.
+__device__ __forceinline__ bool df_lt(DF a, DF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+
+// x / S for a float x and a double-float S > 0, to ~2^-23 relative.
+__device__ __forceinline__ float div_by_df(float x, DF S) {
+  const float q = __fdiv_rn(x, S.hi);
+  return __fmaf_rn(-q, __fdiv_rn(S.lo, S.hi), q);
+}
 
 // ---- log2(e) / T as a double-float -----------------------------------------
+//
+// Everything on the device is float or double-float: double precision runs at
+// a small fraction of the float rate on this part and sits on the latency path
+// of every sampling step.
 
 struct Gscale {
   float hi, lo;
 };
 
+// log2(e) = kLog2eHi + kLog2eLo (the float nearest, and the rest).
+#define kLog2eHi __uint_as_float(0x3fb8aa3bu)
+#define kLog2eLo __uint_as_float(0x32a57060u)
+
+// g = log2(e) / T to ~2^-47 relative: q = RN(hi / T), the remainder hi - q*T
+// is exact (FMA), and the remainder plus lo divided by T gives the low word.
 __device__ __forceinline__ Gscale make_gscale(float T) {
-  const double g = 1.4426950408889634073599246810019 / (double)T;
-  const float hi = (float)g;
-  return {hi, (float)(g - (double)hi)};
+  const float q = __fdiv_rn(kLog2eHi, T);
+  const float rem = __fadd_rn(__fmaf_rn(-q, T, kLog2eHi), kLog2eLo);
+  const float ql = __fdiv_rn(rem, T);
+  const float hi = __fadd_rn(q, ql);
+  return {hi, __fsub_rn(ql, __fsub_rn(hi, q))};
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -151,9 +179,14 @@ __device__ __forceinline__ float scaled_hi(float z, Gscale g) { return __fmul_rn
 
 // ---- uniform ---------------------------------------------------------------
 
-__device__ __forceinline__ double uniform_dev(uint64_t seed, uint32_t request,
-                                              uint32_t position, uint32_t stage) {
-  return uniform_from_word(philox_word(seed, request, position, stage));
+// u = (w + 1/2) * 2^-32 of the stream's first word, exactly, as a double-float:
+// w = a * 2^16 + c gives u = a * 2^-16 + (c + 1/2) * 2^-32 (both terms exact).
+__device__ __forceinline__ DF uniform_df(uint64_t seed, uint32_t request, uint32_t position,
+                                         uint32_t stage) {
+  const uint32_t w = philox_word(seed, request, position, stage);
+  const float a = __uint2float_rn(w >> 16) * 1.52587890625e-05f;               // 2^-16
+  const float c = (__uint2float_rn(w & 0xffffu) + 0.5f) * 2.3283064365386963e-10f;  // 2^-32
+  return fast_two_sum(a, c);
 }
 
 // Non-finite check for logits: NaN or +inf is an error; -inf is allowed.

@@ -48,6 +48,7 @@ constexpr int kEpiWarps = 8;                    // multiple of 4 (TMEM lane quad
 constexpr int kColGroups = kEpiWarps / 4;       // column groups per lane quadrant
 constexpr int kChunks = 4 / kColGroups;         // 32-token chunks per thread per tile
 constexpr int kTcThreads = 64 + 32 * kEpiWarps;
+constexpr int kUnrollChunks = 1;                // code size over TMEM-load overlap
 constexpr int kTileN = 128;
 constexpr int kPStages = 6;           // 64 k-rows x 128 tokens of P each
 constexpr int kZSlots = 4;            // 128 rows x 64 tokens of logits each
@@ -70,6 +71,7 @@ struct Shared {
   uint64_t p_full[kPStages], p_empty[kPStages];
   uint64_t z_full[kZSlots], z_empty[kZSlots];
   uint64_t t_full[kAccum], t_empty[kAccum];
+  uint64_t x_bar;  // barrier of the epilogue threads (all arrive)
   uint32_t tmem_slot;
   int abort_flag;
   int tok[128];
@@ -91,9 +93,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return false;
 }
 
-// Named barrier over the epilogue warps only.
-__device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+// Barrier over the epilogue threads only, bounded like every other wait.
+__device__ __forceinline__ bool epi_barrier(Shared& sh, uint32_t& ph, volatile int* abort_flag,
+                                            int32_t* status) {
+  mbar_arrive(&sh.x_bar);
+  const bool ok = wait_bar(&sh.x_bar, ph & 1, abort_flag, status);
+  ++ph;
+  return ok;
 }
 
 // What the epilogue keeps about its row (a trimmed RowCtx, to save registers).
@@ -161,13 +167,13 @@ __device__ __forceinline__ bool greedy_chunk_fast(const uint32_t* zp, const uint
 // whole warp: it reloads the bias from TMEM (a warp-collective load) and the
 // logits from shared memory, so that the fast paths keep everything in
 // registers. zb / tb: this row's 128-byte logit rows in the (swizzled) slots.
-__device__ __noinline__ void slow_chunk_warp(EpiRow c, bool need, uint32_t taddr,
+__device__ __noinline__ ChunkRec slow_chunk_warp(EpiRow c, bool need, uint32_t taddr,
                                              const uint8_t* zb, const uint8_t* tb, int ch0, int sw,
                                              int n, int col0, ChunkRec* out, int32_t* status) {
   uint32_t braw[32];
   tmem_ld32_issue(taddr, braw);
   tmem_ld_wait(braw);
-  if (!need) return;
+  if (!need) return group_empty();
   float bias[32];
 #pragma unroll
   for (int e = 0; e < 32; ++e) bias[e] = __uint_as_float(braw[e]);
@@ -195,6 +201,7 @@ __device__ __noinline__ void slow_chunk_warp(EpiRow c, bool need, uint32_t taddr
   ChunkRec r;
   chunk_record<false>(rc, Bf16Src{zp}, bias, Bf16Src{tp}, n, col0, r, status);
   *out = r;
+  return r;
 }
 
 // Token whose E row forms A-operand row b of this launch (0 for padding rows).
@@ -239,6 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sh.t_full[i], 1);
       mbar_init(&sh.t_empty[i], kEpiWarps);
     }
+    mbar_init(&sh.x_bar, 32 * kEpiWarps);
     sh.abort_flag = 0;
     fence_barrier_init();
   }
@@ -396,9 +404,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3, cg = ew >> 2;
     const int r_local = q * 32 + lane;
     int cur_mt = -1;
-    uint32_t a_uses = 0;
+    uint32_t a_uses = 0, xph = 0;
     EpiRow c;
     c.mode = kSkip;
+    ChunkRec gacc = group_empty();  // this thread's chunks of the current M-tile
     for (int t = t0, i = 0; t < t1; ++t, ++i) {
       const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
       const int row = mt * 128 + r_local;
@@ -407,7 +416,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // 128B-swizzled (16-byte chunk c of row m at c ^ (m & 7)) for the MMA.
         if (a_uses > 0 && !wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status)) break;
         if (et < 128) sh.tok[et] = a_token_for_row(sp, mt * 128 + et);
-        epi_sync();
+        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
         const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(sp.E);
         const int per_row = prm.nkb * 8;
         const int n_a = 128 * per_row;
@@ -435,7 +444,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.a_full);
         ++a_uses;
-        epi_sync();  // the token list is rewritten at the next M-tile
+        // the token list is rewritten at the next M-tile
+        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
         const RowCtx rc = make_row_ctx<__nv_bfloat16>(sp, row);
         c.mode = rc.mode;
         c.g = rc.g;
@@ -445,6 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         c.Rhi = rc.Rhi;
         c.Rlo = rc.Rlo;
         cur_mt = mt;
+        gacc = group_empty();
       }
       const uint32_t buf = i % kAccum;
       // this thread's chunks: cg * kChunks .. + kChunks - 1, all in logit box nb
@@ -458,18 +469,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       __syncwarp();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * kTileN;
-      // bias of every chunk first (one wait for all TMEM loads)
-      uint32_t braw[kChunks][32];
-#pragma unroll
-      for (int j = 0; j < kChunks; ++j) tmem_ld32_issue(tbase + (cg * kChunks + j) * 32, braw[j]);
-      tmem_ld_wait(braw[0]);
-#pragma unroll
-      for (int j = 1; j < kChunks; ++j) reg_dep32(braw[j]);
       const uint8_t* zb = sZ + zs * kZSlot + r_local * 128;
       const uint8_t* tb = sZ + (draft ? zs : 2 + nb) * kZSlot + r_local * 128;
       const int sw = r_local & 7;
-#pragma unroll
+#pragma unroll kUnrollChunks
       for (int j = 0; j < kChunks; ++j) {
+        uint32_t braw[32];
+        tmem_ld32_issue(tbase + (cg * kChunks + j) * 32, braw);
+        tmem_ld_wait(braw);
         const int ch0 = ((cg * kChunks + j) & 1) * 4;
         const int col0 = nt * kTileN + (cg * kChunks + j) * 32;
         const bool active = row < sp.B && c.mode != kSkip && col0 < sp.V;
@@ -487,13 +494,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             zp[4 * u + 3] = v.w;
           }
           ChunkRec rec;
-          done = (c.mode == kSampleMarkov) ? sample_chunk_fast(c.g16, zp, braw[j], rec)
-                                           : greedy_chunk_fast(zp, braw[j], col0, rec);
-          if (done) *out = rec;
+          done = (c.mode == kSampleMarkov) ? sample_chunk_fast(c.g16, zp, braw, rec)
+                                           : greedy_chunk_fast(zp, braw, col0, rec);
+          if (done) {
+            *out = rec;
+            group_merge(c.mode, gacc, rec);
+          }
         }
-        if (__any_sync(0xffffffffu, !done))
-          slow_chunk_warp(c, !done, tbase + (cg * kChunks + j) * 32, zb, tb, ch0, sw, n, col0, out,
-                          sp.status);
+        if (__any_sync(0xffffffffu, !done)) {
+          const ChunkRec rec = slow_chunk_warp(c, !done, tbase + (cg * kChunks + j) * 32, zb, tb,
+                                               ch0, sw, n, col0, out, sp.status);
+          if (!done) group_merge(c.mode, gacc, rec);
+        }
+      }
+      if (t + 1 == t1 || (t + 1) / prm.n_nt != mt) {
+        // Group record of each row over this CTA's tiles of the M-tile: the
+        // column groups' partial records meet in the row's line of the tile's
+        // first logit slot (consumed, and not released until after this).
+        uint8_t* xb = sZ + (draft ? (2u * i) % kZSlots : 0u) * kZSlot + r_local * 128;
+        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
+        if (cg > 0) *reinterpret_cast<ChunkRec*>(xb + 16 * cg) = gacc;
+        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
+        if (cg == 0 && row < sp.B && c.mode != kSkip) {
+          ChunkRec g = gacc;
+#pragma unroll
+          for (int k = 1; k < kColGroups; ++k)
+            group_merge(c.mode, g, *reinterpret_cast<const ChunkRec*>(xb + 16 * k));
+          sp.supers[(size_t)row * sp.sup_stride + (blockIdx.x - first_group(sp, mt))] = g;
+        }
+        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
       }
       // this warp is done with the tile's accumulator and logit slots
       tc_fence_before();
@@ -545,6 +574,17 @@ int num_sms() {
 
 }  // namespace
 
+void tc_group_layout(SampleParams& p) {
+  static const int sms = num_sms();
+  p.sup_stride = sup_stride_for(p.V);
+  p.sup_nt = (p.V + kTileN - 1) / kTileN;
+  p.sup_rows = 128;
+  p.sup_tiles = p.sup_nt * ((p.B + 127) / 128);
+  int g = sms < kMaxTcGroups ? sms : kMaxTcGroups;
+  p.sup_groups = p.sup_tiles < g ? p.sup_tiles : g;
+  p.sup_cpt = kTileN / 32;
+}
+
 bool tc_path_supported(int32_t dtype, int32_t r) {
   return dtype == DS_BF16 && r % 64 == 0 && r >= 64 && r <= 256;
 }
@@ -584,8 +624,8 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
     const cuuint32_t box[3] = {64, 1, 1};
     if (!encode(&mT, p.target_logits, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  static int sms = num_sms();
-  const int grid = prm.tiles < sms ? prm.tiles : sms;
+  const int grid = p.sup_groups;
+  if (p.sup_tiles != prm.tiles || grid < 1 || grid > prm.tiles) return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

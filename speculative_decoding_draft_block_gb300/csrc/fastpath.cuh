@@ -38,10 +38,9 @@ struct G16 {
 };
 
 __device__ __forceinline__ G16 make_g16(float T) {
-  const double g = 1.4426950408889634073599246810019 / (double)T;
-  const float gf = (float)g;
-  const float G = __uint_as_float(__float_as_uint(gf) & 0xFFFFFF00u);
-  return {G, (float)(g - (double)G), gf};
+  const Gscale g = make_gscale(T);
+  const float G = __uint_as_float(__float_as_uint(g.hi) & 0xFFFFFF00u);
+  return {G, __fadd_rn(__fsub_rn(g.hi, G), g.lo), g.hi};  // g.hi - G is exact
 }
 
 // Scalar weight, bit-identical to one lane of fast_w2.

@@ -58,6 +58,16 @@ struct SampleParams {
   const float* temperature;
   const FinalDesc* final_desc;  // [B]
   ChunkRec* chunks;             // [B][n_chunks]
+  // Group records: the chunks of a row are also combined per column group
+  // (the contiguous token range one tile CTA covers), so that the locate scans
+  // a few hundred group records and then the chunks of one group only.
+  ChunkRec* supers;   // [B][sup_stride]
+  int32_t sup_stride;
+  int32_t sup_tiles;  // T: tiles of the launch, M-tile major
+  int32_t sup_groups; // G: group g covers tiles [g*T/G, (g+1)*T/G)
+  int32_t sup_nt;     // tiles per M-tile (across the vocabulary)
+  int32_t sup_cpt;    // 32-token chunks per tile
+  int32_t sup_rows;   // rows per M-tile
   uint64_t seed;
   int32_t* tokens_out;        // draft: draft_tokens; final: out_tokens
   float* q_token;             // draft only
@@ -106,6 +116,28 @@ constexpr int kTileCols = 256;  // tokens per sampling CTA (8 chunks of 32)
 
 inline int32_t num_chunks(int32_t V) { return (V + 31) / 32; }
 
+// Column groups of the tile kernels. Group g covers tiles
+// [floor(g*T/G), floor((g+1)*T/G)); the groups meeting M-tile mt are
+// first_group(mt) .. last_group(mt), and a row's group records are stored in
+// that order (slot = g - first_group(mt)), so slots follow the vocabulary.
+constexpr int32_t kMaxTcGroups = 256;
+inline int32_t sup_stride_for(int32_t V) {
+  const int32_t simt = (V + kTileCols - 1) / kTileCols;
+  return simt > kMaxTcGroups ? simt : kMaxTcGroups;
+}
+__host__ __device__ inline int32_t ceil_div64(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
+__host__ __device__ inline int32_t group_tile0(const SampleParams& p, int32_t g) {
+  return (int32_t)((int64_t)g * p.sup_tiles / p.sup_groups);
+}
+__host__ __device__ inline int32_t first_group(const SampleParams& p, int32_t mt) {
+  return ceil_div64(((int64_t)mt * p.sup_nt + 1) * p.sup_groups, p.sup_tiles) - 1;
+}
+__host__ __device__ inline int32_t last_group(const SampleParams& p, int32_t mt) {
+  return ceil_div64((int64_t)(mt + 1) * p.sup_nt * p.sup_groups, p.sup_tiles) - 1;
+}
+
+void tc_group_layout(SampleParams& p);
+void simt_group_layout(SampleParams& p);
 size_t sample_tile_smem_bytes(int32_t r);
 size_t locate_smem_bytes(int32_t V);
 bool tc_path_supported(int32_t dtype, int32_t r);

@@ -111,20 +111,37 @@ __global__ void __launch_bounds__(kThreads) sample_tile_kernel(SampleParams p) {
 
   const int row = row0 + rl;
   const int chunk = blockIdx.x * 8 + cl;
-  if (row >= p.B || chunk >= p.n_chunks) return;
   const RowCtx& c = rows[rl];
-  if (c.mode == kSkip) return;
-  const int col0 = chunk * 32;
-  const int n = min(32, p.V - col0);
-  float z[32], t[32];
-  if (c.zrow) load_chunk<Tin>(c.zrow, col0, n, z);
-  if (c.trow) load_chunk<Tin>(c.trow, col0, n, t);
-  ChunkRec rec;
-  if (n == 32)
-    chunk_record<true>(c, F32Src{z}, acc, F32Src{t}, 32, col0, rec, p.status);
-  else
-    chunk_record<false>(c, F32Src{z}, acc, F32Src{t}, n, col0, rec, p.status);
-  p.chunks[(size_t)row * p.n_chunks + chunk] = rec;
+  const bool active = row < p.B && chunk < p.n_chunks && c.mode != kSkip;
+  ChunkRec rec = group_empty();
+  if (active) {
+    const int col0 = chunk * 32;
+    const int n = min(32, p.V - col0);
+    float z[32], t[32];
+    if (c.zrow) load_chunk<Tin>(c.zrow, col0, n, z);
+    if (c.trow) load_chunk<Tin>(c.trow, col0, n, t);
+    if (n == 32)
+      chunk_record<true>(c, F32Src{z}, acc, F32Src{t}, 32, col0, rec, p.status);
+    else
+      chunk_record<false>(c, F32Src{z}, acc, F32Src{t}, n, col0, rec, p.status);
+    p.chunks[(size_t)row * p.n_chunks + chunk] = rec;
+  }
+  // group record of the row's 256 tokens: the 8 lanes of a row are adjacent
+  ChunkRec g = rec;
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    const ChunkRec other = shfl_xor_rec(g, o);
+    // merge in token order so that equal greedy logits keep the first token
+    if (cl & o) {
+      ChunkRec lo = other;
+      group_merge(c.mode, lo, g);
+      g = lo;
+    } else {
+      group_merge(c.mode, g, other);
+    }
+  }
+  if (cl == 0 && row < p.B && c.mode != kSkip)
+    p.supers[(size_t)row * p.sup_stride + blockIdx.x] = g;
 }
 
 // ---- locate ------------------------------------------------------------------
@@ -137,32 +154,65 @@ __device__ __forceinline__ bool df_gt(DF a, DF b) {
   return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
 }
 
-__device__ __forceinline__ DF scaled_rec(const ChunkRec& r, int N) {
-  const int e = (r.ref == kEmptyRef) ? -300 : max(r.ref - N, -300);
-  return df_scale2(DF{r.hi, r.lo}, e);
+// Warp-wide inclusive double-float prefix sum.
+__device__ __forceinline__ DF warp_incl_scan(DF v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF w = shfl_up_df(v, o);
+    if (lane >= o) v = df_add(w, v);
+  }
+  return v;
 }
 
-// One CTA per row: combine the row's chunk records, locate the chunk where the
-// CDF crosses u*S, recompute its 32 weights and pick the token. The records
-// are staged once with independent 16-byte loads; the E row of the bias is
-// prefetched alongside, and the P column loads of the crossing chunk are all
-// issued before they are consumed, so the row costs few dependent round trips.
+__device__ __forceinline__ DF shfl_df(DF v, int l) {
+  return {__shfl_sync(0xffffffffu, v.hi, l), __shfl_sync(0xffffffffu, v.lo, l)};
+}
+
+// One CTA per row, in three levels: (1) combine the row's group records
+// (exact power-of-two rescale, double-float prefix) and find the group where
+// the CDF crosses u*S; (2) scan that group's chunk records to find the
+// crossing chunk; (3) recompute that chunk's 32 weights with the arithmetic
+// its record used and pick the token: x = min{i : u*S < C_i}. Levels 1 and 2
+// run in warp 0 alone (no block barrier); the E row of the bias is loaded by
+// every thread at the start and only stored for level 3, so its latency
+// overlaps levels 1 and 2. Each level costs one round of independent loads.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p) {
-  extern __shared__ ChunkRec srec[];
-  __shared__ int s_int[kThreads / 32];
-  __shared__ DF s_df[kThreads / 32];
+  extern __shared__ ChunkRec sgrp[];
   __shared__ float s_arow[1024];
   __shared__ float s_part[kThreads / 32][32];
   __shared__ int s_found;
-  __shared__ DF s_excl;
+  __shared__ int s_N;
+  __shared__ DF s_excl, s_S, s_theta;
+  __shared__ ChunkRec s_crec;
   sm100::pdl_launch_dependents();
   sm100::pdl_wait();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const RowCtx c = make_row_ctx<Tin>(p, b);
-  if (c.mode == kSkip) return;
   const int nc = p.n_chunks;
   const int r = p.r;
+  const int mt = b / p.sup_rows;
+  const int g_lo = first_group(p, mt);
+  const int ng = last_group(p, mt) - g_lo + 1;
+  // group records first: they do not depend on the row's context
+  if (wid == 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.supers + (size_t)b * p.sup_stride);
+    uint4* dst = reinterpret_cast<uint4*>(sgrp);
+    for (int i0 = 0; i0 < ng; i0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i < ng) v[u] = __ldcg(src + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i < ng) dst[i] = v[u];
+      }
+    }
+  }
+  const RowCtx c = make_row_ctx<Tin>(p, b);
+  if (c.mode == kSkip) return;
   const Tin* Erow = reinterpret_cast<const Tin*>(p.E) + (size_t)(c.a_token >= 0 ? c.a_token : 0) * r;
   float erow[4];
 #pragma unroll
@@ -170,20 +220,152 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
     const int k = tid + q * kThreads;
     erow[q] = (c.a_token >= 0 && k < r) ? to_f32(Erow[k]) : 0.f;
   }
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(p.chunks + (size_t)b * nc);
-    uint4* dst = reinterpret_cast<uint4*>(srec);
-    for (int i0 = 0; i0 < nc; i0 += kThreads * 8) {
-      uint4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        if (i < nc) v[u] = __ldcg(src + i);
+
+  if (wid == 0) {
+    // the row's uniform does not depend on the records: draw it while they load
+    const DF u01 = uniform_df(p.seed, (uint32_t)b, c.upos, c.ustage);
+    __syncwarp();
+    const int seg = (ng + 31) / 32;
+    const int c0 = min(ng, lane * seg), c1 = min(ng, c0 + seg);
+    if (c.mode == kGreedyMarkov) {
+      ChunkRec best = group_empty();
+      for (int i = c0; i < c1; ++i) {
+        const ChunkRec rr = sgrp[i];
+        if (greedy_better(rr, best)) best = rr;
       }
+      for (int o = 16; o > 0; o >>= 1) {
+        const ChunkRec ov = shfl_xor_rec(best, o);
+        if (greedy_better(ov, best)) best = ov;
+      }
+      if (lane == 0) {
+        int bx = best.idx;
+        if (bx < 0) {
+          bx = 0;
+          report(p.status, kErrNonfinite);
+        }
+        p.tokens_out[c.out_index] = bx;
+        if (p.src == 0) {
+          p.q_token[c.out_index] = 1.f;
+          ds_row_stats st;
+          st.sum_hi = 1.f;
+          st.sum_lo = 0.f;
+          st.ref = 0;
+          st.argmax = bx;
+          p.q_stats[c.out_index] = st;
+        }
+      }
+      s_found = -1;
+    } else {
+      // ---- level 1: global reference, prefix over the groups, crossing group ----
+      int N = 0;
+      if (c.mode == kSampleMarkov) {
+        int lm = INT_MIN;
+        for (int i = c0; i < c1; ++i) lm = max(lm, sgrp[i].ref);
+        for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, o));
+        N = lm;
+      }
+      DF tot = {0.f, 0.f};
+      for (int i = c0; i < c1; ++i) tot = df_add(tot, rec_scaled(sgrp[i], N));
+      const DF inc = warp_incl_scan(tot, lane);
+      DF excl = shfl_up_df(inc, 1);
+      if (lane == 0) excl = DF{0.f, 0.f};
+      const DF S = shfl_df(inc, 31);
+      int gsel = -1;
+      DF gexcl = {0.f, 0.f}, theta = {0.f, 0.f};
+      if (S.hi > 0.f && isfinite(S.hi)) {
+        theta = df_mul(u01, S);
+        const unsigned hit = __ballot_sync(0xffffffffu, c1 > c0 && df_gt(inc, theta));
+        if (hit) {
+          // the crossing group is within the first lane whose prefix passes u*S
+          const int l = __ffs(hit) - 1;
+          if (lane == l) {
+            DF run = excl;
+            for (int i = c0; i < c1; ++i) {
+              const DF incl = df_add(run, rec_scaled(sgrp[i], N));
+              if (df_gt(incl, theta)) {
+                gsel = i;
+                gexcl = run;
+                break;
+              }
+              run = incl;
+            }
+          }
+          gsel = __shfl_sync(0xffffffffu, gsel, l);
+          gexcl = shfl_df(gexcl, l);
+        }
+        if (gsel < 0) {  // u*S at the very top (or rounding): last group with mass
+          int gi = ng - 1;
+          while (gi > 0 && !(rec_scaled(sgrp[gi], N).hi > 0.f)) --gi;
+          gsel = gi;
+          const DF sc = rec_scaled(sgrp[gi], N);
+          gexcl = df_add(S, DF{-sc.hi, -sc.lo});
+        }
+      }
+      if (gsel < 0) {
+        if (lane == 0) {
+          report(p.status, kErrNonfinite);
+          p.tokens_out[c.out_index] = 0;
+        }
+        s_found = -1;
+      } else {
+        // ---- level 2: the chunks of the crossing group ----
+        const int g = g_lo + gsel;
+        const int mt0 = mt * p.sup_nt;
+        const int ta = max(group_tile0(p, g), mt0), tb = min(group_tile0(p, g + 1), mt0 + p.sup_nt);
+        const int ch_lo = (ta - mt0) * p.sup_cpt, ch_hi = min((tb - mt0) * p.sup_cpt, nc);
+        const ChunkRec* crow = p.chunks + (size_t)b * nc;
+        DF run = gexcl, fexcl = gexcl, lexcl = gexcl;
+        int found = -1, last = -1;
+        ChunkRec frec = group_empty(), lrec = group_empty();
+        for (int base = ch_lo; base < ch_hi && found < 0; base += 128) {
+          ChunkRec rr[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        if (i < nc) dst[i] = v[u];
+          for (int u = 0; u < 4; ++u) {
+            const int i = base + 32 * u + lane;
+            rr[u] = i < ch_hi ? ld_rec(crow + i) : group_empty();
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (found >= 0) break;
+            const int i = base + 32 * u + lane;
+            const DF v = rec_scaled(rr[u], N);
+            const DF ic = warp_incl_scan(v, lane);
+            DF ex = shfl_up_df(ic, 1);
+            if (lane == 0) ex = DF{0.f, 0.f};
+            const DF incl = df_add(run, ic);
+            const DF exa = df_add(run, ex);
+            const unsigned hit = __ballot_sync(0xffffffffu, i < ch_hi && df_gt(incl, theta));
+            const unsigned mass = __ballot_sync(0xffffffffu, i < ch_hi && v.hi > 0.f);
+            if (hit) {
+              const int l = __ffs(hit) - 1;
+              found = base + 32 * u + l;
+              fexcl = shfl_df(exa, l);
+              frec = {__shfl_sync(0xffffffffu, rr[u].hi, l), 0.f, __shfl_sync(0xffffffffu, rr[u].ref, l),
+                      __shfl_sync(0xffffffffu, rr[u].idx, l)};
+            } else {
+              if (mass) {
+                const int l = 31 - __clz(mass);
+                last = base + 32 * u + l;
+                lexcl = shfl_df(exa, l);
+                lrec = {0.f, 0.f, __shfl_sync(0xffffffffu, rr[u].ref, l), __shfl_sync(0xffffffffu, rr[u].idx, l)};
+              }
+              run = shfl_df(incl, 31);
+            }
+          }
+        }
+        if (found < 0) {  // rounding left u*S past the group's in-order total
+          found = last >= 0 ? last : ch_lo;
+          fexcl = last >= 0 ? lexcl : gexcl;
+          frec = last >= 0 ? lrec : ld_rec(crow + found);
+        }
+        if (lane == 0) {
+          s_found = found;
+          s_excl = fexcl;
+          s_crec = frec;
+          s_N = N;
+          s_S = S;
+          s_theta = theta;
+        }
       }
     }
   }
@@ -193,143 +375,14 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
     if (k < r) s_arow[k] = erow[q];
   }
   __syncthreads();
-  const int seg = (nc + kThreads - 1) / kThreads;
-  const int c0 = min(nc, tid * seg), c1 = min(nc, c0 + seg);
-
-  if (c.mode == kGreedyMarkov) {
-    DF best = {kNegInf, 0.f};
-    int bi = INT_MAX;
-    for (int i = c0; i < c1; ++i) {
-      const ChunkRec rr = srec[i];
-      if (rr.idx < 0) continue;
-      if (bi == INT_MAX || rr.hi > best.hi || (rr.hi == best.hi && rr.lo > best.lo)) {
-        best = {rr.hi, rr.lo};
-        bi = rr.idx;
-      }
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      const DF ov = {__shfl_xor_sync(0xffffffffu, best.hi, o), __shfl_xor_sync(0xffffffffu, best.lo, o)};
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const bool take = (oi != INT_MAX) &&
-                        (bi == INT_MAX || ov.hi > best.hi || (ov.hi == best.hi && ov.lo > best.lo) ||
-                         (ov.hi == best.hi && ov.lo == best.lo && oi < bi));
-      if (take) {
-        best = ov;
-        bi = oi;
-      }
-    }
-    if (lane == 0) {
-      s_df[wid] = best;
-      s_int[wid] = bi;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      DF bb = {kNegInf, 0.f};
-      int bx = INT_MAX;
-      for (int w = 0; w < kThreads / 32; ++w) {
-        const DF v = s_df[w];
-        const int iw = s_int[w];
-        if (iw == INT_MAX) continue;
-        if (bx == INT_MAX || v.hi > bb.hi || (v.hi == bb.hi && v.lo > bb.lo) ||
-            (v.hi == bb.hi && v.lo == bb.lo && iw < bx)) {
-          bb = v;
-          bx = iw;
-        }
-      }
-      if (bx == INT_MAX) {
-        bx = 0;
-        report(p.status, kErrNonfinite);
-      }
-      p.tokens_out[c.out_index] = bx;
-      if (p.src == 0) {
-        p.q_token[c.out_index] = 1.f;
-        ds_row_stats st;
-        st.sum_hi = 1.f;
-        st.sum_lo = 0.f;
-        st.ref = 0;
-        st.argmax = bx;
-        p.q_stats[c.out_index] = st;
-      }
-    }
-    return;
-  }
-
-  // ---- sampling rows: global reference, prefix sums, crossing chunk ----
-  int lm = INT_MIN;
-  if (c.mode == kSampleMarkov)
-    for (int i = c0; i < c1; ++i) lm = max(lm, srec[i].ref);
-  for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, o));
-  if (lane == 0) s_int[wid] = lm;
-  __syncthreads();
-  int N = 0;
-  if (c.mode == kSampleMarkov) {
-    N = s_int[0];
-    for (int w = 1; w < kThreads / 32; ++w) N = max(N, s_int[w]);
-  }
-  DF tot = {0.f, 0.f};
-  for (int i = c0; i < c1; ++i) tot = df_add(tot, scaled_rec(srec[i], N));
-  DF inc = tot;
-  for (int o = 1; o < 32; o <<= 1) {
-    const DF v = shfl_up_df(inc, o);
-    if (lane >= o) inc = df_add(v, inc);
-  }
-  DF prev = shfl_up_df(inc, 1);
-  if (lane == 0) prev = DF{0.f, 0.f};
-  if (lane == 31) s_df[wid] = inc;
-  __syncthreads();
-  if (wid == 0) {
-    DF wv = lane < kThreads / 32 ? s_df[lane] : DF{0.f, 0.f};
-    for (int o = 1; o < 32; o <<= 1) {
-      const DF v = shfl_up_df(wv, o);
-      if (lane >= o) wv = df_add(v, wv);
-    }
-    if (lane < kThreads / 32) s_df[lane] = wv;
-    if (lane == 0) s_found = INT_MAX;
-  }
-  __syncthreads();
-  const DF wexcl = wid > 0 ? s_df[wid - 1] : DF{0.f, 0.f};
-  const DF excl = df_add(wexcl, prev);
-  const DF S = s_df[kThreads / 32 - 1];
-  const double Sd = df_to_double(S);
-  if (!(Sd > 0.0) || !isfinite(Sd)) {
-    if (tid == 0) {
-      report(p.status, kErrNonfinite);
-      p.tokens_out[c.out_index] = 0;
-    }
-    return;
-  }
-  const double u = uniform_dev(p.seed, (uint32_t)b, c.upos, c.ustage);
-  const double theta_d = u * Sd;
-  const float th_hi = (float)theta_d;
-  const DF theta = {th_hi, (float)(theta_d - (double)th_hi)};
-  DF run = excl;
-  int my_found = INT_MAX;
-  DF my_excl = {0.f, 0.f};
-  for (int i = c0; i < c1; ++i) {
-    const DF incl = df_add(run, scaled_rec(srec[i], N));
-    if (df_gt(incl, theta)) {
-      my_found = i;
-      my_excl = run;
-      break;
-    }
-    run = incl;
-  }
-  if (my_found != INT_MAX) atomicMin(&s_found, my_found);
-  __syncthreads();
-  if (my_found != INT_MAX && my_found == s_found) s_excl = my_excl;
-  if (tid == 0 && s_found == INT_MAX) {  // u*S at the very top: last chunk with mass
-    int ch = nc - 1;
-    while (ch > 0 && !(srec[ch].hi > 0.f)) --ch;
-    s_found = ch;
-    const DF sc = scaled_rec(srec[ch], N);
-    s_excl = df_add(S, DF{-sc.hi, -sc.lo});
-  }
-  __syncthreads();
+  if (s_found < 0) return;  // greedy row done, or no mass
   const int chunk = s_found;
   const int col0 = chunk * 32;
   const int n = min(32, p.V - col0);
+  const int N = s_N;
+  const DF S = s_S, theta = s_theta;
 
-  // ---- recompute the crossing chunk: logits first, then the bias (k split over warps) ----
+  // ---- level 3: recompute the crossing chunk: logits first, then the bias (k split over warps) ----
   float zl = 0.f, tl = 0.f;
   if (wid == 0) {
     zl = (c.zrow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.zrow)[col0 + lane]) : 0.f;
@@ -360,7 +413,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
     float w = 0.f;
     int e = 0;
     if (c.mode == kSampleMarkov) {
-      const ChunkRec cr = srec[chunk];
+      const ChunkRec cr = s_crec;
       const int ref = cr.ref;
       if (lane < n && ref != kEmptyRef) {
         if (cr.idx == -2)
@@ -379,7 +432,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
       }
     }
     if (!(w >= 0.f) || !isfinite(w)) w = 0.f;
-    DF pre = {ldexpf(w, e), 0.f};
+    DF pre = {pow2_scale(w, e), 0.f};
     for (int o = 1; o < 32; o <<= 1) {
       const DF v = shfl_up_df(pre, o);
       if (lane >= o) pre = df_add(v, pre);
@@ -393,7 +446,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
       if (!pos) report(p.status, kErrNonfinite);
       p.tokens_out[c.out_index] = col0 + xl;
       if (p.src == 0) {
-        p.q_token[c.out_index] = (float)(ldexp((double)wx, e) / Sd);
+        p.q_token[c.out_index] = pow2_scale(div_by_df(wx, S), e);
         ds_row_stats st;
         st.sum_hi = S.hi;
         st.sum_lo = S.lo;
@@ -428,7 +481,16 @@ cudaError_t launch_sample_tile(const SampleParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-size_t locate_smem_bytes(int32_t V) { return (size_t)num_chunks(V) * sizeof(ChunkRec); }
+size_t locate_smem_bytes(int32_t V) { return (size_t)sup_stride_for(V) * sizeof(ChunkRec); }
+
+void simt_group_layout(SampleParams& p) {
+  p.sup_stride = sup_stride_for(p.V);
+  p.sup_nt = (p.V + kTileCols - 1) / kTileCols;
+  p.sup_rows = kTileRows;
+  p.sup_tiles = p.sup_nt * ((p.B + kTileRows - 1) / kTileRows);
+  p.sup_groups = p.sup_tiles;
+  p.sup_cpt = kTileCols / 32;
+}
 
 template <typename K, typename... Args>
 static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,

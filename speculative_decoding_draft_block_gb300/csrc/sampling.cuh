@@ -199,5 +199,72 @@ __device__ __forceinline__ void chunk_record(const RowCtx& c, ZS z, const float*
   if (bad) report(status, kErrNonfinite);
 }
 
+// ---- group records -------------------------------------------------------
+//
+// A group record combines the chunk records of a contiguous token range:
+//   sampling rows: ref = the largest chunk reference, hi + lo = the sum of the
+//                  chunk sums each scaled by 2^(chunk ref - ref) (exact powers
+//                  of two; contributions below 2^-252 relative are dropped)
+//   greedy rows:   the largest (hi, lo) with the smallest token on ties
+//   residual/bonus rows: the plain double-float sum (records share ref 0)
+
+// x * 2^e for e <= 0 without a library call (rounds only in the subnormal range).
+__device__ __forceinline__ float pow2_scale(float x, int e) {
+  if (e >= -126) return __fmul_rn(x, __int_as_float((e + 127) << 23));
+  if (e < -252) return __fmul_rn(x, 0.f);
+  return __fmul_rn(__fmul_rn(x, __int_as_float(1 << 23)), __int_as_float((e + 253) << 23));
+}
+
+// A record's mass relative to the reference N (N >= every non-empty ref).
+__device__ __forceinline__ DF rec_scaled(const ChunkRec& r, int N) {
+  if (r.ref == kEmptyRef) return {0.f, 0.f};
+  const long long e = (long long)r.ref - N;
+  const int ei = e < -300 ? -300 : (int)e;
+  return {pow2_scale(r.hi, ei), pow2_scale(r.lo, ei)};
+}
+
+// Record load that bypasses L1 (records are written by the previous kernel).
+__device__ __forceinline__ ChunkRec ld_rec(const ChunkRec* q) {
+  const uint4 v = __ldcg(reinterpret_cast<const uint4*>(q));
+  return {__uint_as_float(v.x), __uint_as_float(v.y), (int32_t)v.z, (int32_t)v.w};
+}
+
+__device__ __forceinline__ ChunkRec group_empty() { return {0.f, 0.f, kEmptyRef, -1}; }
+
+__device__ __forceinline__ bool greedy_better(const ChunkRec& a, const ChunkRec& b) {
+  if (a.idx < 0) return false;
+  if (b.idx < 0) return true;
+  return a.hi > b.hi || (a.hi == b.hi && (a.lo > b.lo || (a.lo == b.lo && a.idx < b.idx)));
+}
+
+__device__ __forceinline__ void group_merge(int mode, ChunkRec& acc, const ChunkRec& r) {
+  if (mode == kGreedyMarkov) {
+    if (greedy_better(r, acc)) acc = r;
+  } else if (mode == kSampleMarkov) {
+    if (r.ref == kEmptyRef) return;
+    if (acc.ref == kEmptyRef) {
+      acc.hi = r.hi;
+      acc.lo = r.lo;
+      acc.ref = r.ref;
+      return;
+    }
+    const int R = max(acc.ref, r.ref);
+    const DF s = df_add(rec_scaled(acc, R), rec_scaled(r, R));
+    acc.hi = s.hi;
+    acc.lo = s.lo;
+    acc.ref = R;
+  } else {
+    const DF s = df_add(DF{acc.hi, acc.lo}, DF{r.hi, r.lo});
+    acc.hi = s.hi;
+    acc.lo = s.lo;
+    acc.ref = 0;
+  }
+}
+
+__device__ __forceinline__ ChunkRec shfl_xor_rec(const ChunkRec& r, int o) {
+  return {__shfl_xor_sync(0xffffffffu, r.hi, o), __shfl_xor_sync(0xffffffffu, r.lo, o),
+          __shfl_xor_sync(0xffffffffu, r.ref, o), __shfl_xor_sync(0xffffffffu, r.idx, o)};
+}
+
 }  // namespace
 }  // namespace ds

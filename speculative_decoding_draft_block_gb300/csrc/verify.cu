@@ -10,7 +10,7 @@
 //                           (per-thread power-of-two references merged
 //                           exactly, double-float sums), evaluates p(x_k) and
 //                           takes the accept decision u * q(x_k) < p(x_k) in
-//                           double (greedy rows: target argmax and exact match).
+//                           double-float (greedy rows: target argmax and exact match).
 //   verify_finalize_kernel  one thread per request: accepted prefix length,
 //                           emitted tokens, and the descriptor of the final
 //                           draw (residual at the first rejection, or bonus
@@ -135,22 +135,24 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
     }
     if (tid == 0) {
       const DF S = sdf[0];
-      const double Sd = df_to_double(S);
       out.s_hi = S.hi;
       out.s_lo = S.lo;
       out.ref = N;
-      if (!(Sd > 0.0)) bad = true;
-      if (j < L && Sd > 0.0) {
+      const bool pos = S.hi > 0.f;
+      if (!pos) bad = true;
+      if (j < L && pos) {
         int x = p.draft_tokens[(size_t)b * p.K + j];
         if (x < 0 || x >= p.V) {
           report(p.status, kErrBounds);
           x = 0;
         }
         const float tx = to_f32(row[x]);
-        const double px = (double)weight_rel(tx, 0.f, g, N) / Sd;
-        const double qx = (double)p.q_token[(size_t)b * p.K + j];
-        const double u = uniform_dev(p.seed, (uint32_t)b, (uint32_t)(j + 1), DS_STAGE_ACCEPT);
-        out.accept = (u * qx < px) ? 1 : 0;
+        // u * q(x) < p(x) = w_x / S, tested as u * q(x) * S < w_x
+        const float wx = weight_rel(tx, 0.f, g, N);
+        const float qx = p.q_token[(size_t)b * p.K + j];
+        const DF uq = df_mul(uniform_df(p.seed, (uint32_t)b, (uint32_t)(j + 1), DS_STAGE_ACCEPT),
+                             DF{qx, 0.f});
+        out.accept = df_lt(df_mul(uq, S), DF{wx, 0.f}) ? 1 : 0;
       }
     }
   }
@@ -190,11 +192,16 @@ __global__ void __launch_bounds__(128) verify_finalize_kernel(VerifyParams p) {
       d.a_token = (a == 0) ? p.anchor[b] : p.draft_tokens[(size_t)b * K + (a - 1)];
       const ds_row_stats qs = p.q_stats[(size_t)b * K + a];
       d.Nq = qs.ref;
-      const double Sp = (double)vr[a].s_hi + (double)vr[a].s_lo;
-      const double Sq = (double)qs.sum_hi + (double)qs.sum_lo;
-      const double R = Sp / Sq;
-      d.Rhi = (float)R;
-      d.Rlo = (float)(R - (double)d.Rhi);
+      // R = S_p / S_q as a double-float: q = RN(Sp.hi / Sq.hi) refined by one
+      // correction step with the exact residual of the high words
+      const DF Sp = {vr[a].s_hi, vr[a].s_lo}, Sq = {qs.sum_hi, qs.sum_lo};
+      const float q = __fdiv_rn(Sp.hi, Sq.hi);
+      const DF qS = df_mul(DF{q, 0.f}, Sq);
+      const DF res = df_add(Sp, DF{-qS.hi, -qS.lo});
+      const float ql = __fdiv_rn(res.hi, Sq.hi);
+      const DF R = fast_two_sum(q, ql);
+      d.Rhi = R.hi;
+      d.Rlo = R.lo;
     } else {
       d.mode = kBonus;
     }
