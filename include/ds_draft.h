@@ -121,6 +121,8 @@ typedef struct {
   const void* base_logits;    /* [B][K][V]  z_k, the parallel backbone's logits */
   const void* E;              /* [V][r]     Markov embedding table */
   const void* P;              /* [r][V]     Markov projection */
+  const void* P_t;            /* [V][r]     optional token-major copy of P written by
+                                            ds_transpose_projection, or NULL */
   const int32_t* anchor;      /* [B]        x_0, the last verified token */
   const float* temperature;   /* [B]        sampling temperature, 0 = greedy */
   uint64_t seed;              /* Philox key */
@@ -134,6 +136,19 @@ typedef struct {
 
 size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
 ds_status ds_draft_block(const ds_draft_args* args, ds_stream_t stream);
+
+/*
+ * Token-major copy of the Markov projection: P_t[v][k] = P[k][v] for
+ * v < V, k < r (bit-exact copy, dtype as P). P is a weight of the draft head
+ * ([DSpark] 방법론 › 반자기회귀 생성), so this is a once-per-model layout step,
+ * run when the weights are loaded. With P_t given, the per-step draw reads the
+ * r weights of the 32 tokens it refines as one contiguous block instead of r
+ * rows strided by V; results are the same up to the summation order of that
+ * 32-token bias (a float rounding difference). Shapes follow the limits
+ * above; P and P_t are device pointers, 16-byte aligned, not overlapping.
+ */
+ds_status ds_transpose_projection(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_t,
+                                  ds_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Confidence head, survival and prefix scheduler                            */
@@ -199,6 +214,7 @@ typedef struct {
   const void* base_logits;    /* [B][K][V] */
   const void* E;              /* [V][r] */
   const void* P;              /* [r][V] */
+  const void* P_t;            /* [V][r] optional, as in ds_draft_args */
   const int32_t* anchor;      /* [B] */
   const int32_t* draft_tokens;/* [B][K] */
   const float* q_token;       /* [B][K] */

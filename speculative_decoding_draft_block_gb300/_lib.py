@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_UNSUPPORTED", 3:
 EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspace_bytes",
            "ds_draft_block", "ds_sched_workspace_bytes", "ds_confidence_schedule",
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
-           "ds_version")
+           "ds_version", "ds_transpose_projection")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -33,7 +33,7 @@ _i32 = ctypes.c_int32
 
 class DraftArgs(ctypes.Structure):
     _fields_ = [("B", _i32), ("K", _i32), ("V", _i32), ("r", _i32), ("dtype", _i32),
-                ("base_logits", _vp), ("E", _vp), ("P", _vp), ("anchor", _vp),
+                ("base_logits", _vp), ("E", _vp), ("P", _vp), ("P_t", _vp), ("anchor", _vp),
                 ("temperature", _vp), ("seed", ctypes.c_uint64), ("draft_tokens", _vp),
                 ("q_token", _vp), ("q_stats", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
@@ -50,7 +50,7 @@ class SchedArgs(ctypes.Structure):
 
 class VerifyArgs(ctypes.Structure):
     _fields_ = [("B", _i32), ("K", _i32), ("V", _i32), ("r", _i32), ("dtype", _i32),
-                ("target_logits", _vp), ("base_logits", _vp), ("E", _vp), ("P", _vp),
+                ("target_logits", _vp), ("base_logits", _vp), ("E", _vp), ("P", _vp), ("P_t", _vp),
                 ("anchor", _vp), ("draft_tokens", _vp), ("q_token", _vp), ("q_stats", _vp),
                 ("sched_len", _vp), ("temperature", _vp), ("seed", ctypes.c_uint64),
                 ("out_tokens", _vp), ("accept_count", _vp), ("num_emitted", _vp),
@@ -85,6 +85,8 @@ def load():
     lib.ds_verify.argtypes = [ctypes.POINTER(VerifyArgs), _vp]
     for f in ("ds_draft_block", "ds_confidence_schedule", "ds_verify"):
         getattr(lib, f).restype = ctypes.c_int
+    lib.ds_transpose_projection.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp]
+    lib.ds_transpose_projection.restype = ctypes.c_int
     lib.ds_check_status.argtypes = [_vp, _vp]
     lib.ds_check_status.restype = ctypes.c_int
     lib.ds_status_string.argtypes = [ctypes.c_int]
@@ -171,10 +173,11 @@ def ds_verify_workspace_bytes(B, K, V, r):
 # ---- the three calls ----------------------------------------------------------
 
 def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q_token, q_stats,
-                   workspace, status, stream=None):
+                   workspace, status, stream=None, P_t=None):
     B, K, V = base_logits.shape
     a = DraftArgs(B=B, K=K, V=V, r=E.shape[1], dtype=_dtype_code(base_logits),
                   base_logits=_ptr(base_logits, "base_logits"), E=_ptr(E, "E"), P=_ptr(P, "P"),
+                  P_t=None if P_t is None else _ptr(P_t, "P_t"),
                   anchor=_ptr(anchor, "anchor"), temperature=_ptr(temperature, "temperature"),
                   seed=int(seed), draft_tokens=_ptr(draft_tokens, "draft_tokens"),
                   q_token=_ptr(q_token, "q_token"), q_stats=_ptr(q_stats, "q_stats"),
@@ -204,11 +207,12 @@ def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp,
 
 def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats, sched_len,
               temperature, seed, out_tokens, accept_count, num_emitted, workspace, status,
-              stream=None):
+              stream=None, P_t=None):
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
                    target_logits=_ptr(target_logits, "target_logits"),
                    base_logits=_ptr(base_logits, "base_logits"), E=_ptr(E, "E"), P=_ptr(P, "P"),
+                   P_t=None if P_t is None else _ptr(P_t, "P_t"),
                    anchor=_ptr(anchor, "anchor"), draft_tokens=_ptr(draft_tokens, "draft_tokens"),
                    q_token=_ptr(q_token, "q_token"), q_stats=_ptr(q_stats, "q_stats"),
                    sched_len=_ptr(sched_len, "sched_len"), temperature=_ptr(temperature, "temperature"),
@@ -219,6 +223,13 @@ def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q
                    workspace_bytes=workspace.numel() * workspace.element_size(),
                    status=_ptr(status, "status"))
     return load().ds_verify(ctypes.byref(a), _stream(stream))
+
+
+def ds_transpose_projection(P, P_t, stream=None):
+    """P_t[v, k] = P[k, v] on the device (once per model; see ds_draft.h)."""
+    r, V = P.shape
+    return load().ds_transpose_projection(_ptr(P, "P"), r, V, _dtype_code(P), _ptr(P_t, "P_t"),
+                                          _stream(stream))
 
 
 def ds_check_status(status, stream=None):

@@ -111,6 +111,20 @@ ds_status ds_philox_fill(const uint32_t* ctr, uint32_t key0, uint32_t key1, uint
   return from_cuda(launch_philox_fill(ctr, key0, key1, out, n, (cudaStream_t)stream));
 }
 
+ds_status ds_transpose_projection(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_t,
+                                  ds_stream_t stream) {
+  if (!shape_ok(1, 1, V, r)) return DS_ERR_INVALID_ARG;
+  if (dtype != DS_F32 && dtype != DS_BF16) return DS_ERR_INVALID_ARG;
+  if (P == nullptr || P_t == nullptr || !aligned16(P) || !aligned16(P_t)) return DS_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)r * V * (dtype == DS_BF16 ? 2 : 4);
+  const char* a = static_cast<const char*>(P);
+  const char* b = static_cast<const char*>(P_t);
+  if (a < b + bytes && b < a + bytes) return DS_ERR_INVALID_ARG;  // overlapping
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  return from_cuda(launch_transpose(P, r, V, dtype, P_t, (cudaStream_t)stream));
+}
+
 size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r) {
   if (!shape_ok(B, K, V, r)) return 0;
   return draft_ws(B, V, r);
@@ -124,6 +138,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
                         a->draft_tokens, a->q_token, a->q_stats, a->status};
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
+  if (a->P_t != nullptr && !aligned16(a->P_t)) return DS_ERR_INVALID_ARG;
   if (a->workspace == nullptr || !aligned16(a->workspace) ||
       a->workspace_bytes < draft_ws(a->B, a->V, a->r))
     return DS_ERR_WORKSPACE;
@@ -142,6 +157,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   p.base_logits = a->base_logits;
   p.E = a->E;
   p.P = a->P;
+  p.P_t = a->P_t;
   p.anchor = a->anchor;
   p.draft_tokens = a->draft_tokens;
   p.temperature = a->temperature;
@@ -239,6 +255,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
                         a->status};
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
+  if (a->P_t != nullptr && !aligned16(a->P_t)) return DS_ERR_INVALID_ARG;
   const VerifyLayout l = verify_layout(a->B, a->K, a->V, a->r);
   const bool tc = tc_path_supported(a->dtype, a->r);
   if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < l.total)
@@ -285,6 +302,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   p.target_logits = a->target_logits;
   p.E = a->E;
   p.P = a->P;
+  p.P_t = a->P_t;
   p.anchor = a->anchor;
   p.draft_tokens = a->draft_tokens;
   p.temperature = a->temperature;

@@ -53,6 +53,7 @@ struct SampleParams {
   const void* target_logits;  // [B][K+1][V]
   const void* E;
   const void* P;
+  const void* P_t;              // [V][r] token-major copy of P, or null
   const int32_t* anchor;
   const int32_t* draft_tokens;  // [B][K] (read: previous positions; written by locate)
   const float* temperature;
@@ -149,6 +150,8 @@ cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_confidence(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 size_t schedule_smem_bytes(int32_t B, int32_t K);
+cudaError_t launch_transpose(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_t,
+                             cudaStream_t s);
 cudaError_t launch_philox_fill(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_t* out,
                                int32_t n, cudaStream_t s);
 

@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
   extern __shared__ ChunkRec sgrp[];
   __shared__ float s_arow[1024];
   __shared__ float s_part[kThreads / 32][32];
+  __shared__ float s_bias[32];
   __shared__ int s_found;
   __shared__ int s_N;
   __shared__ DF s_excl, s_S, s_theta;
@@ -388,7 +389,33 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
     zl = (c.zrow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.zrow)[col0 + lane]) : 0.f;
     tl = (c.trow && lane < n) ? to_f32(reinterpret_cast<const Tin*>(c.trow)[col0 + lane]) : 0.f;
   }
-  {
+  const bool token_major = p.P_t != nullptr;
+  if (token_major) {
+    // 8 threads per token, each over 8-element groups part, part + 8, ...
+    const int j = tid >> 3, part = tid & 7;
+    float acc = 0.f;
+    if (c.a_token >= 0 && j < n) {
+      const Tin* row = reinterpret_cast<const Tin*>(p.P_t) + (size_t)(col0 + j) * r;
+      const int groups = r >> 3;
+      for (int g0 = part; g0 < groups; g0 += 32) {
+        float v[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (g0 + 8 * u < groups) load8(row + (g0 + 8 * u) * 8, v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (g0 + 8 * u < groups) {
+            const float* a = s_arow + (g0 + 8 * u) * 8;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = __fmaf_rn(a[e], v[u][e], acc);
+          }
+      }
+    }
+    acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
+    acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
+    acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 4));
+    if (part == 0) s_bias[j] = acc;
+  } else {
     float acc = 0.f;
     if (c.a_token >= 0) {
       const int per = r / (kThreads / 32);
@@ -408,7 +435,10 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
   __syncthreads();
   if (wid == 0) {
     float bsum = 0.f;
-    for (int w = 0; w < kThreads / 32; ++w) bsum = __fadd_rn(bsum, s_part[w][lane]);
+    if (token_major)
+      bsum = s_bias[lane];
+    else
+      for (int w = 0; w < kThreads / 32; ++w) bsum = __fadd_rn(bsum, s_part[w][lane]);
     // weights with the arithmetic of the chunk's record (idx -2: tensor-core fast path)
     float w = 0.f;
     int e = 0;

@@ -34,7 +34,8 @@ INPUT_KEYS = ("base_logits", "target_logits", "E", "P", "anchor", "temperature",
 
 
 class DeviceCycle:
-    def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0):
+    def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0,
+                 token_major_projection=True):
         self.inp = inp
         self.device = torch.device(device)
         self.mode = mode
@@ -64,13 +65,19 @@ class DeviceCycle:
             raise ValueError("shape not supported by the library")
         self.ws_draft = torch.empty((wd,), dtype=torch.uint8, device=dev)
         self.ws_verify = torch.empty((wv,), dtype=torch.uint8, device=dev)
+        # weight layout step, once per model: the token-major copy of P
+        self.P_t = None
+        if token_major_projection:
+            P = self.t["P"]
+            self.P_t = torch.empty((P.shape[1], P.shape[0]), dtype=P.dtype, device=dev)
+            check(_lib.ds_transpose_projection(P, self.P_t), "ds_transpose_projection")
 
     # -- the three calls ---------------------------------------------------------
     def draft(self, seed, stream=None):
         t = self.t
         check(_lib.ds_draft_block(t["base_logits"], t["E"], t["P"], t["anchor"], t["temperature"],
                                   seed, self.draft_tokens, self.q_token, self.q_stats,
-                                  self.ws_draft, self.status, stream), "ds_draft_block")
+                                  self.ws_draft, self.status, stream, P_t=self.P_t), "ds_draft_block")
 
     def schedule(self, stream=None):
         t = self.t
@@ -85,7 +92,8 @@ class DeviceCycle:
         check(_lib.ds_verify(t["target_logits"], t["base_logits"], t["E"], t["P"], t["anchor"],
                              self.draft_tokens, self.q_token, self.q_stats, self.sched_len,
                              t["temperature"], seed, self.out_tokens, self.accept_count,
-                             self.num_emitted, self.ws_verify, self.status, stream), "ds_verify")
+                             self.num_emitted, self.ws_verify, self.status, stream, P_t=self.P_t),
+              "ds_verify")
 
     def run(self, seed, stream=None):
         """Enqueue one cycle (three library calls); no host synchronisation."""

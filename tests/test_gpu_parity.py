@@ -98,6 +98,34 @@ def test_ragged_multitile_mixed_temperatures(ds, bf16):
     assert rep["draft"]["draws"] == 37 * 5
 
 
+@pytest.mark.parametrize("bf16", [True, False])
+def test_ragged_strided_projection(ds, bf16):
+    """The draw without the token-major copy of P (r strided rows per chunk)."""
+    inp = _ragged(bf16, (0.0, 0.6, 1.0), 17, r=64)
+    _, g = _run(inp, token_major_projection=False)
+    rep = _parity.assert_parity(inp, g, SEED)
+    assert rep["draft"]["draws"] == 37 * 5
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_transpose_projection_exact(ds, bf16):
+    import torch
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.cycle import _to_device
+    for r, V in ((48, 3000), (64, 4096), (16, 8), (256, 1032)):
+        rng = np.random.default_rng(r * 7 + V)
+        P = rng.standard_normal((r, V), dtype=np.float32)
+        if bf16:
+            P = P.view(np.uint32).__rshift__(16).astype(np.uint16)
+        Pd = _to_device(P, "cuda")
+        Pt = torch.empty((V, r), dtype=Pd.dtype, device="cuda")
+        assert _lib.ds_transpose_projection(Pd, Pt) == 0
+        torch.cuda.synchronize()
+        got = Pt.view(torch.int16 if bf16 else torch.float32).cpu().numpy()
+        want = P.T.view(np.int16) if bf16 else P.T
+        assert np.array_equal(got, want)
+
+
 def test_independent_cycle_matches_oracle_cycle(ds):
     """No teacher forcing: the oracle's own cycle and the GPU's agree end to end."""
     import oracle
