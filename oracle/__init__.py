@@ -20,8 +20,8 @@ Sources (cited by page title and section):
     as 1, 2, 3", SC'11.
 
 Parity status per function (see the pins in tests/test_oracle_*.py):
-  philox4x32_10, uniform ........ pinned (published known-answer vectors and an
-                                  independent library implementation)
+  philox4x32_10, uniform ........ pinned (an independent library implementation:
+                                  Triton's Philox run by its CPU interpreter)
   inverse_cdf, argmax_first ..... pinned (hand-built CDFs, brute force)
   markov_logits, draft_block .... pinned (full-rank transition matrix, the
                                   "of course / no problem" toy, exact law by
