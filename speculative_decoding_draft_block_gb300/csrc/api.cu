@@ -56,11 +56,10 @@ ds_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DS_OK : DS_ERR_CU
 // steps so that a step's records are never overwritten while the previous
 // locate still reads them.
 struct DraftLayout {
-  size_t rec[2], sup[2], total;
+  size_t rec[2], sup[2], astage, total;
 };
 
 DraftLayout draft_layout(int32_t B, int32_t V, int32_t r) {
-  (void)r;
   DraftLayout l;
   const size_t rec = align_up((size_t)B * num_chunks(V) * sizeof(ChunkRec));
   const size_t sup = align_up((size_t)B * sup_stride_for(V) * sizeof(ChunkRec));
@@ -68,7 +67,9 @@ DraftLayout draft_layout(int32_t B, int32_t V, int32_t r) {
   l.rec[1] = rec;
   l.sup[0] = 2 * rec;
   l.sup[1] = 2 * rec + sup;
-  l.total = 2 * rec + 2 * sup;
+  l.astage = 2 * rec + 2 * sup;
+  const size_t esz = 4;  // room for f32 E rows; bf16 uses half
+  l.total = l.astage + align_up((size_t)B * r * esz);
   return l;
 }
 
@@ -178,6 +179,8 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
     p.step = k;
     p.chunks = reinterpret_cast<ChunkRec*>(ws + l.rec[k & 1]);
     p.supers = reinterpret_cast<ChunkRec*>(ws + l.sup[k & 1]);
+    p.a_stage_in = (tc && k > 1) ? ws + l.astage : nullptr;
+    p.a_stage_out = (tc && k < a->K) ? ws + l.astage : nullptr;
     cudaError_t e = tc ? launch_tile_tc(p, s) : launch_sample_tile(p, s);
     if (e != cudaSuccess) return DS_ERR_CUDA;
     e = launch_sample_locate(p, s);

@@ -74,7 +74,6 @@ struct Shared {
   uint64_t x_bar;  // barrier of the epilogue threads (all arrive)
   uint32_t tmem_slot;
   int abort_flag;
-  int tok[128];
 };
 
 // Bounded wait (about a second at most): the thread sleeps in try_wait with a
@@ -102,14 +101,39 @@ __device__ __forceinline__ bool epi_barrier(Shared& sh, uint32_t& ph, volatile i
   return ok;
 }
 
-// What the epilogue keeps about its row (a trimmed RowCtx, to save registers).
+// What the epilogue keeps about its row in registers (the general path
+// rebuilds the full row context itself). Np, Nq, Rhi, Rlo: final draw only.
 struct EpiRow {
   int32_t mode;
-  Gscale g;
   G16 g16;
   int32_t Np, Nq;
   float Rhi, Rlo;
+  const __nv_bfloat16* zrow;  // final draw: the request's base and target rows
+  const __nv_bfloat16* trow;
 };
+
+// Row context of a draft row from its temperature alone (no token reads), so
+// it can be formed before the wait on the previous kernel.
+__device__ __forceinline__ EpiRow epi_row_draft(const SampleParams& sp, int row) {
+  EpiRow c;
+  c.mode = kSkip;
+  c.g16 = G16{0.f, 0.f, 0.f};
+  c.Np = c.Nq = 0;
+  c.Rhi = c.Rlo = 0.f;
+  c.zrow = c.trow = nullptr;
+  if (row < sp.B) {
+    const float T = sp.temperature[row];
+    if (T == 0.f) {
+      c.mode = kGreedyMarkov;
+    } else if (T >= 1e-3f && T <= 1e3f) {
+      c.mode = kSampleMarkov;
+      c.g16 = make_g16(T);
+    } else {
+      report(sp.status, kErrInvalidArg);
+    }
+  }
+  return c;
+}
 
 // Fast path of a full sampling chunk (bf16 logits; see fastpath.cuh). False
 // when the chunk needs the general path.
@@ -121,7 +145,8 @@ __device__ __forceinline__ bool sample_chunk_fast(const G16& g16, const uint32_t
   float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < 16; ++i)
-    fast_pair(zp[i], __uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1]), k, shi, slo);
+    fast_pair(zp[i], make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])), k,
+              shi, slo);
   const float hi = __fadd_rn(shi.x, shi.y);  // exact: multiples of 2^-15 below 1024
   const float lo = __fadd_rn(slo.x, slo.y);
   if (!(shi.x >= 0.f && shi.x < kFastHiLimit && shi.y >= 0.f && shi.y < kFastHiLimit &&
@@ -131,6 +156,45 @@ __device__ __forceinline__ bool sample_chunk_fast(const G16& g16, const uint32_t
   rec.hi = r.hi;
   rec.lo = r.lo;
   rec.ref = fref;
+  rec.idx = -2;  // fast-path record
+  return true;
+}
+
+// Fast path of a full chunk of the final draw (bf16; see fastpath.cuh): bonus
+// weights 2^(t g - Np), or residual weights max(0, 2^(t g - Np) - R 2^((z + b) g - Nq)),
+// both against the rows' global references. False when the chunk needs the
+// general path.
+__device__ __forceinline__ bool final_chunk_fast(const EpiRow& c, const uint32_t* zp,
+                                                 const uint32_t* tp, const uint32_t* braw,
+                                                 ChunkRec& rec) {
+  const bool res = (c.mode == kResidual);
+  if (!fast_span_ok(tp, c.g16.G, c.Np)) return false;
+  if (res && !fast_span_ok(zp, c.g16.G, c.Nq)) return false;
+  const FastConsts kp = make_fast_consts(c.g16, c.Np);
+  float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
+  if (res) {
+    const FastConsts kq = make_fast_consts(c.g16, c.Nq);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 wp = fast_w2(tp[i], make_float2(0.f, 0.f), kp);
+      const float2 wq =
+          fast_w2(zp[i], make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])), kq);
+      grid_acc(make_float2(residual_w(wp.x, wq.x, c.Rhi, c.Rlo), residual_w(wp.y, wq.y, c.Rhi, c.Rlo)),
+               kp, shi, slo);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) fast_pair(tp[i], make_float2(0.f, 0.f), kp, shi, slo);
+  }
+  const float hi = __fadd_rn(shi.x, shi.y);
+  const float lo = __fadd_rn(slo.x, slo.y);
+  if (!(shi.x >= 0.f && shi.x < kFastHiLimit && shi.y >= 0.f && shi.y < kFastHiLimit &&
+        isfinite(lo)))
+    return false;
+  const DF r = fast_two_sum(hi, lo);
+  rec.hi = r.hi;
+  rec.lo = r.lo;
+  rec.ref = 0;
   rec.idx = -2;  // fast-path record
   return true;
 }
@@ -167,9 +231,10 @@ __device__ __forceinline__ bool greedy_chunk_fast(const uint32_t* zp, const uint
 // whole warp: it reloads the bias from TMEM (a warp-collective load) and the
 // logits from shared memory, so that the fast paths keep everything in
 // registers. zb / tb: this row's 128-byte logit rows in the (swizzled) slots.
-__device__ __noinline__ ChunkRec slow_chunk_warp(EpiRow c, bool need, uint32_t taddr,
-                                             const uint8_t* zb, const uint8_t* tb, int ch0, int sw,
-                                             int n, int col0, ChunkRec* out, int32_t* status) {
+__device__ __noinline__ ChunkRec slow_chunk_warp(const SampleParams* sp, int row, bool need,
+                                                 uint32_t taddr, const uint8_t* zb,
+                                                 const uint8_t* tb, int ch0, int sw, int col0,
+                                                 ChunkRec* out) {
   uint32_t braw[32];
   tmem_ld32_issue(taddr, braw);
   tmem_ld_wait(braw);
@@ -178,28 +243,30 @@ __device__ __noinline__ ChunkRec slow_chunk_warp(EpiRow c, bool need, uint32_t t
 #pragma unroll
   for (int e = 0; e < 32; ++e) bias[e] = __uint_as_float(braw[e]);
   uint32_t zp[16], tp[16];
+  const RowCtx rc = make_row_ctx<__nv_bfloat16>(*sp, row);
+  const int n = min(32, sp->V - col0);
+  if (zb != nullptr) {
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int off = ((ch0 + u) ^ sw) << 4;
-    const uint4 v = *reinterpret_cast<const uint4*>(zb + off);
-    const uint4 t = *reinterpret_cast<const uint4*>(tb + off);
-    zp[4 * u] = v.x; zp[4 * u + 1] = v.y; zp[4 * u + 2] = v.z; zp[4 * u + 3] = v.w;
-    tp[4 * u] = t.x; tp[4 * u + 1] = t.y; tp[4 * u + 2] = t.z; tp[4 * u + 3] = t.w;
+    for (int u = 0; u < 4; ++u) {
+      const int off = ((ch0 + u) ^ sw) << 4;
+      const uint4 v = *reinterpret_cast<const uint4*>(zb + off);
+      const uint4 t = *reinterpret_cast<const uint4*>(tb + off);
+      zp[4 * u] = v.x; zp[4 * u + 1] = v.y; zp[4 * u + 2] = v.z; zp[4 * u + 3] = v.w;
+      tp[4 * u] = t.x; tp[4 * u + 1] = t.y; tp[4 * u + 2] = t.z; tp[4 * u + 3] = t.w;
+    }
+  } else {  // the rows in global memory (n is even: V % 8 == 0)
+    const uint32_t* zr = reinterpret_cast<const uint32_t*>(
+        reinterpret_cast<const __nv_bfloat16*>(rc.zrow) + col0);
+    const uint32_t* tr = reinterpret_cast<const uint32_t*>(
+        reinterpret_cast<const __nv_bfloat16*>(rc.trow) + col0);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      zp[u] = (rc.zrow && 2 * u < n) ? zr[u] : 0u;
+      tp[u] = (rc.trow && 2 * u < n) ? tr[u] : 0u;
+    }
   }
-  RowCtx rc;
-  rc.mode = c.mode;
-  rc.a_token = -1;
-  rc.zrow = nullptr;
-  rc.trow = nullptr;
-  rc.g = c.g;
-  rc.Np = c.Np;
-  rc.Nq = c.Nq;
-  rc.Rhi = c.Rhi;
-  rc.Rlo = c.Rlo;
-  rc.upos = rc.ustage = 0;
-  rc.out_index = rc.zk = 0;
   ChunkRec r;
-  chunk_record<false>(rc, Bf16Src{zp}, bias, Bf16Src{tp}, n, col0, r, status);
+  chunk_record<false>(rc, Bf16Src{zp}, bias, Bf16Src{tp}, n, col0, r, sp->status);
   *out = r;
   return r;
 }
@@ -217,9 +284,11 @@ __device__ __forceinline__ int a_token_for_row(const SampleParams& sp, int b) {
   return (tok >= 0 && tok < sp.V) ? tok : 0;  // out-of-range ids are reported by make_row_ctx
 }
 
+template <bool kFinal>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tile_tc_kernel(const TcParams prm, const __grid_constant__ CUtensorMap tmP,
-                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmT) {
+    tile_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUtensorMap tmP,
+                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmT,
+                   const __grid_constant__ CUtensorMap tmA) {
   extern __shared__ uint8_t raw[];
   __shared__ Shared sh;
   const SampleParams& sp = prm.sp;
@@ -229,10 +298,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sP = smem + kOffP;
   uint8_t* sZ = smem + kOffZ;
-  const bool draft = (sp.src == 0);
+  constexpr bool draft = !kFinal;
+  const bool staged = (sp.a_stage_in != nullptr);  // A rows staged by the previous locate
 
   if (threadIdx.x == 0) {
-    mbar_init(&sh.a_full, kEpiWarps);
+    mbar_init(&sh.a_full, staged ? 1 : kEpiWarps);
     mbar_init(&sh.a_empty, 1);
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&sh.p_full[i], 1);
@@ -267,11 +337,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t pol_z = policy_evict_first();
     if (lane == 0) {
       prefetch_tmap(&tmP);
-      prefetch_tmap(&tmZ);
-      if (!draft) prefetch_tmap(&tmT);
+      if (draft) prefetch_tmap(&tmZ);
     }
-    uint32_t pc = 0, zc = 0;
-    bool waited = draft, ok = true;  // a draft step's P and logits are inputs, not results
+    if (lane == 0 && staged) prefetch_tmap(&tmA);
+    uint32_t pc = 0, zc = 0, a_loads = 0;
+    int a_mt = -1;
+    bool waited = draft && !staged, ok = true;  // a draft step's P and logits are inputs
     for (int t = t0, i = 0; t < t1 && ok; ++t, ++i) {
       const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
       const int n0 = nt * kTileN;
@@ -301,59 +372,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-      } else {
+      }
+      if (ok && staged && mt != a_mt) {
+        // this M-tile's A rows, written by the previous step's locate; issued after
+        // the tile's P and logit loads so those are in flight during the wait, and
+        // before anything that waits on the MMA
         if (!waited) {
-          pdl_wait();  // final-draw descriptors come from the finalize kernel
+          pdl_wait();
           waited = true;
         }
-        // each request's own base and target rows, one 128-byte box per row and
-        // half; slots 0/1 hold the base-logit halves, slots 2/3 the target halves
-        if (lane == 0)
-          for (int s = 0; s < kZSlots && ok; ++s)
-            ok = wait_bar(&sh.z_empty[s], (i & 1) ^ 1, abort_flag, sp.status);
+        if (lane == 0) {
+          ok = a_loads == 0 || wait_bar(&sh.a_empty, (a_loads - 1) & 1, abort_flag, sp.status);
+          if (ok) {
+            mbar_expect_tx(&sh.a_full, (uint32_t)prm.nkb * 16384u);
+            for (int c = 0; c < prm.nkb; ++c)
+              tma_load_2d(sA + c * 16384, &tmA, &sh.a_full, c * 64, mt * 128, pol_p);
+          }
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        int rows_z[4], rows_t[4];
-        uint32_t nz = 0, ntr = 0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int b = mt * 128 + lane + 32 * u;
-          rows_z[u] = rows_t[u] = -1;
-          if (b < sp.B && sp.temperature[b] != 0.f) {
-            const FinalDesc d = sp.final_desc[b];
-            if (d.mode == kResidual) rows_z[u] = d.row;
-            if (d.mode == kResidual || d.mode == kBonus) rows_t[u] = d.row;
-          }
-          nz += rows_z[u] >= 0;
-          ntr += rows_t[u] >= 0;
-        }
-        for (int o = 16; o > 0; o >>= 1) {
-          nz += __shfl_xor_sync(0xffffffffu, nz, o);
-          ntr += __shfl_xor_sync(0xffffffffu, ntr, o);
-        }
-        if (lane == 0) {
-          for (int s = 0; s < kZSlots; ++s) {
-            const uint32_t bytes = 128u * (s < 2 ? nz : ntr);
-            if (bytes)
-              mbar_expect_tx(&sh.z_full[s], bytes);
-            else
-              mbar_arrive(&sh.z_full[s]);
-          }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int rr = lane + 32 * u, b = mt * 128 + rr;
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-            if (rows_z[u] >= 0)
-              tma_load_3d(sZ + nb * kZSlot + rr * 128, &tmZ, &sh.z_full[nb], n0 + nb * 64,
-                          rows_z[u], b, pol_z);
-            if (rows_t[u] >= 0)
-              tma_load_3d(sZ + (2 + nb) * kZSlot + rr * 128, &tmT, &sh.z_full[2 + nb], n0 + nb * 64,
-                          rows_t[u], b, pol_z);
-          }
-        }
+        ++a_loads;
+        a_mt = mt;
       }
     }
   } else if (warp == 1) {
@@ -399,14 +438,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    pdl_wait();  // tokens and final-draw descriptors come from earlier kernels
     const int ew = warp - 2, et = threadIdx.x - 64;
     const int q = warp & 3, cg = ew >> 2;
     const int r_local = q * 32 + lane;
-    int cur_mt = -1;
+    int cur_mt = -1, pre_mt = -1;
     uint32_t a_uses = 0, xph = 0;
     EpiRow c;
     c.mode = kSkip;
+    if (draft && t0 < t1) {  // temperatures are inputs: read them before the wait
+      pre_mt = t0 / prm.n_nt;
+      c = epi_row_draft(sp, pre_mt * 128 + r_local);
+    }
+    pdl_wait();  // tokens and final-draw descriptors come from earlier kernels
     ChunkRec gacc = group_empty();  // this thread's chunks of the current M-tile
     for (int t = t0, i = 0; t < t1; ++t, ++i) {
       const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
@@ -414,46 +457,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (mt != cur_mt) {
         // A operand of this M-tile: E rows of its conditioning tokens, written
         // 128B-swizzled (16-byte chunk c of row m at c ^ (m & 7)) for the MMA.
-        if (a_uses > 0 && !wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status)) break;
-        if (et < 128) sh.tok[et] = a_token_for_row(sp, mt * 128 + et);
-        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
-        const __nv_bfloat16* E = reinterpret_cast<const __nv_bfloat16*>(sp.E);
-        const int per_row = prm.nkb * 8;
-        const int n_a = 128 * per_row;
-        for (int base = 0; base < n_a; base += 8 * 32 * kEpiWarps) {
-          uint4 v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * 32 * kEpiWarps + et;
-            if (idx < n_a) {
-              const int m = idx / per_row, rem = idx - m * per_row;
-              v[u] = __ldg(reinterpret_cast<const uint4*>(E + (size_t)sh.tok[m] * sp.r + rem * 8));
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * 32 * kEpiWarps + et;
-            if (idx < n_a) {
-              const int m = idx / per_row, rem = idx - m * per_row;
-              const int kb = rem >> 3, ch = rem & 7;
-              *reinterpret_cast<uint4*>(sA + kb * 16384 + m * 128 + ((ch ^ (m & 7)) << 4)) = v[u];
-            }
-          }
+        if (draft) {
+          if (mt != pre_mt) c = epi_row_draft(sp, row);
+        } else {
+          const RowCtx rc = make_row_ctx<__nv_bfloat16>(sp, row);
+          c.mode = rc.mode;
+          c.g16 = (rc.mode == kResidual || rc.mode == kBonus) ? make_g16_from(rc.g) : G16{0.f, 0.f, 0.f};
+          c.Np = rc.Np;
+          c.Nq = rc.Nq;
+          c.Rhi = rc.Rhi;
+          c.Rlo = rc.Rlo;
+          c.zrow = reinterpret_cast<const __nv_bfloat16*>(rc.zrow);
+          c.trow = reinterpret_cast<const __nv_bfloat16*>(rc.trow);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.a_full);
-        ++a_uses;
-        // the token list is rewritten at the next M-tile
-        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
-        const RowCtx rc = make_row_ctx<__nv_bfloat16>(sp, row);
-        c.mode = rc.mode;
-        c.g = rc.g;
-        c.g16 = (rc.mode == kSampleMarkov) ? make_g16(sp.temperature[row]) : G16{0.f, 0.f, 0.f};
-        c.Np = rc.Np;
-        c.Nq = rc.Nq;
-        c.Rhi = rc.Rhi;
-        c.Rlo = rc.Rlo;
+        if (!staged) {
+          if (a_uses > 0 && !wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status)) break;
+          // kThreadsPerRow threads per A row, each a contiguous run of its
+          // 16-byte chunks, all loads in flight before the first store
+          constexpr int kThreadsPerRow = 32 * kEpiWarps / 128;
+          const int m = et / kThreadsPerRow, part = et % kThreadsPerRow;
+          const int per_row = prm.nkb * 8;  // 16-byte chunks per row
+          const int cpt = per_row / kThreadsPerRow;
+          const int tok = a_token_for_row(sp, mt * 128 + m);
+          const uint4* src = reinterpret_cast<const uint4*>(
+              reinterpret_cast<const __nv_bfloat16*>(sp.E) + (size_t)tok * sp.r) + part * cpt;
+          constexpr int kMaxCpt = 32 / kThreadsPerRow;
+          constexpr int kBatch = kMaxCpt < 8 ? kMaxCpt : 8;  // loads in flight per thread
+#pragma unroll
+          for (int u0 = 0; u0 < kMaxCpt; u0 += kBatch) {
+            uint4 v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+              if (u0 + u < cpt) v[u] = __ldg(src + u0 + u);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+              if (u0 + u < cpt) {
+                const int rem = part * cpt + u0 + u, kb = rem >> 3, ch = rem & 7;
+                *reinterpret_cast<uint4*>(sA + kb * 16384 + m * 128 + ((ch ^ (m & 7)) << 4)) = v[u];
+              }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.a_full);
+          ++a_uses;
+        }
         cur_mt = mt;
         gacc = group_empty();
       }
@@ -463,8 +510,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t zc = 2u * i + nb;
       const uint32_t zs = draft ? zc % kZSlots : nb;
       const uint32_t zph = draft ? (zc / kZSlots) & 1 : (i & 1);
-      if (!wait_bar(&sh.z_full[zs], zph, abort_flag, sp.status)) break;
-      if (!draft && !wait_bar(&sh.z_full[2 + nb], zph, abort_flag, sp.status)) break;
+      if (draft && !wait_bar(&sh.z_full[zs], zph, abort_flag, sp.status)) break;
+      // final draw: each thread loads its own row's 2 x 64 tokens (base and
+      // target) straight from global memory, issued before the MMA wait
+      uint4 fz[kChunks][4], ft[kChunks][4];
+      if (kFinal) {
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+          const int col0 = nt * kTileN + (cg * kChunks + j) * 32;
+          const bool full = row < sp.B && col0 + 32 <= sp.V;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            ft[j][u] = (full && c.trow) ? __ldcs(reinterpret_cast<const uint4*>(c.trow + col0) + u)
+                                        : make_uint4(0, 0, 0, 0);
+            fz[j][u] = (full && c.zrow) ? __ldcs(reinterpret_cast<const uint4*>(c.zrow + col0) + u)
+                                        : make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
       if (!wait_bar(&sh.t_full[buf], (i / kAccum) & 1, abort_flag, sp.status)) break;
       tc_fence_after();
       __syncwarp();
@@ -472,7 +535,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint8_t* zb = sZ + zs * kZSlot + r_local * 128;
       const uint8_t* tb = sZ + (draft ? zs : 2 + nb) * kZSlot + r_local * 128;
       const int sw = r_local & 7;
-#pragma unroll kUnrollChunks
+      // the final draw indexes its prefetched rows by j: fully unrolled there
+#pragma unroll(kFinal ? kChunks : kUnrollChunks)
       for (int j = 0; j < kChunks; ++j) {
         uint32_t braw[32];
         tmem_ld32_issue(tbase + (cg * kChunks + j) * 32, braw);
@@ -481,9 +545,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int col0 = nt * kTileN + (cg * kChunks + j) * 32;
         const bool active = row < sp.B && c.mode != kSkip && col0 < sp.V;
         const int n = min(32, sp.V - col0);
-        ChunkRec* out = sp.chunks + (size_t)row * sp.n_chunks + (col0 >> 5);
+        ChunkRec* out = sp.chunks + (size_t)(col0 >> 5) * sp.B + row;  // chunk-major: coalesced
         bool done = !active;
-        if (active && n == 32 && (c.mode == kSampleMarkov || c.mode == kGreedyMarkov)) {
+        if (kFinal) {
+          if (active && n == 32 && (c.mode == kResidual || c.mode == kBonus)) {
+            uint32_t zp[16], tp[16];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint4 t = ft[j][u], v = fz[j][u];
+              tp[4 * u] = t.x; tp[4 * u + 1] = t.y; tp[4 * u + 2] = t.z; tp[4 * u + 3] = t.w;
+              zp[4 * u] = v.x; zp[4 * u + 1] = v.y; zp[4 * u + 2] = v.z; zp[4 * u + 3] = v.w;
+            }
+            ChunkRec rec;
+            done = final_chunk_fast(c, zp, tp, braw, rec);
+            if (done) {
+              *out = rec;
+              group_merge(c.mode, gacc, rec);
+            }
+          }
+        } else if (active && n == 32 && (c.mode == kSampleMarkov || c.mode == kGreedyMarkov)) {
           uint32_t zp[16];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -502,8 +582,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (__any_sync(0xffffffffu, !done)) {
-          const ChunkRec rec = slow_chunk_warp(c, !done, tbase + (cg * kChunks + j) * 32, zb, tb,
-                                               ch0, sw, n, col0, out, sp.status);
+          const ChunkRec rec = slow_chunk_warp(&sp, row, !done, tbase + (cg * kChunks + j) * 32,
+                                               kFinal ? nullptr : zb, kFinal ? nullptr : tb, ch0, sw,
+                                               col0, out);
           if (!done) group_merge(c.mode, gacc, rec);
         }
       }
@@ -529,8 +610,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sh.t_empty[buf]);
-        mbar_arrive(&sh.z_empty[zs]);
-        if (!draft) mbar_arrive(&sh.z_empty[2 + nb]);
+        if (draft) mbar_arrive(&sh.z_empty[zs]);
       }
     }
   }
@@ -590,9 +670,12 @@ bool tc_path_supported(int32_t dtype, int32_t r) {
 }
 
 cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
-  static cudaError_t attr = cudaFuncSetAttribute(
-      tile_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (attr != cudaSuccess) return attr;
+  static cudaError_t attr_d = cudaFuncSetAttribute(
+      tile_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static cudaError_t attr_f = cudaFuncSetAttribute(
+      tile_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (attr_d != cudaSuccess) return attr_d;
+  if (attr_f != cudaSuccess) return attr_f;
   TcParams prm;
   prm.sp = p;
   prm.n_mt = (p.B + 127) / 128;
@@ -624,6 +707,13 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
     const cuuint32_t box[3] = {64, 1, 1};
     if (!encode(&mT, p.target_logits, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
+  CUtensorMap mA = mP;  // unused unless A rows are staged
+  if (p.a_stage_in != nullptr) {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.r, (cuuint64_t)p.B};
+    const cuuint64_t str[1] = {(cuuint64_t)p.r * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!encode(&mA, p.a_stage_in, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
   const int grid = p.sup_groups;
   if (p.sup_tiles != prm.tiles || grid < 1 || grid > prm.tiles) return cudaErrorInvalidValue;
 
@@ -637,7 +727,8 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tile_tc_kernel, prm, mP, mZ, mT);
+  if (p.src == 0) return cudaLaunchKernelEx(&cfg, tile_tc_kernel<false>, prm, mP, mZ, mT, mA);
+  return cudaLaunchKernelEx(&cfg, tile_tc_kernel<true>, prm, mP, mZ, mT, mA);
 }
 
 }  // namespace ds

@@ -2,16 +2,19 @@
 //
 // For a bf16 logit z (8 significant bits) and g = log2(e)/T split as
 // g = G + gl with G truncated to 16 significant bits, a = z*G is exact in fp32.
-// With t = (z + b)*g = a + (b*g + z*gl), the bias term uses g rounded to fp32
-// (its own rounding is far below the tolerance) and z*gl is folded in by FMA:
+// With t = (z + b)*g = a + z*gl + b*g and the chunk reference ref:
 //
-//   k = rint(a) via the 1.5*2^23 rounding constant, d = a - k (exact),
-//   f = d + (b*g + z*gl),  p = 2^f (ex2.approx),  w = p * 2^(k - ref),
+//   m = z*G + C with C = 1.5*2^23 - ref (one rounding: m = C + k, k an
+//       integer within 1/2 of a), -k = C - m and d = a - k (both exact, FMA),
+//   f = b*g + (z*gl + d),  p = 2^f (ex2.approx),
+//   w = p * 2^(k - ref): the float bits of m hold 1.5*2^23 + (k - ref), so
+//       bits(p) + (bits(m) << 23) adds k - ref to p's exponent field.
 //
-// the last factor applied to p's exponent field. The chunk reference ref is
-// rint(max_j z_j * G). The path is taken only when every z of the chunk is
-// finite and spans less than 96 / G (so 2^(k - ref) stays a normal number);
-// otherwise the general path of common.cuh is used.
+// The chunk reference is ref = rint(max_j z_j * G). The path is taken only
+// when every z of the chunk is finite and spans less than 96 / G (so the
+// scaled weights stay normal numbers) and |max z * G| < 4e6 (so C stays in
+// [2^23, 2^24), where the float spacing is 1); otherwise the general path of
+// common.cuh is used.
 //
 // Chunk sums on this path are exact up to ~2^-36 relative: each weight is split
 // on a fixed 2^-15 grid, w = w_hi + w_lo with w_hi = (w + 384) - 384 (exact),
@@ -37,58 +40,73 @@ struct G16 {
   float G, gl, gf;  // g = G + gl exactly to ~2^-40; gf = g rounded to fp32
 };
 
+__device__ __forceinline__ G16 make_g16_from(Gscale g) {
+  const float G = __uint_as_float(__float_as_uint(g.hi) & 0xFFFFFF00u);
+  return {G, __fadd_rn(__fsub_rn(g.hi, G), g.lo), g.hi};  // g.hi - G is exact
+}
+
 __device__ __forceinline__ G16 make_g16(float T) {
   const Gscale g = make_gscale(T);
   const float G = __uint_as_float(__float_as_uint(g.hi) & 0xFFFFFF00u);
   return {G, __fadd_rn(__fsub_rn(g.hi, G), g.lo), g.hi};  // g.hi - G is exact
 }
 
-// Scalar weight, bit-identical to one lane of fast_w2.
-__device__ __forceinline__ float fast_w1(float z, float b, G16 g, uint32_t ref23) {
-  const float a = __fmul_rn(z, g.G);
-  const float t = __fmul_rn(b, g.gf);
-  const float tl = __fmaf_rn(z, g.gl, t);
-  const float m = __fadd_rn(a, kMagic);
-  const float kf = __fadd_rn(m, -kMagic);
-  const float d = __fmaf_rn(kf, -1.0f, a);
-  const float f = __fadd_rn(d, tl);
+// Scalar weight, bit-identical to one lane of fast_pair (used by the locate).
+__device__ __forceinline__ float fast_w1(float z, float b, G16 g, int ref) {
+  const float C = __fsub_rn(kMagic, (float)ref);
+  const float m = __fmaf_rn(z, g.G, C);
+  const float nk = __fmaf_rn(m, -1.0f, C);
+  const float d = __fmaf_rn(z, g.G, nk);
+  const float f = __fmaf_rn(b, g.gf, __fmaf_rn(z, g.gl, d));
   const float p = ex2_approx(f);
-  return __uint_as_float(__float_as_uint(p) + (__float_as_uint(m) << 23) - ref23);
+  return __uint_as_float(__float_as_uint(p) + (__float_as_uint(m) << 23));
 }
 
 struct FastConsts {
-  float G, gl, gf;
-  uint32_t ref23;
+  float2 G, gl, gf, C, neg1;
 };
 
 __device__ __forceinline__ FastConsts make_fast_consts(G16 g, int ref) {
-  return {g.G, g.gl, g.gf, (uint32_t)ref << 23};
+  const float C = __fsub_rn(kMagic, (float)ref);
+  return {make_float2(g.G, g.G), make_float2(g.gl, g.gl), make_float2(g.gf, g.gf), make_float2(C, C),
+          make_float2(-1.0f, -1.0f)};
 }
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Weights of the two tokens packed in zw, accumulated into (shi, slo).
-__device__ __forceinline__ void fast_pair(uint32_t zw, float b0, float b1, const FastConsts& k,
-                                          float2& shi, float2& slo) {
+// Weights of the two tokens packed in zw (bias b2) against the constants' reference.
+__device__ __forceinline__ float2 fast_w2(uint32_t zw, float2 b2, const FastConsts& k) {
   const float2 z2 = unpack_bf16x2(zw);
-  const float2 a2 = __fmul2_rn(z2, make_float2(k.G, k.G));
-  const float2 t2 = __fmul2_rn(make_float2(b0, b1), make_float2(k.gf, k.gf));
-  const float2 tl2 = __ffma2_rn(z2, make_float2(k.gl, k.gl), t2);
-  const float2 m2 = __fadd2_rn(a2, make_float2(kMagic, kMagic));
-  const float2 kf2 = __fadd2_rn(m2, make_float2(-kMagic, -kMagic));
-  const float2 d2 = __ffma2_rn(kf2, make_float2(-1.0f, -1.0f), a2);
-  const float2 f2 = __fadd2_rn(d2, tl2);
+  const float2 m2 = __ffma2_rn(z2, k.G, k.C);
+  const float2 nk2 = __ffma2_rn(m2, k.neg1, k.C);
+  const float2 d2 = __ffma2_rn(z2, k.G, nk2);
+  const float2 f2 = __ffma2_rn(b2, k.gf, __ffma2_rn(z2, k.gl, d2));
   const float p0 = ex2_approx(f2.x), p1 = ex2_approx(f2.y);
-  const float2 w2 =
-      make_float2(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(m2.x) << 23) - k.ref23),
-                  __uint_as_float(__float_as_uint(p1) + (__float_as_uint(m2.y) << 23) - k.ref23));
+  return make_float2(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(m2.x) << 23)),
+                     __uint_as_float(__float_as_uint(p1) + (__float_as_uint(m2.y) << 23)));
+}
+
+// Exact grid-split accumulation of two weights in [0, 512).
+__device__ __forceinline__ void grid_acc(float2 w2, const FastConsts& k, float2& shi, float2& slo) {
   const float2 tt = __fadd2_rn(w2, make_float2(kGrid, kGrid));
   const float2 wh = __fadd2_rn(tt, make_float2(-kGrid, -kGrid));
-  const float2 wl = __ffma2_rn(wh, make_float2(-1.0f, -1.0f), w2);
+  const float2 wl = __ffma2_rn(wh, k.neg1, w2);
   shi = __fadd2_rn(shi, wh);
   slo = __fadd2_rn(slo, wl);
+}
+
+// Weights of the two tokens packed in zw, accumulated into (shi, slo).
+__device__ __forceinline__ void fast_pair(uint32_t zw, float2 b2, const FastConsts& k, float2& shi,
+                                          float2& slo) {
+  grid_acc(fast_w2(zw, b2, k), k, shi, slo);
+}
+
+// Residual weight max(0, wp - R * wq) of one token, R = Rhi + Rlo (two FMAs,
+// the order every side uses).
+__device__ __forceinline__ float residual_w(float wp, float wq, float Rhi, float Rlo) {
+  return fmaxf(__fmaf_rn(-wq, Rlo, __fmaf_rn(-wq, Rhi, wp)), 0.f);
 }
 
 // Scalar split of one weight on the same grid (for prefix sums in the locate).
@@ -96,6 +114,24 @@ __device__ __forceinline__ void fast_split(float w, float& wh, float& wl) {
   const float tt = __fadd_rn(w, kGrid);
   wh = __fadd_rn(tt, -kGrid);
   wl = __fmaf_rn(wh, -1.0f, w);
+}
+
+// Chunk predicate against a given reference (the row-global references of the
+// final draw): every logit finite, z*G within (ref - 96, ref + 1], |z*G| < 4e6.
+__device__ __forceinline__ bool fast_span_ok(const uint32_t* zp, float G, int ref) {
+  __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&zp[0]);
+  __nv_bfloat162 mn = mx;
+#pragma unroll
+  for (int i = 1; i < 16; ++i) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&zp[i]);
+    mx = __hmax2(mx, v);
+    mn = __hmin2(mn, v);
+  }
+  const float zmax = fmaxf(__low2float(mx), __high2float(mx));
+  const float zmin = fminf(__low2float(mn), __high2float(mn));
+  const float r = (float)ref;
+  return (zmin > kNegInf) && (fabsf(zmax * G) < 4.0e6f) && (r - zmin * G < kFastSpan) &&
+         (zmax * G <= r + 1.0f) && (fabsf(r) < 4.0e6f);
 }
 
 // Chunk predicate and reference from the packed bf16 logits of 32 tokens.

@@ -58,7 +58,12 @@ struct SampleParams {
   const int32_t* draft_tokens;  // [B][K] (read: previous positions; written by locate)
   const float* temperature;
   const FinalDesc* final_desc;  // [B]
-  ChunkRec* chunks;             // [B][n_chunks]
+  ChunkRec* chunks;             // [n_chunks][B] (chunk-major: a warp's rows store contiguously)
+  // Staged A operand: the locate of step k writes E[x_k] rows here
+  // (a_stage_out), the tensor-core tile kernel of step k+1 loads them with TMA
+  // (a_stage_in). Null where unused (first step, last step, SIMT path).
+  const void* a_stage_in;       // [B][r]
+  void* a_stage_out;            // [B][r]
   // Group records: the chunks of a row are also combined per column group
   // (the contiguous token range one tile CTA covers), so that the locate scans
   // a few hundred group records and then the chunks of one group only.

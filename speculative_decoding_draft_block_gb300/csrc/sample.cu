@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) sample_tile_kernel(SampleParams p) {
       chunk_record<true>(c, F32Src{z}, acc, F32Src{t}, 32, col0, rec, p.status);
     else
       chunk_record<false>(c, F32Src{z}, acc, F32Src{t}, n, col0, rec, p.status);
-    p.chunks[(size_t)row * p.n_chunks + chunk] = rec;
+    p.chunks[(size_t)chunk * p.B + row] = rec;
   }
   // group record of the row's 256 tokens: the 8 lanes of a row are adjacent
   ChunkRec g = rec;
@@ -152,6 +152,16 @@ __device__ __forceinline__ DF shfl_up_df(DF v, int o) {
 
 __device__ __forceinline__ bool df_gt(DF a, DF b) {
   return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+// The drawn token's E row into the staged A operand of the next step (warp).
+template <typename Tin>
+__device__ __forceinline__ void stage_e_row(const SampleParams& p, int b, int tok, int lane) {
+  if (p.a_stage_out == nullptr) return;
+  const int n16 = p.r * (int)sizeof(Tin) / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(p.E) + (size_t)tok * p.r);
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(p.a_stage_out) + (size_t)b * p.r);
+  for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
 }
 
 // Warp-wide inclusive double-float prefix sum.
@@ -238,12 +248,10 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
         const ChunkRec ov = shfl_xor_rec(best, o);
         if (greedy_better(ov, best)) best = ov;
       }
+      const int bx = best.idx < 0 ? 0 : best.idx;
+      stage_e_row<Tin>(p, b, bx, lane);
       if (lane == 0) {
-        int bx = best.idx;
-        if (bx < 0) {
-          bx = 0;
-          report(p.status, kErrNonfinite);
-        }
+        if (best.idx < 0) report(p.status, kErrNonfinite);
         p.tokens_out[c.out_index] = bx;
         if (p.src == 0) {
           p.q_token[c.out_index] = 1.f;
@@ -303,6 +311,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
         }
       }
       if (gsel < 0) {
+        stage_e_row<Tin>(p, b, 0, lane);
         if (lane == 0) {
           report(p.status, kErrNonfinite);
           p.tokens_out[c.out_index] = 0;
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
         const int mt0 = mt * p.sup_nt;
         const int ta = max(group_tile0(p, g), mt0), tb = min(group_tile0(p, g + 1), mt0 + p.sup_nt);
         const int ch_lo = (ta - mt0) * p.sup_cpt, ch_hi = min((tb - mt0) * p.sup_cpt, nc);
-        const ChunkRec* crow = p.chunks + (size_t)b * nc;
+        const ChunkRec* crow = p.chunks + b;  // chunk i of row b at crow[i * B]
         DF run = gexcl, fexcl = gexcl, lexcl = gexcl;
         int found = -1, last = -1;
         ChunkRec frec = group_empty(), lrec = group_empty();
@@ -323,7 +332,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int i = base + 32 * u + lane;
-            rr[u] = i < ch_hi ? ld_rec(crow + i) : group_empty();
+            rr[u] = i < ch_hi ? ld_rec(crow + (size_t)i * p.B) : group_empty();
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -357,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
         if (found < 0) {  // rounding left u*S past the group's in-order total
           found = last >= 0 ? last : ch_lo;
           fexcl = last >= 0 ? lexcl : gexcl;
-          frec = last >= 0 ? lrec : ld_rec(crow + found);
+          frec = last >= 0 ? lrec : ld_rec(crow + (size_t)found * p.B);
         }
         if (lane == 0) {
           s_found = found;
@@ -447,18 +456,24 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
       const int ref = cr.ref;
       if (lane < n && ref != kEmptyRef) {
         if (cr.idx == -2)
-          w = fast_w1(zl, bsum, make_g16(p.temperature[b]), (uint32_t)ref << 23);
+          w = fast_w1(zl, bsum, make_g16(p.temperature[b]), ref);
         else
           w = weight_rel(zl, bsum, c.g, ref);
       }
       e = (ref == kEmptyRef) ? -300 : max(ref - N, -300);
     } else if (lane < n) {
-      w = weight_rel(tl, 0.f, c.g, c.Np);
-      if (c.mode == kResidual) {
-        const float wq = weight_rel(zl, bsum, c.g, c.Nq);
-        float d = __fmaf_rn(-wq, c.Rhi, w);
-        d = __fmaf_rn(-wq, c.Rlo, d);
-        w = fmaxf(d, 0.f);
+      if (s_crec.idx == -2) {  // fast-path record of the final draw
+        const G16 g16 = make_g16_from(c.g);
+        w = fast_w1(tl, 0.f, g16, c.Np);
+        if (c.mode == kResidual) w = residual_w(w, fast_w1(zl, bsum, g16, c.Nq), c.Rhi, c.Rlo);
+      } else {
+        w = weight_rel(tl, 0.f, c.g, c.Np);
+        if (c.mode == kResidual) {
+          const float wq = weight_rel(zl, bsum, c.g, c.Nq);
+          float d = __fmaf_rn(-wq, c.Rhi, w);
+          d = __fmaf_rn(-wq, c.Rlo, d);
+          w = fmaxf(d, 0.f);
+        }
       }
     }
     if (!(w >= 0.f) || !isfinite(w)) w = 0.f;
@@ -472,6 +487,7 @@ __global__ void __launch_bounds__(kThreads) sample_locate_kernel(SampleParams p)
     const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
     const int xl = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
     const float wx = __shfl_sync(0xffffffffu, w, xl);
+    stage_e_row<Tin>(p, b, col0 + xl, lane);
     if (lane == 0) {
       if (!pos) report(p.status, kErrNonfinite);
       p.tokens_out[c.out_index] = col0 + xl;

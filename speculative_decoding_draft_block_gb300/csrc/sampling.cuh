@@ -204,7 +204,8 @@ __device__ __forceinline__ void chunk_record(const RowCtx& c, ZS z, const float*
 // A group record combines the chunk records of a contiguous token range:
 //   sampling rows: ref = the largest chunk reference, hi + lo = the sum of the
 //                  chunk sums each scaled by 2^(chunk ref - ref) (exact powers
-//                  of two; contributions below 2^-252 relative are dropped)
+//                  of two; chunks below 2^-126 relative to the group's
+//                  reference are dropped, far below the sampling tolerance)
 //   greedy rows:   the largest (hi, lo) with the smallest token on ties
 //   residual/bonus rows: the plain double-float sum (records share ref 0)
 
@@ -237,19 +238,19 @@ __device__ __forceinline__ bool greedy_better(const ChunkRec& a, const ChunkRec&
   return a.hi > b.hi || (a.hi == b.hi && (a.lo > b.lo || (a.lo == b.lo && a.idx < b.idx)));
 }
 
+// 2^e for e in [-127, 0] as a float (2^-127 -> +0: contributions below 2^-126
+// relative to the group's reference are dropped).
+__device__ __forceinline__ float pow2_clamped(int e) { return __int_as_float((max(e, -127) + 127) << 23); }
+
 __device__ __forceinline__ void group_merge(int mode, ChunkRec& acc, const ChunkRec& r) {
   if (mode == kGreedyMarkov) {
     if (greedy_better(r, acc)) acc = r;
   } else if (mode == kSampleMarkov) {
-    if (r.ref == kEmptyRef) return;
-    if (acc.ref == kEmptyRef) {
-      acc.hi = r.hi;
-      acc.lo = r.lo;
-      acc.ref = r.ref;
-      return;
-    }
+    // branch-free: an empty side (ref kEmptyRef, sum 0) scales to 0
     const int R = max(acc.ref, r.ref);
-    const DF s = df_add(rec_scaled(acc, R), rec_scaled(r, R));
+    const float fa = pow2_clamped(acc.ref - R), fr = pow2_clamped(r.ref - R);
+    const DF s = df_add(DF{__fmul_rn(acc.hi, fa), __fmul_rn(acc.lo, fa)},
+                        DF{__fmul_rn(r.hi, fr), __fmul_rn(r.lo, fr)});
     acc.hi = s.hi;
     acc.lo = s.lo;
     acc.ref = R;

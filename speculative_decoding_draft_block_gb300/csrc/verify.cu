@@ -19,7 +19,10 @@
 #include <float.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
+#include "fastpath.cuh"
 #include "internal.h"
 #include "sampling.cuh"
 #include "sm100.cuh"
@@ -29,6 +32,89 @@ namespace ds {
 namespace {
 
 constexpr int kRowThreads = 512;
+
+// Row sum of one thread's 8-token groups of bf16 target logits, relative to a
+// running integer reference R (the largest group reference seen). Groups go
+// through the fast path of fastpath.cuh against R; a group that raises R first
+// folds the exact grid sums into the double-float total and rescales it by a
+// power of two; groups the fast path cannot take (non-finite, too wide a span
+// below R) fall back to weight_rel. Returns false if nothing was finite.
+__device__ __forceinline__ bool row_sum_bf16(const __nv_bfloat16* row, int V, int tid, Gscale g,
+                                             DF& total, int& R, bool& bad) {
+  const G16 g16 = make_g16_from(g);
+  R = INT_MIN;
+  total = {0.f, 0.f};
+  float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
+  int pending = 0;  // groups in the grid accumulators since the last fold
+  FastConsts k = make_fast_consts(g16, 0);
+  for (int i = tid * 8; i < V; i += kRowThreads * 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + i));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mn = mx;
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+      const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&w[q]);
+      mx = __hmax2(mx, t);
+      mn = __hmin2(mn, t);
+    }
+    const float zmax = fmaxf(__low2float(mx), __high2float(mx));
+    const float zmin = fminf(__low2float(mn), __high2float(mn));
+    const bool finite = zmin > kNegInf && zmax < __int_as_float(0x7f800000) && zmax == zmax &&
+                        fabsf(zmax * g16.G) < 4.0e6f;
+    if (finite) {
+      const int gref = (int)rintf(__fmul_rn(zmax, g16.G));
+      if (gref > R || pending == 32) {
+        // fold the grid sums into the total, then move the reference up
+        const DF part = fast_two_sum(__fadd_rn(shi.x, shi.y), __fadd_rn(slo.x, slo.y));
+        total = df_add(total, part);
+        shi = slo = make_float2(0.f, 0.f);
+        pending = 0;
+        if (gref > R) {
+          if (R != INT_MIN) {
+            const float f = pow2_clamped(R - gref);
+            total = {__fmul_rn(total.hi, f), __fmul_rn(total.lo, f)};
+          }
+          R = gref;
+          k = make_fast_consts(g16, R);
+        }
+      }
+      if ((float)R - __fmul_rn(zmin, g16.G) < kFastSpan) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) fast_pair(w[q], make_float2(0.f, 0.f), k, shi, slo);
+        ++pending;
+        continue;
+      }
+    }
+    // general path for this group (relative to R, or to a new R if none yet)
+    float f8[8];
+    load8(row + i, f8);
+    float amax = kNegInf;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      bad |= bad_logit(f8[q]);
+      if (f8[q] != kNegInf) amax = fmaxf(amax, scaled_hi(f8[q], g));
+    }
+    if (amax == kNegInf) continue;
+    const int ng = (int)rintf(amax);
+    if (ng > R) {
+      const DF part = fast_two_sum(__fadd_rn(shi.x, shi.y), __fadd_rn(slo.x, slo.y));
+      total = df_add(total, part);
+      shi = slo = make_float2(0.f, 0.f);
+      pending = 0;
+      if (R != INT_MIN) {
+        const float f = pow2_clamped(R - ng);
+        total = {__fmul_rn(total.hi, f), __fmul_rn(total.lo, f)};
+      }
+      R = ng;
+      k = make_fast_consts(g16, R);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) df_accumulate(total, weight_rel(f8[q], 0.f, g, R));
+  }
+  const DF part = fast_two_sum(__fadd_rn(shi.x, shi.y), __fadd_rn(slo.x, slo.y));
+  total = df_add(total, part);
+  return R != INT_MIN;
+}
 
 template <typename Tin>
 __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p) {
@@ -102,6 +188,10 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
     const Gscale g = make_gscale(T);
     int nt = INT_MIN;
     DF acc = {0.f, 0.f};
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+      int R;
+      if (row_sum_bf16(row, p.V, tid, g, acc, R, bad)) nt = R;
+    } else
     for (int i = tid * 8; i < p.V; i += kRowThreads * 8) {
       float v[8];
       load8(row + i, v);
@@ -126,7 +216,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
     __syncthreads();
     int N = sref[0];
     for (int w = 1; w < kRowThreads / 32; ++w) N = max(N, sref[w]);
-    sdf[tid] = (nt == INT_MIN) ? DF{0.f, 0.f} : df_scale2(acc, max(nt - N, -300));
+    sdf[tid] = (nt == INT_MIN) ? DF{0.f, 0.f} : rec_scaled(ChunkRec{acc.hi, acc.lo, nt, 0}, N);
     __syncthreads();
     // fixed-order tree reduction
     for (int s = kRowThreads / 2; s > 0; s >>= 1) {
