@@ -12,7 +12,10 @@
 //                      products), sigmoid.
 //   schedule_kernel    one CTA: survival cumprod, bitonic sort of 64-bit keys
 //                      (survival descending, then k, then b) in shared memory,
-//                      double-precision prefix scan of A and J, first drop.
+//                      double-float prefix scan of A, first drop of J tested
+//                      without division: J' > J <=> SPS(N+1) (A+s) N > SPS(N) A (N+1).
+//                      (double precision runs at a small fraction of the float
+//                      rate here, and this kernel is one CTA on one SM)
 #include <cuda_bf16.h>
 #include <float.h>
 #include <stdint.h>
@@ -27,7 +30,20 @@ namespace {
 template <typename Tin>
 __device__ __forceinline__ float dot_warp(const Tin* a, const Tin* w, int n, int lane) {
   float acc = 0.f;
-  for (int i = lane * 8; i < n; i += 32 * 8) {
+  int i = lane * 8;
+  for (; i + 3 * 256 < n; i += 4 * 256) {  // four groups of loads in flight
+    float x[4][8], y[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      load8(a + i + u * 256, x[u]);
+      load8(w + i + u * 256, y[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc = __fmaf_rn(x[u][q], y[u][q], acc);
+  }
+  for (; i < n; i += 32 * 8) {
     float x[8], y[8];
     load8(a + i, x);
     load8(w + i, y);
@@ -55,22 +71,44 @@ __global__ void __launch_bounds__(256) confidence_kernel(SchedParams p) {
   const float de = dot_warp(E, reinterpret_cast<const Tin*>(p.w_e), p.r, lane);
   if (lane == 0) {
     const float Tk = p.sts_temp[k];
-    const float logit = (dh + de + p.bias) / Tk;
-    const float c = 1.f / (1.f + expf(-logit));
+    const float logit = __fdiv_rn(__fadd_rn(__fadd_rn(dh, de), p.bias), Tk);
+    const float c = __frcp_rn(__fadd_rn(1.f, expf(-logit)));
     if (!(c == c) || !(Tk > 0.f)) report(p.status, kErrNonfinite);
     p.conf[item] = c;
   }
 }
 
-__device__ __forceinline__ double sps_at(const float* sps, int n_max, int n) {
-  return (double)sps[(n < n_max ? n : n_max) - 1];
+__device__ __forceinline__ float sps_at(const float* sps, int n_max, int n) {
+  return sps[(n < n_max ? n : n_max) - 1];
+}
+
+__device__ __forceinline__ DF shfl_up_df2(DF v, int o) {
+  return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+
+// J = SPS(N) * A / N as a double (for the objective output only).
+__device__ __forceinline__ double objective_of(float sps, DF A, int N) {
+  const DF num = df_mul(DF{sps, 0.f}, A);
+  const float q = __fdiv_rn(num.hi, (float)N);
+  const DF back = df_mul(DF{q, 0.f}, DF{(float)N, 0.f});
+  const DF res = df_add(num, DF{-back.hi, -back.lo});
+  const float ql = __fdiv_rn(res.hi, (float)N);
+  return (double)q + (double)ql;
+}
+
+// J(N+1, A+s) > J(N, A) without division (all factors positive).
+__device__ __forceinline__ bool gains(float sps1, float sps0, DF A, float s, int N) {
+  const DF A1 = df_add(A, DF{s, 0.f});
+  const DF lhs = df_mul(df_mul(DF{sps1, 0.f}, A1), DF{(float)N, 0.f});
+  const DF rhs = df_mul(df_mul(DF{sps0, 0.f}, A), DF{(float)(N + 1), 0.f});
+  return lhs.hi > rhs.hi || (lhs.hi == rhs.hi && lhs.lo > rhs.lo);
 }
 
 constexpr int kSchedThreads = 1024;
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) {
   extern __shared__ unsigned long long keys[];
-  __shared__ double wsum[32];
+  __shared__ DF wsum[32];
   __shared__ int red[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int B = p.B, K = p.K, n = B * K;
@@ -88,15 +126,31 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   }
   __syncthreads();
   if (p.mode != DS_SCHED_GREEDY_EARLYSTOP) {
+    // objective of the fixed selection: block sums of N and A (double-float)
+    int nsum = 0;
+    DF a = {0.f, 0.f};
+    for (int b = tid; b < B; b += kSchedThreads) {
+      const int L = p.sched_len[b];
+      nsum += L;
+      for (int k = 0; k < L; ++k) a = df_add(a, DF{p.survival[(size_t)b * K + k], 0.f});
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      nsum += __shfl_xor_sync(0xffffffffu, nsum, o);
+      a = df_add(a, DF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)});
+    }
+    if (lane == 0) {
+      red[wid] = nsum;
+      wsum[wid] = a;
+    }
+    __syncthreads();
     if (tid == 0) {
-      long long nsum = B;
-      double a = B;
-      for (int b = 0; b < B; ++b) {
-        const int L = p.sched_len[b];
-        nsum += L;
-        for (int k = 0; k < L; ++k) a += (double)p.survival[(size_t)b * K + k];
+      int N = B;
+      DF A = {(float)B, 0.f};
+      for (int w = 0; w < kSchedThreads / 32; ++w) {
+        N += red[w];
+        A = df_add(A, wsum[w]);
       }
-      p.objective[0] = sps_at(p.sps, p.n_max, (int)nsum) * a / (double)nsum;
+      p.objective[0] = objective_of(sps_at(p.sps, p.n_max, N), A, N);
     }
     return;
   }
@@ -130,46 +184,44 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
     }
   }
 
-  // A_m = B + sum of the first m sorted survivals (double); each thread owns a
-  // contiguous run of sorted candidates.
+  // A_m = B + sum of the first m sorted survivals (double-float); each thread
+  // owns a contiguous run of sorted candidates.
   const int per = (n + kSchedThreads - 1) / kSchedThreads;
   const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
-  double local = 0.0;
+  DF local = {0.f, 0.f};
   for (int i = i0; i < i1; ++i)
-    local += (double)__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
+    local = df_add(local, DF{__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32)), 0.f});
   // block exclusive scan of `local`
-  double incl = local;
+  DF incl = local;
   for (int o = 1; o < 32; o <<= 1) {
-    const double v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
+    const DF v = shfl_up_df2(incl, o);
+    if (lane >= o) incl = df_add(v, incl);
   }
   if (lane == 31) wsum[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    double v = wsum[lane];
+    DF v = wsum[lane];
     for (int o = 1; o < 32; o <<= 1) {
-      const double u = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += u;
+      const DF u = shfl_up_df2(v, o);
+      if (lane >= o) v = df_add(u, v);
     }
     wsum[lane] = v;  // inclusive over warps
   }
   __syncthreads();
-  double excl = incl - local + (wid > 0 ? wsum[wid - 1] : 0.0);
+  DF excl = shfl_up_df2(incl, 1);
+  if (lane == 0) excl = DF{0.f, 0.f};
+  if (wid > 0) excl = df_add(wsum[wid - 1], excl);
 
   int first_drop = INT_MAX;
-  double a_prev = (double)B + excl;
-  double j_prev = sps_at(p.sps, p.n_max, B + i0) * a_prev / (double)(B + i0);
+  DF a_prev = df_add(DF{(float)B, 0.f}, excl);
   for (int i = i0; i < i1; ++i) {
-    const double s = (double)__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
-    const double a_new = a_prev + s;
-    const int nn = B + i + 1;
-    const double j_new = sps_at(p.sps, p.n_max, nn) * a_new / (double)nn;
-    if (!(j_new > j_prev)) {
+    const float sv = __uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
+    const int nb = B + i;  // verified tokens before adding candidate i
+    if (!gains(sps_at(p.sps, p.n_max, nb + 1), sps_at(p.sps, p.n_max, nb), a_prev, sv, nb)) {
       first_drop = i;
       break;
     }
-    a_prev = a_new;
-    j_prev = j_new;
+    a_prev = df_add(a_prev, DF{sv, 0.f});
   }
   for (int o = 16; o > 0; o >>= 1) first_drop = min(first_drop, __shfl_xor_sync(0xffffffffu, first_drop, o));
   if (lane == 0) red[wid] = first_drop;
@@ -185,11 +237,12 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   }
   // objective at the chosen set: thread owning item M-1 (or thread 0 for M = 0)
   if (M == 0) {
-    if (tid == 0) p.objective[0] = sps_at(p.sps, p.n_max, B);
+    if (tid == 0) p.objective[0] = (double)sps_at(p.sps, p.n_max, B);
   } else if (M - 1 >= i0 && M - 1 < i1) {
-    double a = (double)B + excl;
-    for (int i = i0; i < M; ++i) a += (double)__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
-    p.objective[0] = sps_at(p.sps, p.n_max, B + M) * a / (double)(B + M);
+    DF a = df_add(DF{(float)B, 0.f}, excl);
+    for (int i = i0; i < M; ++i)
+      a = df_add(a, DF{__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32)), 0.f});
+    p.objective[0] = objective_of(sps_at(p.sps, p.n_max, B + M), a, B + M);
   }
 }
 

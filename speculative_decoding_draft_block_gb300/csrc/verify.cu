@@ -47,8 +47,21 @@ __device__ __forceinline__ bool row_sum_bf16(const __nv_bfloat16* row, int V, in
   float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
   int pending = 0;  // groups in the grid accumulators since the last fold
   FastConsts k = make_fast_consts(g16, 0);
-  for (int i = tid * 8; i < V; i += kRowThreads * 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + i));
+  // fold the grid sums into the total and move the reference up to nr (>= R)
+  auto fold = [&](int nr) {
+    total = df_add(total, fast_two_sum(__fadd_rn(shi.x, shi.y), __fadd_rn(slo.x, slo.y)));
+    shi = slo = make_float2(0.f, 0.f);
+    pending = 0;
+    if (nr > R) {
+      if (R != INT_MIN) {
+        const float f = pow2_clamped(R - nr);
+        total = {__fmul_rn(total.hi, f), __fmul_rn(total.lo, f)};
+      }
+      R = nr;
+      k = make_fast_consts(g16, R);
+    }
+  };
+  auto group = [&](const uint4 v, int i) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mn = mx;
 #pragma unroll
@@ -63,56 +76,45 @@ __device__ __forceinline__ bool row_sum_bf16(const __nv_bfloat16* row, int V, in
                         fabsf(zmax * g16.G) < 4.0e6f;
     if (finite) {
       const int gref = (int)rintf(__fmul_rn(zmax, g16.G));
-      if (gref > R || pending == 32) {
-        // fold the grid sums into the total, then move the reference up
-        const DF part = fast_two_sum(__fadd_rn(shi.x, shi.y), __fadd_rn(slo.x, slo.y));
-        total = df_add(total, part);
-        shi = slo = make_float2(0.f, 0.f);
-        pending = 0;
-        if (gref > R) {
-          if (R != INT_MIN) {
-            const float f = pow2_clamped(R - gref);
-            total = {__fmul_rn(total.hi, f), __fmul_rn(total.lo, f)};
-          }
-          R = gref;
-          k = make_fast_consts(g16, R);
-        }
-      }
+      if (gref > R || pending == 32) fold(gref);
       if ((float)R - __fmul_rn(zmin, g16.G) < kFastSpan) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) fast_pair(w[q], make_float2(0.f, 0.f), k, shi, slo);
         ++pending;
-        continue;
+        return;
       }
     }
     // general path for this group (relative to R, or to a new R if none yet)
     float f8[8];
-    load8(row + i, f8);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      f8[2 * q] = __uint_as_float(w[q] << 16);
+      f8[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+    }
     float amax = kNegInf;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       bad |= bad_logit(f8[q]);
       if (f8[q] != kNegInf) amax = fmaxf(amax, scaled_hi(f8[q], g));
     }
-    if (amax == kNegInf) continue;
+    if (amax == kNegInf) return;
     const int ng = (int)rintf(amax);
-    if (ng > R) {
-      const DF part = fast_two_sum(__fadd_rn(shi.x, shi.y), __fadd_rn(slo.x, slo.y));
-      total = df_add(total, part);
-      shi = slo = make_float2(0.f, 0.f);
-      pending = 0;
-      if (R != INT_MIN) {
-        const float f = pow2_clamped(R - ng);
-        total = {__fmul_rn(total.hi, f), __fmul_rn(total.lo, f)};
-      }
-      R = ng;
-      k = make_fast_consts(g16, R);
-    }
+    if (ng > R) fold(ng);
 #pragma unroll
     for (int q = 0; q < 8; ++q) df_accumulate(total, weight_rel(f8[q], 0.f, g, R));
+  };
+  // four 16-byte loads in flight per thread
+  constexpr int kStride = kRowThreads * 8;
+  for (int i0 = tid * 8; i0 < V; i0 += 4 * kStride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * kStride < V) v[u] = __ldcs(reinterpret_cast<const uint4*>(row + i0 + u * kStride));
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * kStride < V) group(v[u], i0 + u * kStride);
   }
-  const DF part = fast_two_sum(__fadd_rn(shi.x, shi.y), __fadd_rn(slo.x, slo.y));
-  total = df_add(total, part);
+  fold(R);
   return R != INT_MIN;
 }
 
