@@ -233,6 +233,26 @@ typedef struct {
 size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
 ds_status ds_verify(const ds_verify_args* args, ds_stream_t stream);
 
+/*
+ * ds_verify without a caller workspace. The pages have no counterpart: this is
+ * an integration entry point for callers that cannot allocate device memory
+ * (hosts without a device allocator, or serving loops that must not call
+ * cudaMalloc/cudaFree, which synchronise the device, between steps).
+ * Arguments and results are those of ds_verify; `workspace` and
+ * `workspace_bytes` are ignored. The scratch is a file-scope device array of
+ * DS_VERIFY_STATIC_SCRATCH_BYTES bytes per device, allocated with the module:
+ *   - calls with ds_verify_workspace_bytes(B, K, V, r) above that size return
+ *     DS_ERR_WORKSPACE and launch nothing (B = 128, K = 16, V = 151936,
+ *     r = 256 needs about 11 MB and fits);
+ *   - the first call on a device (with that device current) looks up the
+ *     array's address once; make one call per device before any stream capture;
+ *   - calls whose executions overlap on the same device race on the array:
+ *     order them on one stream or with events;
+ *   - nothing in the array needs to start at zero.
+ */
+#define DS_VERIFY_STATIC_SCRATCH_BYTES (16u << 20)
+ds_status ds_verify_static(const ds_verify_args* args, ds_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status and identification                                                 */
 /* ------------------------------------------------------------------------ */

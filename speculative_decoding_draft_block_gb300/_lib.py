@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_UNSUPPORTED", 3:
 EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspace_bytes",
            "ds_draft_block", "ds_sched_workspace_bytes", "ds_confidence_schedule",
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
-           "ds_version", "ds_transpose_projection")
+           "ds_version", "ds_transpose_projection", "ds_verify_static")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -83,6 +83,8 @@ def load():
     lib.ds_draft_block.argtypes = [ctypes.POINTER(DraftArgs), _vp]
     lib.ds_confidence_schedule.argtypes = [ctypes.POINTER(SchedArgs), _vp]
     lib.ds_verify.argtypes = [ctypes.POINTER(VerifyArgs), _vp]
+    lib.ds_verify_static.argtypes = [ctypes.POINTER(VerifyArgs), _vp]
+    lib.ds_verify_static.restype = ctypes.c_int
     for f in ("ds_draft_block", "ds_confidence_schedule", "ds_verify"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ds_transpose_projection.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp]
@@ -230,6 +232,25 @@ def ds_transpose_projection(P, P_t, stream=None):
     r, V = P.shape
     return load().ds_transpose_projection(_ptr(P, "P"), r, V, _dtype_code(P), _ptr(P_t, "P_t"),
                                           _stream(stream))
+
+
+def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats,
+                     sched_len, temperature, seed, out_tokens, accept_count, num_emitted, status,
+                     stream=None, P_t=None):
+    """ds_verify with the library's static scratch (no workspace argument)."""
+    B, K1, V = target_logits.shape
+    a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
+                   target_logits=_ptr(target_logits, "target_logits"),
+                   base_logits=_ptr(base_logits, "base_logits"), E=_ptr(E, "E"), P=_ptr(P, "P"),
+                   P_t=None if P_t is None else _ptr(P_t, "P_t"),
+                   anchor=_ptr(anchor, "anchor"), draft_tokens=_ptr(draft_tokens, "draft_tokens"),
+                   q_token=_ptr(q_token, "q_token"), q_stats=_ptr(q_stats, "q_stats"),
+                   sched_len=_ptr(sched_len, "sched_len"), temperature=_ptr(temperature, "temperature"),
+                   seed=int(seed), out_tokens=_ptr(out_tokens, "out_tokens"),
+                   accept_count=_ptr(accept_count, "accept_count"),
+                   num_emitted=_ptr(num_emitted, "num_emitted"),
+                   workspace=None, workspace_bytes=0, status=_ptr(status, "status"))
+    return load().ds_verify_static(ctypes.byref(a), _stream(stream))
 
 
 def ds_check_status(status, stream=None):

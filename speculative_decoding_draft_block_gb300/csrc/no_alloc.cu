@@ -1,0 +1,78 @@
+// ds_verify_static: ds_verify with its scratch in a file-scope device array.
+//
+// Some callers cannot hand the library a workspace:
+//   * plain C hosts that embed the library without any device allocator of
+//     their own;
+//   * serving loops that must not allocate between steps, because
+//     cudaMalloc / cudaFree synchronise the device and stall the other
+//     streams.
+// For them this entry point takes the same arguments as ds_verify, ignores
+// `workspace` / `workspace_bytes`, and uses a statically allocated scratch
+// array of kScratchBytes bytes that lives as long as the loaded module. It
+// allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+//
+// Set-up: the first call on each device (with that device current) takes the
+// array's device address with cudaGetSymbolAddress and caches it per device.
+// Make one call on every device before capturing work into a CUDA graph, so
+// that the capture does not include the set-up query.
+//
+// Zero-initialisation: none is needed. ds_verify writes every scratch word it
+// reads within the same call (per-row results for rows 0..L_b, the final-draw
+// descriptors, the chunk and group records).
+//
+// Concurrency: there is one scratch array per device. Two calls on the same
+// device whose executions overlap (different streams, or different host
+// threads) race on it; the caller must order them (one stream, or events).
+//
+// Limit: calls whose ds_verify_workspace_bytes(B, K, V, r) exceeds
+// kScratchBytes return DS_ERR_WORKSPACE without launching anything.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace ds {
+namespace {
+
+constexpr size_t kScratchBytes = size_t(DS_VERIFY_STATIC_SCRATCH_BYTES);
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up once per device).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_verify_scratch);
+    if (e != cudaSuccess) return e;
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace ds
+
+extern "C" ds_status ds_verify_static(const ds_verify_args* a, ds_stream_t stream) {
+  if (a == nullptr) return DS_ERR_INVALID_ARG;
+  const size_t need = ds_verify_workspace_bytes(a->B, a->K, a->V, a->r);
+  if (need == 0) return DS_ERR_INVALID_ARG;
+  if (need > ds::kScratchBytes) return DS_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (ds::scratch_address(&scratch) != cudaSuccess) return DS_ERR_CUDA;
+  ds_verify_args b = *a;
+  b.workspace = scratch;
+  b.workspace_bytes = ds::kScratchBytes;
+  return ds_verify(&b, stream);
+}
