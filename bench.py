@@ -129,15 +129,20 @@ def gpu_launches_per_cycle(w):
 STEP_KEYS = ("base_logits", "target_logits", "anchor", "temperature", "h")
 
 
+# Sources of the draft-step kernels (tile + locate) and everything they include.
+STEP_SOURCES = ("draft_tc.cu", "sample.cu", "common.cuh", "fastpath.cuh", "sampling.cuh",
+                "sm100.cuh", "internal.h", "philox.h")
+
+
 def sources_digest():
-    """sha256 over the CUDA sources: ties recorded ncu traffic to the kernels it measured."""
+    """sha256 over the draft-step kernels' sources: ties recorded ncu traffic to
+    the kernels it measured."""
     import hashlib
     d = os.path.join(ROOT, "speculative_decoding_draft_block_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in STEP_SOURCES:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
 
 
