@@ -603,7 +603,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             group_merge(c.mode, g, *reinterpret_cast<const ChunkRec*>(xb + 16 * k));
           sp.supers[(size_t)row * sp.sup_stride + (blockIdx.x - first_group(sp, mt))] = g;
         }
-        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
+        // With two column groups the exchange line lies in the slot that only
+        // column group 0 releases, after these reads; more groups would share
+        // slots and need one more barrier here.
+        static_assert(kColGroups == 2, "the flush exchange assumes two column groups");
       }
       // this warp is done with the tile's accumulator and logit slots
       tc_fence_before();
