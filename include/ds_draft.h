@@ -67,7 +67,9 @@ enum { DS_STAGE_DRAFT = 0, DS_STAGE_ACCEPT = 1, DS_STAGE_RESAMPLE = 2 };
 enum {
   DS_SCHED_GREEDY_EARLYSTOP = 0, /* [DSpark] 신뢰도 기반 검증: global greedy + early stop */
   DS_SCHED_FIXED_K = 1,          /* verify every drafted token (scheduler off) */
-  DS_SCHED_THRESHOLD = 2         /* static survival threshold (the page's threshold sweep) */
+  DS_SCHED_THRESHOLD = 2,        /* static survival threshold (the page's threshold sweep) */
+  DS_SCHED_ASYNC = 3             /* [DSpark] 프로덕션 배포 결과: budget from two cycles back,
+                                    dynamic top-k on the current survivals */
 };
 
 /*
@@ -163,7 +165,14 @@ ds_status ds_transpose_projection(const void* P, int32_t r, int32_t V, int32_t d
  * iff J' = SPS(N+1) * (A + s) / (N+1) > J, and the walk stops at the first
  * candidate that is not taken. SPS(n) = sps[min(n, n_max) - 1].
  * FIXED_K: L_b = K. THRESHOLD: L_b = #{k : s_k >= threshold}.
- * The objective J is evaluated in double precision.
+ * ASYNC ([DSpark] 주요 결과 › 프로덕션 배포 결과, 한계와 주의사항): the number
+ * of drafted tokens to verify this cycle is M = budget_ring[cycle & 1], the
+ * GREEDY_EARLYSTOP count computed two cycles earlier (or the caller's initial
+ * value), so the verify batch B + min(M, B*K) is fixed before this cycle's
+ * confidences exist; the M candidates taken are the first M of the same sorted
+ * order on the current survivals (prefix-closed). The call then stores this
+ * cycle's GREEDY_EARLYSTOP count in budget_ring[cycle & 1] for cycle + 2.
+ * The objective J is evaluated in double-float arithmetic, stored as double.
  */
 typedef struct {
   int32_t B, K, d, r, V;
@@ -180,6 +189,8 @@ typedef struct {
   int32_t n_max;
   int32_t mode;               /* DS_SCHED_* */
   float threshold;            /* DS_SCHED_THRESHOLD only */
+  int32_t* budget_ring;       /* DS_SCHED_ASYNC only: [2] device words, read then overwritten */
+  int32_t cycle;              /* DS_SCHED_ASYNC only: the caller's cycle counter */
   float* conf;                /* out [B][K] c_k */
   float* survival;            /* out [B][K] s_k */
   int32_t* sched_len;         /* out [B]    L_b in [0, K] */

@@ -41,7 +41,8 @@ from .philox import philox4x32_10, uniform, STAGE_DRAFT, STAGE_ACCEPT, STAGE_RES
 from .sampling import inverse_cdf, argmax_first, softmax_weights
 from .draft import markov_logits, draft_block, draft_step
 from .confidence import confidence, survival
-from .schedule import schedule, sps_at, SCHED_GREEDY_EARLYSTOP, SCHED_FIXED_K, SCHED_THRESHOLD
+from .schedule import (schedule, sps_at, async_budgets, SCHED_GREEDY_EARLYSTOP, SCHED_FIXED_K,
+                       SCHED_THRESHOLD, SCHED_ASYNC)
 from .verify import verify, verify_request
 from .cycle import cycle
 from .bf16 import bf16_bits_to_f64
@@ -51,6 +52,7 @@ __all__ = [
     "inverse_cdf", "argmax_first", "softmax_weights",
     "markov_logits", "draft_block", "draft_step",
     "confidence", "survival",
-    "schedule", "sps_at", "SCHED_GREEDY_EARLYSTOP", "SCHED_FIXED_K", "SCHED_THRESHOLD",
+    "schedule", "sps_at", "async_budgets", "SCHED_GREEDY_EARLYSTOP", "SCHED_FIXED_K",
+    "SCHED_THRESHOLD", "SCHED_ASYNC",
     "verify", "verify_request", "cycle", "bf16_bits_to_f64",
 ]

@@ -17,6 +17,15 @@ Start at N = B, A = B. Walk candidates by survival descending, ties by
 position ascending then request ascending; include a candidate iff the new J is
 strictly larger than the current J, otherwise stop. SPS(n) beyond the table is
 the last entry.
+
+Asynchronous variant (same page, 주요 결과 › 프로덕션 배포 결과, and
+한계와 주의사항): the verify capacity of the coming cycle is estimated from the
+confidence head two cycles back, while the current cycle's candidates are
+ranked by their own (fresh) cumulative confidence, a dynamic top-k. Reading:
+the budget of cycle t is the greedy early-stop count of cycle t - 2 (an initial
+value for the first two cycles), and cycle t verifies the first budget-many
+candidates of its own sorted order. The budget never depends on cycle t's
+tokens, which is the causal barrier the page describes.
 """
 
 import numpy as np
@@ -24,6 +33,7 @@ import numpy as np
 SCHED_GREEDY_EARLYSTOP = 0
 SCHED_FIXED_K = 1
 SCHED_THRESHOLD = 2
+SCHED_ASYNC = 3
 
 
 def sps_at(sps, n):
@@ -34,7 +44,13 @@ def sps_at(sps, n):
     return float(sps[min(n, len(sps)) - 1])
 
 
-def schedule(s, sps, mode=SCHED_GREEDY_EARLYSTOP, threshold=0.0):
+def _sorted_candidates(s):
+    B, K = s.shape
+    return sorted(((b, k) for b in range(B) for k in range(K)),
+                  key=lambda bk: (-s[bk[0], bk[1]], bk[1], bk[0]))
+
+
+def schedule(s, sps, mode=SCHED_GREEDY_EARLYSTOP, threshold=0.0, budget=0):
     """Choose per-request verify lengths L [B] from survivals s [B, K].
 
     Returns a dict: L (int64 [B]), objective (J at the chosen set),
@@ -59,11 +75,23 @@ def schedule(s, sps, mode=SCHED_GREEDY_EARLYSTOP, threshold=0.0):
         a = B + sum(float(s[b, :L[b]].sum()) for b in range(B))
         return {"L": L, "objective": sps_at(sps, n) * a / n, "n_included": int(L.sum()),
                 "stop_rel_gain": np.inf, "survival_gap": np.inf}
+    if mode == SCHED_ASYNC:
+        # dynamic top-k: the first `budget` candidates of the current order
+        greedy_count = schedule(s, sps)["n_included"]
+        m = min(max(int(budget), 0), B * K)
+        a = float(B)
+        for b, k in _sorted_candidates(s)[:m]:
+            if L[b] != k:
+                raise AssertionError("selection is not prefix-closed")
+            L[b] += 1
+            a += s[b, k]
+        n = B + m
+        return {"L": L, "objective": sps_at(sps, n) * a / n, "n_included": m,
+                "greedy_count": greedy_count, "stop_rel_gain": np.inf, "survival_gap": np.inf}
     if mode != SCHED_GREEDY_EARLYSTOP:
         raise ValueError("unknown schedule mode")
 
-    order = sorted(((b, k) for b in range(B) for k in range(K)),
-                   key=lambda bk: (-s[bk[0], bk[1]], bk[1], bk[0]))
+    order = _sorted_candidates(s)
     n, a = B, float(B)
     j = sps_at(sps, n) * a / n
     stop_rel_gain = np.inf
@@ -85,3 +113,9 @@ def schedule(s, sps, mode=SCHED_GREEDY_EARLYSTOP, threshold=0.0):
             break
     return {"L": L, "objective": j, "n_included": int(L.sum()),
             "stop_rel_gain": float(stop_rel_gain), "survival_gap": float(survival_gap)}
+
+
+def async_budgets(greedy_counts, initial):
+    """Budgets of cycles 0, 1, 2, ... under the asynchronous scheduler: the
+    first two cycles use `initial`, cycle t >= 2 uses the greedy count of t - 2."""
+    return [initial if t < 2 else int(greedy_counts[t - 2]) for t in range(len(greedy_counts))]

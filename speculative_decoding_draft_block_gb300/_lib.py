@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libdsdraft.so")
 DS_OK = 0
 DS_F32, DS_BF16 = 0, 1
 DS_STAGE_DRAFT, DS_STAGE_ACCEPT, DS_STAGE_RESAMPLE = 0, 1, 2
-DS_SCHED_GREEDY_EARLYSTOP, DS_SCHED_FIXED_K, DS_SCHED_THRESHOLD = 0, 1, 2
+DS_SCHED_GREEDY_EARLYSTOP, DS_SCHED_FIXED_K, DS_SCHED_THRESHOLD, DS_SCHED_ASYNC = 0, 1, 2, 3
 STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_UNSUPPORTED", 3: "DS_ERR_WORKSPACE",
                 4: "DS_ERR_CUDA", 5: "DS_ERR_TIMEOUT", 6: "DS_ERR_BOUNDS", 7: "DS_ERR_NONFINITE"}
 
@@ -44,6 +44,7 @@ class SchedArgs(ctypes.Structure):
                 ("h", _vp), ("E", _vp), ("anchor", _vp), ("draft_tokens", _vp), ("w_h", _vp),
                 ("w_e", _vp), ("bias", ctypes.c_float), ("sts_temp", _vp), ("sps", _vp),
                 ("n_max", _i32), ("mode", _i32), ("threshold", ctypes.c_float),
+                ("budget_ring", _vp), ("cycle", _i32),
                 ("conf", _vp), ("survival", _vp), ("sched_len", _vp), ("objective", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
 
@@ -191,14 +192,16 @@ def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q
 
 def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp, sps, mode,
                            conf, survival, sched_len, objective, status, threshold=0.0,
-                           workspace=None, stream=None):
+                           workspace=None, stream=None, budget_ring=None, cycle=0):
     B, K, d = h.shape
     a = SchedArgs(B=B, K=K, d=d, r=E.shape[1], V=E.shape[0], dtype=_dtype_code(h),
                   h=_ptr(h, "h"), E=_ptr(E, "E"), anchor=_ptr(anchor, "anchor"),
                   draft_tokens=_ptr(draft_tokens, "draft_tokens"), w_h=_ptr(w_h, "w_h"),
                   w_e=_ptr(w_e, "w_e"), bias=float(bias), sts_temp=_ptr(sts_temp, "sts_temp"),
                   sps=_ptr(sps, "sps"), n_max=int(sps.shape[0]), mode=int(mode),
-                  threshold=float(threshold), conf=_ptr(conf, "conf"),
+                  threshold=float(threshold),
+                  budget_ring=None if budget_ring is None else _ptr(budget_ring, "budget_ring"),
+                  cycle=int(cycle), conf=_ptr(conf, "conf"),
                   survival=_ptr(survival, "survival"), sched_len=_ptr(sched_len, "sched_len"),
                   objective=_ptr(objective, "objective"),
                   workspace=_ptr(workspace, "workspace") if workspace is not None else None,

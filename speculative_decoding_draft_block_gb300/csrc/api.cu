@@ -204,7 +204,9 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
   if (a->dtype != DS_F32 && a->dtype != DS_BF16) return DS_ERR_INVALID_ARG;
   if (a->n_max < 1) return DS_ERR_INVALID_ARG;
   if (a->mode != DS_SCHED_GREEDY_EARLYSTOP && a->mode != DS_SCHED_FIXED_K &&
-      a->mode != DS_SCHED_THRESHOLD)
+      a->mode != DS_SCHED_THRESHOLD && a->mode != DS_SCHED_ASYNC)
+    return DS_ERR_INVALID_ARG;
+  if (a->mode == DS_SCHED_ASYNC && (a->budget_ring == nullptr || (uintptr_t)a->budget_ring % 8 != 0))
     return DS_ERR_INVALID_ARG;
   const void* ptrs[] = {a->h, a->E, a->anchor, a->draft_tokens, a->w_h, a->w_e, a->sts_temp,
                         a->sps, a->conf, a->survival, a->sched_len, a->objective, a->status};
@@ -224,6 +226,8 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
   p.mode = a->mode;
   p.bias = a->bias;
   p.threshold = a->threshold;
+  p.budget_ring = a->budget_ring;
+  p.cycle = a->cycle;
   p.h = a->h;
   p.E = a->E;
   p.anchor = a->anchor;

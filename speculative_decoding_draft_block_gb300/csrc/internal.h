@@ -102,6 +102,8 @@ struct VerifyParams {
 struct SchedParams {
   int32_t B, K, d, r, V, dtype, n_max, mode;
   float bias, threshold;
+  int32_t* budget_ring;  // DS_SCHED_ASYNC: [2]
+  int32_t cycle;
   const void* h;
   const void* E;
   const int32_t* anchor;

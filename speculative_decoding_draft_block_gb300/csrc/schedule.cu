@@ -1,5 +1,10 @@
 // Confidence head, survival and the hardware-aware prefix scheduler.
 //
+// Asynchronous variant (DSpark summary page, 주요 결과 › 프로덕션 배포 결과):
+// the verify budget of cycle t is the early-stop count of cycle t - 2, kept in
+// a two-word device ring, and the candidates taken are the first budget-many
+// of cycle t's own sorted order.
+//
 // DSpark summary page, 방법론 › 신뢰도 기반 검증:
 //   c_k = sigmoid((w_h . h_k + w_e . E[x_{k-1}] + b) / T_k)   (STS temperature T_k)
 //   s_k = c_1 * ... * c_k                                      (prefix survival)
@@ -110,8 +115,11 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   extern __shared__ unsigned long long keys[];
   __shared__ DF wsum[32];
   __shared__ int red[32];
+  __shared__ int s_budget;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int B = p.B, K = p.K, n = B * K;
+  // asynchronous mode: this cycle's budget, written two cycles ago
+  if (tid == 0) s_budget = (p.mode == DS_SCHED_ASYNC) ? p.budget_ring[p.cycle & 1] : 0;
 
   // survival (sequential over k per request, fp32)
   for (int b = tid; b < B; b += kSchedThreads) {
@@ -125,7 +133,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
     p.sched_len[b] = (p.mode == DS_SCHED_FIXED_K) ? K : (p.mode == DS_SCHED_THRESHOLD ? L : 0);
   }
   __syncthreads();
-  if (p.mode != DS_SCHED_GREEDY_EARLYSTOP) {
+  if (p.mode != DS_SCHED_GREEDY_EARLYSTOP && p.mode != DS_SCHED_ASYNC) {
     // objective of the fixed selection: block sums of N and A (double-float)
     int nsum = 0;
     DF a = {0.f, 0.f};
@@ -229,6 +237,12 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   int M = red[0];
   for (int w = 1; w < kSchedThreads / 32; ++w) M = min(M, red[w]);
   if (M == INT_MAX) M = n;
+  if (p.mode == DS_SCHED_ASYNC) {
+    // dynamic top-k: take the budget's worth of the current order; store this
+    // cycle's early-stop count as the budget of cycle + 2
+    if (tid == 0) p.budget_ring[p.cycle & 1] = M;
+    M = min(max(s_budget, 0), n);
+  }
 
   for (int i = tid; i < M; i += kSchedThreads) {
     const unsigned long long key = keys[i];

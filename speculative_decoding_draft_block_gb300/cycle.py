@@ -35,7 +35,7 @@ INPUT_KEYS = ("base_logits", "target_logits", "E", "P", "anchor", "temperature",
 
 class DeviceCycle:
     def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0,
-                 token_major_projection=True):
+                 token_major_projection=True, initial_budget=None):
         self.inp = inp
         self.device = torch.device(device)
         self.mode = mode
@@ -59,6 +59,12 @@ class DeviceCycle:
         self.accept_count = torch.zeros((B,), **i32)
         self.num_emitted = torch.zeros((B,), **i32)
         self.status = torch.zeros((4,), **i32)
+        # asynchronous scheduler: budgets of the next two cycles (device ring)
+        # and the cycle counter; the first two cycles use initial_budget
+        if initial_budget is None:
+            initial_budget = B * K // 2
+        self.budget_ring = torch.full((2,), int(initial_budget), **i32)
+        self.sched_cycle = 0
         wd = _lib.ds_draft_workspace_bytes(B, K, V, r)
         wv = _lib.ds_verify_workspace_bytes(B, K, V, r)
         if wd == 0 or wv == 0:
@@ -85,7 +91,9 @@ class DeviceCycle:
                                           t["w_e"], self.conf_bias, t["sts_temp"], t["sps"],
                                           self.mode, self.conf, self.survival, self.sched_len,
                                           self.objective, self.status, threshold=self.threshold,
-                                          stream=stream), "ds_confidence_schedule")
+                                          stream=stream, budget_ring=self.budget_ring,
+                                          cycle=self.sched_cycle), "ds_confidence_schedule")
+        self.sched_cycle += 1
 
     def verify(self, seed, stream=None):
         t = self.t

@@ -170,6 +170,44 @@ def test_schedule_modes(ds):
     _parity.assert_parity(inp, g, SEED, check_schedule=False)
 
 
+def test_async_scheduler_over_cycles(ds):
+    """Budget from two cycles back (device ring), dynamic top-k on the current
+    survivals; each cycle compared with the oracle's asynchronous schedule."""
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
+    import oracle
+    inp = _ragged(True, (1.0, 0.6), 23, B=24, K=6, V=2048, r=64, d=128)
+    B, K = inp["B"], inp["K"]
+    cyc = DeviceCycle(inp, mode=_lib.DS_SCHED_ASYNC, initial_budget=17)
+    counts, near = [], []
+    for t in range(5):
+        budget = int(cyc.budget_ring.cpu()[t & 1])       # what the device will use
+        want_budget = 17 if t < 2 else counts[t - 2]
+        assert budget == want_budget or near[t - 2]
+        cyc.reset_status()
+        cyc.run(SEED + t)
+        cyc.check_status()
+        g = cyc.results()
+        s = oracle.survival(oracle.confidence(inp["h"], inp["E"], inp["anchor"], g["tokens"],
+                                              inp["w_h"], inp["w_e"], inp["conf_bias"],
+                                              inp["sts_temp"]))
+        greedy = oracle.schedule(s, inp["sps"])
+        counts.append(greedy["n_included"])
+        near.append(min(greedy["stop_rel_gain"], greedy["survival_gap"]) < _parity.SCHED_NEAR_TIE)
+        want = oracle.schedule(s, inp["sps"], mode=oracle.SCHED_ASYNC, budget=budget)
+        assert int(g["L"].sum()) == min(budget, B * K)        # fixed verify batch
+        top = np.sort(s.ravel())[::-1]
+        m = min(budget, B * K)
+        boundary_tie = 0 < m < B * K and (top[m - 1] - top[m]) <= _parity.SCHED_NEAR_TIE * top[m - 1]
+        if not boundary_tie:
+            assert np.array_equal(g["L"], want["L"])
+            assert abs(g["objective"] - want["objective"]) <= 1e-5 * want["objective"]
+        _parity.assert_parity(inp, g, SEED + t, check_schedule=False)
+    # the ring holds the last two cycles' early-stop counts
+    ring = sorted(cyc.budget_ring.cpu().numpy().tolist())
+    assert ring == sorted(counts[-2:]) or near[-1] or near[-2]
+
+
 def test_minimal_shapes(ds):
     inp = _ragged(True, (1.0,), 19, B=1, K=1, V=8, r=16, d=8)
     _, g = _run(inp)

@@ -113,3 +113,79 @@ def test_global_search_would_anticipate():
     hi = np.array([[0.5, 0.45]])
     assert glob(lo) == 0 and glob(hi) == 2           # min(L, 1) flips with s_2
     assert schedule(lo, sps)["n_included"] == schedule(hi, sps)["n_included"] == 0
+
+
+# ---- asynchronous scheduler (budget from two cycles back, dynamic top-k) -----
+
+def _hyper_sps(B, K):
+    n = np.arange(1, B * (K + 1) + 1)
+    return n * 9e4 / (1.0 + n / 96.0)
+
+
+def test_async_with_its_own_greedy_count_is_the_greedy_schedule():
+    from oracle import SCHED_ASYNC
+    rng = np.random.default_rng(11)
+    for B, K in ((3, 4), (8, 5), (16, 8)):
+        sps = _hyper_sps(B, K)
+        for _ in range(10):
+            s = _random_s(rng, B, K)
+            g = schedule(s, sps)
+            a = schedule(s, sps, SCHED_ASYNC, budget=g["n_included"])
+            assert np.array_equal(a["L"], g["L"])
+            assert abs(a["objective"] - g["objective"]) <= 1e-12 * g["objective"]
+            assert a["greedy_count"] == g["n_included"]
+
+
+def test_async_budget_edges_and_fixed_shape():
+    from oracle import SCHED_ASYNC
+    rng = np.random.default_rng(12)
+    B, K = 5, 4
+    sps = _hyper_sps(B, K)
+    s = _random_s(rng, B, K)
+    for budget in (-3, 0):
+        r = schedule(s, sps, SCHED_ASYNC, budget=budget)
+        assert (r["L"] == 0).all() and r["objective"] == sps_at(sps, B)
+    for budget in (B * K, B * K + 7):
+        assert (schedule(s, sps, SCHED_ASYNC, budget=budget)["L"] == K).all()
+    for budget in range(B * K + 1):
+        r = schedule(s, sps, SCHED_ASYNC, budget=budget)
+        assert int(r["L"].sum()) == budget          # the verify batch is fixed in advance
+        assert abs(r["objective"] - _J(sps, B, r["L"], s)) <= 1e-12 * r["objective"]
+
+
+def test_async_top_k_is_the_best_prefix_closed_set_of_its_size():
+    """Brute force: for every budget m, the selection maximises the summed
+    survival over all prefix-closed selections with m candidates."""
+    from oracle import SCHED_ASYNC
+    rng = np.random.default_rng(13)
+    B, K = 3, 3
+    sps = _hyper_sps(B, K)
+    for _ in range(20):
+        s = _random_s(rng, B, K)
+        best = {}
+        for L in itertools.product(range(K + 1), repeat=B):
+            tot = sum(float(s[b, :L[b]].sum()) for b in range(B))
+            best[sum(L)] = max(best.get(sum(L), -1.0), tot)
+        for m, v in best.items():
+            L = schedule(s, sps, SCHED_ASYNC, budget=m)["L"]
+            got = sum(float(s[b, :L[b]].sum()) for b in range(B))
+            assert abs(got - v) < 1e-12
+
+
+def test_async_budget_never_sees_the_current_cycle():
+    """Causal barrier: changing cycle t's survivals leaves the budgets of
+    cycles 0..t+1 unchanged (only cycle t+2 may follow it)."""
+    from oracle import async_budgets
+    rng = np.random.default_rng(14)
+    B, K, T = 6, 5, 7
+    sps = _hyper_sps(B, K)
+    cycles = [_random_s(rng, B, K) for _ in range(T)]
+    counts = [schedule(s, sps)["n_included"] for s in cycles]
+    base = async_budgets(counts, initial=9)
+    assert base[:2] == [9, 9] and base[2:] == counts[:T - 2]
+    for t in range(T):
+        pert = list(cycles)
+        pert[t] = _random_s(rng, B, K) ** 3
+        c2 = [schedule(s, sps)["n_included"] for s in pert]
+        b2 = async_budgets(c2, initial=9)
+        assert b2[:t + 2] == base[:t + 2]
