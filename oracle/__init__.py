@@ -34,6 +34,10 @@ Parity status per function (see the pins in tests/test_oracle_*.py):
   verify ........................ pinned (acceptance = 1 - TV(p, q) by exact
                                   integration over u; V=8, K=3 losslessness by
                                   exhaustive enumeration)
+  sts_fit, ece .................. pinned (hand-binned ECE values, one-bin closed
+                                  form, exact recovery of the true temperatures
+                                  with zero ECE, prefix and causality
+                                  metamorphic tests, first-index ties)
   cycle ......................... composition of the above
 """
 
@@ -46,6 +50,7 @@ from .schedule import (schedule, sps_at, async_budgets, SCHED_GREEDY_EARLYSTOP, 
 from .verify import verify, verify_request
 from .cycle import cycle
 from .bf16 import bf16_bits_to_f64
+from .sts import sts_fit, sts_curves, ece
 
 __all__ = [
     "philox4x32_10", "uniform", "STAGE_DRAFT", "STAGE_ACCEPT", "STAGE_RESAMPLE",
@@ -55,4 +60,5 @@ __all__ = [
     "schedule", "sps_at", "async_budgets", "SCHED_GREEDY_EARLYSTOP", "SCHED_FIXED_K",
     "SCHED_THRESHOLD", "SCHED_ASYNC",
     "verify", "verify_request", "cycle", "bf16_bits_to_f64",
+    "sts_fit", "sts_curves", "ece",
 ]

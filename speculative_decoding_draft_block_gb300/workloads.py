@@ -181,3 +181,29 @@ def make_inputs(w, seed=None, threads=None):
         "conf_bias": float(w.conf_bias), "sts_temp": sts,
         "sps": _sps_table(w.sps_kind, w.sps_nmax), "true_tokens": true_tok, "sigma_b": sigma_b,
     }
+
+
+def make_sts_inputs(N, K, seed=7, t_true=(1.2, 2.5), noise=0.25):
+    """Synthetic calibration set for the STS fit (float32, deterministic in the seed).
+
+    Raw confidence logits a[n, k] ~ N(2 - 0.1 k, 1.5^2). The soft per-step
+    acceptance labels follow a logistic law in a / T_true[k] with N(0, noise^2)
+    jitter, T_true[k] ~ U[t_true]: with T_true > 1 the raw confidences are
+    over-confident, the situation the calibration exists to correct.
+    """
+    ss = np.random.SeedSequence(seed)
+    rng = np.random.Generator(np.random.PCG64(ss))
+    k = np.arange(K, dtype=np.float32)
+    a = (2.0 - 0.1 * k)[None, :] + rng.standard_normal((N, K), dtype=np.float32) * np.float32(1.5)
+    lo, hi = t_true
+    T = rng.uniform(lo, hi, size=K).astype(np.float32)
+    jitter = rng.standard_normal((N, K), dtype=np.float32) * np.float32(noise)
+    x = (a / T[None, :] + jitter).astype(np.float64)
+    y = np.where(x >= 0, 1.0 / (1.0 + np.exp(-np.abs(x))), np.exp(-np.abs(x)) / (1.0 + np.exp(-np.abs(x))))
+    return {"logits": np.ascontiguousarray(a, dtype=np.float32),
+            "labels": np.ascontiguousarray(y, dtype=np.float32), "t_true": T}
+
+
+def sts_grid(lo=0.05, hi=5.0, n=256):
+    """Candidate STS temperatures: n log-spaced float32 values in [lo, hi]."""
+    return np.geomspace(lo, hi, n).astype(np.float32)
