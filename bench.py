@@ -270,6 +270,116 @@ def run_reference(args, rank, ws):
     print(json.dumps(line), flush=True)
 
 
+STS_METRIC = "STS fit: calibration sample-positions/s (N=65536, K=16, 256-point grid, 15 bins)"
+STS_N, STS_K, STS_G, STS_BINS = 65536, 16, 256, 15
+MUFU_PER_CLK_SM = 16       # exp2 / reciprocal issue rate per SM per clock
+MUFU_PER_EVAL = 2          # one exp2 and one reciprocal per sigmoid
+
+
+def run_sts(args, rank, ws, local):
+    """Time ds_sts_fit (all K positions, both kernels) on the synthetic calibration set."""
+    import numpy as np
+    import torch
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.workloads import make_sts_inputs, sts_grid
+
+    if not os.path.exists(_lib.LIB_PATH):
+        from speculative_decoding_draft_block_gb300 import build
+        build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    d = make_sts_inputs(STS_N, STS_K, seed=7 + rank)
+    grid_h = sts_grid(0.05, 5.0, STS_G)
+    a = torch.from_numpy(d["logits"]).to(dev)
+    y = torch.from_numpy(d["labels"]).to(dev)
+    grid = torch.from_numpy(grid_h).to(dev)
+    T = torch.empty((STS_K,), dtype=torch.float32, device=dev)
+    idx = torch.empty((STS_K,), dtype=torch.int32, device=dev)
+    ece = torch.empty((STS_K,), dtype=torch.float32, device=dev)
+    wsb = torch.empty((_lib.ds_sts_workspace_bytes(STS_N, STS_K, STS_G, STS_BINS),), dtype=torch.uint8,
+                      device=dev)
+    status = torch.zeros((4,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def fit():
+        _lib.check(_lib.ds_sts_fit(a, y, grid, STS_BINS, T, idx, ece, wsb, status), "ds_sts_fit")
+
+    for _ in range(args.warmup):
+        fit()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local)
+    with sampler:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fit()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(ws)
+    _lib.check(_lib.ds_check_status(status), "device status")
+    ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
+    total_s = reduce_max(float(ms.sum()) / 1e3, ws)
+    units = STS_N * STS_K
+    value = ws * units * K / total_s
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fmax = (sampler.max_mhz or 2070) * 1e6
+    peak = sms * MUFU_PER_CLK_SM * fmax / MUFU_PER_EVAL / 1e12          # T evaluations / s
+    evals = STS_N * STS_K * STS_G
+    achieved = evals / (float(ms.mean()) * 1e-3) / 1e12
+    line = {
+        "metric": STS_METRIC, "value": value, "unit": "sample-positions/s", "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": float(ms.mean()),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded logistic calibration set, over-confident raw head)",
+        "config": {"workload": "sts_N%d_K%d_G%d_bins%d" % (STS_N, STS_K, STS_G, STS_BINS),
+                   "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "T sigmoid evals/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "whole ds_sts_fit call (sts_hist_kernel + sts_reduce_kernel, K each)",
+                     "peak_source": "derived: SMs x %d MUFU/clk / %d MUFU per evaluation x max SM clock"
+                                    % (MUFU_PER_CLK_SM, MUFU_PER_EVAL)},
+        "gpu_launches": K * 2 * STS_K,
+        "fitted_temps": [float(x) for x in T.cpu().numpy()],
+        "ece": [float(x) for x in ece.cpu().numpy()],
+        "clocks": sampler.summary(),
+    }
+    # end to end: logits and labels copied from pinned host memory, temperatures copied back
+    ha = torch.from_numpy(d["logits"]).pin_memory()
+    hy = torch.from_numpy(d["labels"]).pin_memory()
+    hT = torch.empty((STS_K,), dtype=torch.float32).pin_memory()
+    E = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        a.copy_(ha, non_blocking=True)
+        y.copy_(hy, non_blocking=True)
+        fit()
+        hT.copy_(T, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws)
+    line["e2e"] = {"value": ws * units * E / e2e_s, "unit": "sample-positions/s",
+                   "h2d_bytes_per_step": int(ha.numel() * 4 + hy.numel() * 4),
+                   "d2h_bytes_per_step": int(hT.numel() * 4), "steps": E}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = 8192
+        t0 = time.perf_counter()
+        oracle.sts_fit(d["logits"][:n], d["labels"][:n], grid_h.astype(np.float64), STS_BINS)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n * STS_K / dt, "unit": "sample-positions/s",
+                                "cores": 1, "kind": "oracle",
+                                "sample": "first %d of %d samples, all %d positions and %d grid points"
+                                          % (n, STS_N, STS_K, STS_G)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -281,12 +391,20 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--part", choices=("cycle", "sts"), default="cycle",
+                    help="cycle: draft+schedule+verify (default); sts: the STS calibration fit")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank, ws, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, ws)
+        return
+    if args.part == "sts":
+        run_sts(args, rank, ws, local)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
 
     import numpy as np

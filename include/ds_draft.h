@@ -192,6 +192,8 @@ typedef struct {
   int32_t* budget_ring;       /* DS_SCHED_ASYNC only: [2] device words, read then overwritten */
   int32_t cycle;              /* DS_SCHED_ASYNC only: the caller's cycle counter */
   float* conf;                /* out [B][K] c_k */
+  float* conf_logit;          /* out [B][K] raw logit w_h.h_k + w_e.E[x_{k-1}] + b (before the
+                                 temperature), the input of ds_sts_fit; may be NULL */
   float* survival;            /* out [B][K] s_k */
   int32_t* sched_len;         /* out [B]    L_b in [0, K] */
   double* objective;          /* out [1]    J at the chosen lengths */
@@ -202,6 +204,47 @@ typedef struct {
 
 size_t ds_sched_workspace_bytes(int32_t B, int32_t K);
 ds_status ds_confidence_schedule(const ds_sched_args* args, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* STS calibration fit                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [DSpark] 방법론 › 신뢰도 기반 검증 (Sequential Temperature Scaling) and
+ * 주요 결과 (over-confident raw head; ECE lowered by STS). Fits the per-position
+ * temperatures sts_temp used by ds_confidence_schedule, left to right, on a
+ * calibration set of N samples. For k = 1..K, with T_1..T_{k-1} already fitted:
+ *     pred_n(T) = prod_{j<k} sigmoid(a_nj / T_j) * sigmoid(a_nk / T)
+ *     lab_n     = prod_{j<=k} y_nj
+ *     ECE(T)    = sum over n_bins equal-width bins of [0, 1] (bin = floor(pred * n_bins),
+ *                 clamped to the last) of |sum_{n in bin} (lab_n - pred_n)| / N
+ *     T_k       = the first grid point with the smallest ECE.
+ * a_nk is the raw confidence logit w_h . h_k + w_e . E[x_{k-1}] + b (before
+ * the temperature; ds_confidence_schedule returns it in conf_logit) and y_nk
+ * in [0, 1] the soft per-step acceptance label (the pages train on the
+ * analytic rate 1 - TV(p_k, q_k)). Arithmetic: float32 with double-float
+ * reductions, deterministic (no atomically accumulated sums).
+ * Limits: 1 <= N <= 2^26, 1 <= K <= 64, 1 <= n_grid <= 4096, 1 <= n_bins <= 64.
+ * Device-side errors: a non-finite logit -> DS_ERR_NONFINITE; a label outside
+ * [0, 1] or a grid value that is not a positive finite number -> DS_ERR_INVALID_ARG.
+ */
+typedef struct {
+  int32_t N, K;               /* calibration samples, positions */
+  int32_t n_grid, n_bins;
+  const float* logits;        /* [N][K] raw confidence logits a */
+  const float* labels;        /* [N][K] soft per-step labels y */
+  const float* grid;          /* [n_grid] candidate temperatures */
+  float* sts_temp;            /* out [K] fitted T_k (a grid value) */
+  int32_t* grid_index;        /* out [K] index of T_k in grid */
+  float* ece;                 /* out [K] ECE at T_k */
+  float* ece_curve;           /* out [K][n_grid] ECE at every grid point; may be NULL */
+  void* workspace;            /* ds_sts_workspace_bytes(N, K, n_grid, n_bins) bytes */
+  size_t workspace_bytes;
+  int32_t* status;
+} ds_sts_args;
+
+size_t ds_sts_workspace_bytes(int32_t N, int32_t K, int32_t n_grid, int32_t n_bins);
+ds_status ds_sts_fit(const ds_sts_args* args, ds_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Lossless verification                                                     */

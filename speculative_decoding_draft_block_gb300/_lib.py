@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_UNSUPPORTED", 3:
 EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspace_bytes",
            "ds_draft_block", "ds_sched_workspace_bytes", "ds_confidence_schedule",
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
-           "ds_version", "ds_transpose_projection", "ds_verify_static")
+           "ds_version", "ds_transpose_projection", "ds_verify_static", "ds_sts_workspace_bytes",
+           "ds_sts_fit")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -45,7 +46,15 @@ class SchedArgs(ctypes.Structure):
                 ("w_e", _vp), ("bias", ctypes.c_float), ("sts_temp", _vp), ("sps", _vp),
                 ("n_max", _i32), ("mode", _i32), ("threshold", ctypes.c_float),
                 ("budget_ring", _vp), ("cycle", _i32),
-                ("conf", _vp), ("survival", _vp), ("sched_len", _vp), ("objective", _vp),
+                ("conf", _vp), ("conf_logit", _vp), ("survival", _vp), ("sched_len", _vp),
+                ("objective", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
+
+
+class StsArgs(ctypes.Structure):
+    _fields_ = [("N", _i32), ("K", _i32), ("n_grid", _i32), ("n_bins", _i32),
+                ("logits", _vp), ("labels", _vp), ("grid", _vp), ("sts_temp", _vp),
+                ("grid_index", _vp), ("ece", _vp), ("ece_curve", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
 
 
@@ -88,6 +97,10 @@ def load():
     lib.ds_verify_static.restype = ctypes.c_int
     for f in ("ds_draft_block", "ds_confidence_schedule", "ds_verify"):
         getattr(lib, f).restype = ctypes.c_int
+    lib.ds_sts_workspace_bytes.argtypes = [_i32] * 4
+    lib.ds_sts_workspace_bytes.restype = ctypes.c_size_t
+    lib.ds_sts_fit.argtypes = [ctypes.POINTER(StsArgs), _vp]
+    lib.ds_sts_fit.restype = ctypes.c_int
     lib.ds_transpose_projection.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp]
     lib.ds_transpose_projection.restype = ctypes.c_int
     lib.ds_check_status.argtypes = [_vp, _vp]
@@ -192,7 +205,8 @@ def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q
 
 def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp, sps, mode,
                            conf, survival, sched_len, objective, status, threshold=0.0,
-                           workspace=None, stream=None, budget_ring=None, cycle=0):
+                           workspace=None, stream=None, budget_ring=None, cycle=0,
+                           conf_logit=None):
     B, K, d = h.shape
     a = SchedArgs(B=B, K=K, d=d, r=E.shape[1], V=E.shape[0], dtype=_dtype_code(h),
                   h=_ptr(h, "h"), E=_ptr(E, "E"), anchor=_ptr(anchor, "anchor"),
@@ -202,6 +216,7 @@ def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp,
                   threshold=float(threshold),
                   budget_ring=None if budget_ring is None else _ptr(budget_ring, "budget_ring"),
                   cycle=int(cycle), conf=_ptr(conf, "conf"),
+                  conf_logit=None if conf_logit is None else _ptr(conf_logit, "conf_logit"),
                   survival=_ptr(survival, "survival"), sched_len=_ptr(sched_len, "sched_len"),
                   objective=_ptr(objective, "objective"),
                   workspace=_ptr(workspace, "workspace") if workspace is not None else None,
@@ -254,6 +269,28 @@ def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_t
                    num_emitted=_ptr(num_emitted, "num_emitted"),
                    workspace=None, workspace_bytes=0, status=_ptr(status, "status"))
     return load().ds_verify_static(ctypes.byref(a), _stream(stream))
+
+
+def ds_sts_workspace_bytes(N, K, n_grid, n_bins):
+    return load().ds_sts_workspace_bytes(N, K, n_grid, n_bins)
+
+
+def ds_sts_fit(logits, labels, grid, n_bins, sts_temp, grid_index, ece, workspace, status,
+               ece_curve=None, stream=None):
+    """Left-to-right STS temperature fit (float32 logits and labels [N, K], grid [G])."""
+    for t, name in ((logits, "logits"), (labels, "labels"), (grid, "grid")):
+        if t.dtype != torch.float32:
+            raise TypeError("%s must be float32" % name)
+    N, K = logits.shape
+    a = StsArgs(N=N, K=K, n_grid=int(grid.shape[0]), n_bins=int(n_bins),
+                logits=_ptr(logits, "logits"), labels=_ptr(labels, "labels"),
+                grid=_ptr(grid, "grid"), sts_temp=_ptr(sts_temp, "sts_temp"),
+                grid_index=_ptr(grid_index, "grid_index"), ece=_ptr(ece, "ece"),
+                ece_curve=None if ece_curve is None else _ptr(ece_curve, "ece_curve"),
+                workspace=_ptr(workspace, "workspace"),
+                workspace_bytes=workspace.numel() * workspace.element_size(),
+                status=_ptr(status, "status"))
+    return load().ds_sts_fit(ctypes.byref(a), _stream(stream))
 
 
 def ds_check_status(status, stream=None):

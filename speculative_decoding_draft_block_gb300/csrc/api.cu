@@ -90,6 +90,35 @@ VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
   return l;
 }
 
+// STS fit workspace: ticket, prefix buffers, per-chunk histograms, bin sums, ECE curve.
+struct StsLayout {
+  size_t ticket, base, lab, part, binsum, ece_all, total;
+};
+
+bool sts_shape_ok(int32_t N, int32_t K, int32_t G, int32_t n_bins) {
+  return N >= 1 && N <= (1 << 26) && K >= 1 && K <= 64 && G >= 1 && G <= 4096 && n_bins >= 1 &&
+         n_bins <= 64;
+}
+
+StsLayout sts_layout(int32_t N, int32_t G, int32_t n_bins) {
+  StsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) & ~size_t(255);
+    return at;
+  };
+  const size_t chunks = (size_t)sts_num_chunks(N);
+  L.ticket = take(sizeof(unsigned));
+  L.base = take(sizeof(float) * 2 * (size_t)N);
+  L.lab = take(sizeof(float) * 2 * (size_t)N);
+  L.part = take(sizeof(float) * chunks * n_bins * G);
+  L.binsum = take(sizeof(float) * (size_t)n_bins * G);
+  L.ece_all = take(sizeof(float) * (size_t)G);
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -212,6 +241,7 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
                         a->sps, a->conf, a->survival, a->sched_len, a->objective, a->status};
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
+  if (a->conf_logit != nullptr && !aligned16(a->conf_logit)) return DS_ERR_INVALID_ARG;
   const ds_status st = device_supported();
   if (st != DS_OK) return st;
   SchedParams p;
@@ -237,6 +267,7 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
   p.sts_temp = a->sts_temp;
   p.sps = a->sps;
   p.conf = a->conf;
+  p.conf_logit = a->conf_logit;
   p.survival = a->survival;
   p.sched_len = a->sched_len;
   p.objective = a->objective;
@@ -244,6 +275,51 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
   const cudaStream_t s = (cudaStream_t)stream;
   if (launch_confidence(p, s) != cudaSuccess) return DS_ERR_CUDA;
   if (launch_schedule(p, s) != cudaSuccess) return DS_ERR_CUDA;
+  return DS_OK;
+}
+
+size_t ds_sts_workspace_bytes(int32_t N, int32_t K, int32_t n_grid, int32_t n_bins) {
+  if (!sts_shape_ok(N, K, n_grid, n_bins)) return 0;
+  return sts_layout(N, n_grid, n_bins).total;
+}
+
+ds_status ds_sts_fit(const ds_sts_args* a, ds_stream_t stream) {
+  if (a == nullptr) return DS_ERR_INVALID_ARG;
+  if (!sts_shape_ok(a->N, a->K, a->n_grid, a->n_bins)) return DS_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->logits, a->labels, a->grid, a->sts_temp, a->grid_index, a->ece,
+                        a->status};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return DS_ERR_INVALID_ARG;
+  if (a->ece_curve != nullptr && !aligned16(a->ece_curve)) return DS_ERR_INVALID_ARG;
+  const StsLayout L = sts_layout(a->N, a->n_grid, a->n_bins);
+  if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < L.total)
+    return DS_ERR_WORKSPACE;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  char* ws = static_cast<char*>(a->workspace);
+  StsParams p;
+  memset(&p, 0, sizeof(p));
+  p.N = a->N;
+  p.K = a->K;
+  p.G = a->n_grid;
+  p.n_bins = a->n_bins;
+  p.n_chunks = sts_num_chunks(a->N);
+  p.chunk = sts_chunk(a->N);
+  p.logits = a->logits;
+  p.labels = a->labels;
+  p.grid = a->grid;
+  p.sts_temp = a->sts_temp;
+  p.grid_index = a->grid_index;
+  p.ece = a->ece;
+  p.ece_curve = a->ece_curve;
+  p.ticket = reinterpret_cast<unsigned*>(ws + L.ticket);
+  p.base = reinterpret_cast<float*>(ws + L.base);
+  p.lab = reinterpret_cast<float*>(ws + L.lab);
+  p.part = reinterpret_cast<float*>(ws + L.part);
+  p.binsum = reinterpret_cast<float*>(ws + L.binsum);
+  p.ece_all = reinterpret_cast<float*>(ws + L.ece_all);
+  p.status = a->status;
+  if (launch_sts_fit(p, (cudaStream_t)stream) != cudaSuccess) return DS_ERR_CUDA;
   return DS_OK;
 }
 

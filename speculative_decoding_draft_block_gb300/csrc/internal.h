@@ -113,11 +113,37 @@ struct SchedParams {
   const float* sts_temp;
   const float* sps;
   float* conf;
+  float* conf_logit;  // optional
   float* survival;
   int32_t* sched_len;
   double* objective;
   int32_t* status;
 };
+
+// STS fit (sts.cu). Samples are split into at most kStsMaxChunks chunks of
+// sts_chunk(N) samples; each chunk leaves one partial histogram per grid point.
+constexpr int32_t kStsMaxChunks = 608;
+struct StsParams {
+  int32_t N, K, G, n_bins, n_chunks, chunk;
+  const float* logits;   // [N][K]
+  const float* labels;   // [N][K]
+  const float* grid;     // [G]
+  float* sts_temp;       // [K] out
+  int32_t* grid_index;   // [K] out
+  float* ece;            // [K] out
+  float* ece_curve;      // [K][G] out, optional
+  // workspace
+  unsigned* ticket;      // last-CTA counter of the reduce kernel
+  float* base;           // [2][N] prefix predictions, by position parity
+  float* lab;            // [2][N] prefix labels, by position parity
+  float* part;           // [n_chunks][n_bins][G]
+  float* binsum;         // [n_bins][G]
+  float* ece_all;        // [G]
+  int32_t* status;
+};
+int32_t sts_num_chunks(int32_t N);
+int32_t sts_chunk(int32_t N);
+size_t sts_hist_smem_bytes(int32_t n_bins);
 
 constexpr int kTileRows = 32;   // rows per sampling CTA
 constexpr int kTileCols = 256;  // tokens per sampling CTA (8 chunks of 32)
@@ -156,6 +182,7 @@ cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_confidence(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
+cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t s);
 size_t schedule_smem_bytes(int32_t B, int32_t K);
 cudaError_t launch_transpose(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_t,
                              cudaStream_t s);

@@ -76,10 +76,12 @@ __global__ void __launch_bounds__(256) confidence_kernel(SchedParams p) {
   const float de = dot_warp(E, reinterpret_cast<const Tin*>(p.w_e), p.r, lane);
   if (lane == 0) {
     const float Tk = p.sts_temp[k];
-    const float logit = __fdiv_rn(__fadd_rn(__fadd_rn(dh, de), p.bias), Tk);
+    const float raw = __fadd_rn(__fadd_rn(dh, de), p.bias);
+    const float logit = __fdiv_rn(raw, Tk);
     const float c = __frcp_rn(__fadd_rn(1.f, expf(-logit)));
     if (!(c == c) || !(Tk > 0.f)) report(p.status, kErrNonfinite);
     p.conf[item] = c;
+    if (p.conf_logit) p.conf_logit[item] = raw;
   }
 }
 

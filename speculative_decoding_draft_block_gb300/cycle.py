@@ -52,6 +52,7 @@ class DeviceCycle:
         self.q_token = torch.zeros((B, K), **f32)
         self.q_stats = torch.zeros((B, K, 4), **i32)
         self.conf = torch.zeros((B, K), **f32)
+        self.conf_logit = torch.zeros((B, K), **f32)   # raw logit: the STS fit's input
         self.survival = torch.zeros((B, K), **f32)
         self.sched_len = torch.zeros((B,), **i32)
         self.objective = torch.zeros((2,), dtype=torch.float64, device=dev)
@@ -92,7 +93,8 @@ class DeviceCycle:
                                           self.mode, self.conf, self.survival, self.sched_len,
                                           self.objective, self.status, threshold=self.threshold,
                                           stream=stream, budget_ring=self.budget_ring,
-                                          cycle=self.sched_cycle), "ds_confidence_schedule")
+                                          cycle=self.sched_cycle, conf_logit=self.conf_logit),
+              "ds_confidence_schedule")
         self.sched_cycle += 1
 
     def verify(self, seed, stream=None):
@@ -124,6 +126,7 @@ class DeviceCycle:
             "q_sum": st[..., 0].view(np.float32).astype(np.float64) + st[..., 1].view(np.float32),
             "q_ref": st[..., 2].copy(),
             "conf": self.conf.cpu().numpy().astype(np.float64),
+            "conf_logit": self.conf_logit.cpu().numpy().astype(np.float64),
             "survival": self.survival.cpu().numpy().astype(np.float64),
             "L": self.sched_len.cpu().numpy().astype(np.int64),
             "objective": float(self.objective[0].item()),

@@ -62,6 +62,14 @@ def test_workspace_sizes_and_limits(lib):
     assert _lib.ds_draft_workspace_bytes(128, 16, 151937, 256) == 0      # V % 8 != 0
     assert _lib.ds_draft_workspace_bytes(1024, 17, 1024, 256) == 0       # B*K > 16384
     assert _lib.ds_sched_workspace_bytes(128, 16) == 0
+    # STS fit: N samples x K positions, grid and bins within their limits
+    ws = _lib.ds_sts_workspace_bytes(65536, 16, 256, 15)
+    assert ws >= 4 * (4 * 65536 + 256 * 256 * 15)        # prefixes + one partial per chunk
+    assert _lib.ds_sts_workspace_bytes(0, 16, 256, 15) == 0
+    assert _lib.ds_sts_workspace_bytes(100, 65, 256, 15) == 0
+    assert _lib.ds_sts_workspace_bytes(100, 4, 4097, 15) == 0
+    assert _lib.ds_sts_workspace_bytes(100, 4, 16, 65) == 0
+    assert _lib.ds_sts_workspace_bytes(1, 1, 1, 1) > 0
 
 
 def test_host_validation_rejects_without_launching(lib):
@@ -72,5 +80,8 @@ def test_host_validation_rejects_without_launching(lib):
     assert lib.ds_draft_block(ctypes.byref(a), None) == 1
     assert lib.ds_verify(ctypes.byref(_lib.VerifyArgs()), None) == 1
     assert lib.ds_confidence_schedule(ctypes.byref(_lib.SchedArgs()), None) == 1
+    assert lib.ds_sts_fit(ctypes.byref(_lib.StsArgs()), None) == 1
+    a = _lib.StsArgs(N=4, K=2, n_grid=8, n_bins=10)      # sizes fine, pointers missing
+    assert lib.ds_sts_fit(ctypes.byref(a), None) == 1
     assert _lib.ds_status_string(7) == "non-finite logit or empty distribution"
     assert _lib.ds_version() == "0.1.0"
