@@ -277,7 +277,7 @@ MUFU_PER_EVAL = 2          # one exp2 and one reciprocal per sigmoid
 
 
 def run_sts(args, rank, ws, local):
-    """Time ds_sts_fit (all K positions, both kernels) on the synthetic calibration set."""
+    """Time ds_sts_fit (all K positions) on the synthetic calibration set."""
     import numpy as np
     import torch
     from speculative_decoding_draft_block_gb300 import _lib
@@ -340,10 +340,10 @@ def run_sts(args, rank, ws, local):
                    "l2": "flushed between steps (256 MiB write, outside the timed events)"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "T sigmoid evals/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "whole ds_sts_fit call (sts_hist_kernel + sts_reduce_kernel, K each)",
+                     "kernel": "whole ds_sts_fit call (sts_fit_kernel, one launch per position)",
                      "peak_source": "derived: SMs x %d MUFU/clk / %d MUFU per evaluation x max SM clock"
                                     % (MUFU_PER_CLK_SM, MUFU_PER_EVAL)},
-        "gpu_launches": K * 2 * STS_K,
+        "gpu_launches": K * STS_K,
         "fitted_temps": [float(x) for x in T.cpu().numpy()],
         "ece": [float(x) for x in ece.cpu().numpy()],
         "clocks": sampler.summary(),

@@ -90,9 +90,9 @@ VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
   return l;
 }
 
-// STS fit workspace: ticket, prefix buffers, per-chunk histograms, bin sums, ECE curve.
+// STS fit workspace: ticket, prefix buffers, fixed-point histogram, ECE curve.
 struct StsLayout {
-  size_t ticket, base, lab, part, binsum, ece_all, total;
+  size_t ticket, base, lab, hist64, ece_all, total;
 };
 
 bool sts_shape_ok(int32_t N, int32_t K, int32_t G, int32_t n_bins) {
@@ -108,12 +108,10 @@ StsLayout sts_layout(int32_t N, int32_t G, int32_t n_bins) {
     off += (bytes + 255) & ~size_t(255);
     return at;
   };
-  const size_t chunks = (size_t)sts_num_chunks(N);
   L.ticket = take(sizeof(unsigned));
   L.base = take(sizeof(float) * 2 * (size_t)N);
   L.lab = take(sizeof(float) * 2 * (size_t)N);
-  L.part = take(sizeof(float) * chunks * n_bins * G);
-  L.binsum = take(sizeof(float) * (size_t)n_bins * G);
+  L.hist64 = take(sizeof(long long) * (size_t)n_bins * G);
   L.ece_all = take(sizeof(float) * (size_t)G);
   L.total = off;
   return L;
@@ -303,8 +301,6 @@ ds_status ds_sts_fit(const ds_sts_args* a, ds_stream_t stream) {
   p.K = a->K;
   p.G = a->n_grid;
   p.n_bins = a->n_bins;
-  p.n_chunks = sts_num_chunks(a->N);
-  p.chunk = sts_chunk(a->N);
   p.logits = a->logits;
   p.labels = a->labels;
   p.grid = a->grid;
@@ -315,8 +311,7 @@ ds_status ds_sts_fit(const ds_sts_args* a, ds_stream_t stream) {
   p.ticket = reinterpret_cast<unsigned*>(ws + L.ticket);
   p.base = reinterpret_cast<float*>(ws + L.base);
   p.lab = reinterpret_cast<float*>(ws + L.lab);
-  p.part = reinterpret_cast<float*>(ws + L.part);
-  p.binsum = reinterpret_cast<float*>(ws + L.binsum);
+  p.hist64 = reinterpret_cast<long long*>(ws + L.hist64);
   p.ece_all = reinterpret_cast<float*>(ws + L.ece_all);
   p.status = a->status;
   if (launch_sts_fit(p, (cudaStream_t)stream) != cudaSuccess) return DS_ERR_CUDA;

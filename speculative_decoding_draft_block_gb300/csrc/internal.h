@@ -120,9 +120,8 @@ struct SchedParams {
   int32_t* status;
 };
 
-// STS fit (sts.cu). Samples are split into at most kStsMaxChunks chunks of
-// sts_chunk(N) samples; each chunk leaves one partial histogram per grid point.
-constexpr int32_t kStsMaxChunks = 608;
+// STS fit (sts.cu). The sample chunks per CTA are chosen at launch from the
+// SM count; the workspace does not depend on them.
 struct StsParams {
   int32_t N, K, G, n_bins, n_chunks, chunk;
   const float* logits;   // [N][K]
@@ -133,17 +132,13 @@ struct StsParams {
   float* ece;            // [K] out
   float* ece_curve;      // [K][G] out, optional
   // workspace
-  unsigned* ticket;      // last-CTA counter of the reduce kernel
+  unsigned* ticket;      // last-CTA counter
   float* base;           // [2][N] prefix predictions, by position parity
   float* lab;            // [2][N] prefix labels, by position parity
-  float* part;           // [n_chunks][n_bins][G]
-  float* binsum;         // [n_bins][G]
+  long long* hist64;     // [n_bins][G] fixed-point bin totals (zero between positions)
   float* ece_all;        // [G]
   int32_t* status;
 };
-int32_t sts_num_chunks(int32_t N);
-int32_t sts_chunk(int32_t N);
-size_t sts_hist_smem_bytes(int32_t n_bins);
 
 constexpr int kTileRows = 32;   // rows per sampling CTA
 constexpr int kTileCols = 256;  // tokens per sampling CTA (8 chunks of 32)

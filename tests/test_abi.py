@@ -64,7 +64,7 @@ def test_workspace_sizes_and_limits(lib):
     assert _lib.ds_sched_workspace_bytes(128, 16) == 0
     # STS fit: N samples x K positions, grid and bins within their limits
     ws = _lib.ds_sts_workspace_bytes(65536, 16, 256, 15)
-    assert ws >= 4 * (4 * 65536 + 256 * 256 * 15)        # prefixes + one partial per chunk
+    assert ws >= 4 * 4 * 65536 + 8 * 256 * 15            # prefixes + fixed-point histogram
     assert _lib.ds_sts_workspace_bytes(0, 16, 256, 15) == 0
     assert _lib.ds_sts_workspace_bytes(100, 65, 256, 15) == 0
     assert _lib.ds_sts_workspace_bytes(100, 4, 4097, 15) == 0
