@@ -38,6 +38,11 @@ Parity status per function (see the pins in tests/test_oracle_*.py):
                                   form, exact recovery of the true temperatures
                                   with zero ECE, prefix and causality
                                   metamorphic tests, first-index ties)
+  gru_cell, rnn_draft_block ..... pinned (torch.nn.GRUCell in float64, closed
+                                  forms with saturated gates, a frozen zero
+                                  state drawing from the base logits alone,
+                                  memory beyond the previous token, bfloat16
+                                  rounding against the generator's rounding)
   cycle ......................... composition of the above
 """
 
@@ -51,6 +56,7 @@ from .verify import verify, verify_request
 from .cycle import cycle
 from .bf16 import bf16_bits_to_f64
 from .sts import sts_fit, sts_curves, ece
+from .rnn import gru_cell, rnn_draft_block
 
 __all__ = [
     "philox4x32_10", "uniform", "STAGE_DRAFT", "STAGE_ACCEPT", "STAGE_RESAMPLE",
@@ -60,5 +66,5 @@ __all__ = [
     "schedule", "sps_at", "async_budgets", "SCHED_GREEDY_EARLYSTOP", "SCHED_FIXED_K",
     "SCHED_THRESHOLD", "SCHED_ASYNC",
     "verify", "verify_request", "cycle", "bf16_bits_to_f64",
-    "sts_fit", "sts_curves", "ece",
+    "sts_fit", "sts_curves", "ece", "gru_cell", "rnn_draft_block",
 ]

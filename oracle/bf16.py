@@ -18,3 +18,29 @@ def as_f64(x):
     if x.dtype == np.uint16:
         return bf16_bits_to_f64(x)
     return x.astype(np.float64)
+
+
+def round_bf16(x):
+    """Round float64 values to the nearest bfloat16 (ties to even), returned as float64.
+
+    Rounds from float64 directly (no intermediate float32, so no double
+    rounding): x = m * 2^e with 0.5 <= |m| < 1 has 8 significant bits kept.
+    Values are assumed inside the normal bfloat16 range (|x| >= 2^-126 or 0).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def bf16_tie_distance(x):
+    """Distance of x to the nearest bfloat16 rounding boundary, relative to |x|.
+
+    A value this close to a boundary may round the other way in any other
+    working precision; comparisons with another implementation excuse it.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, _ = np.frexp(x)
+    s = np.abs(m) * 256.0                      # in [128, 256): rounding boundaries at k + 0.5
+    d = np.abs(s - (np.floor(s) + 0.5))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return np.where(x == 0, np.inf, d / s)

@@ -75,7 +75,7 @@ def verify_request(tokens, L, p_row, q_row, u_accept, u_resample, greedy=False):
 
 
 def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperature, seed,
-           request_ids=None):
+           request_ids=None, states=None):
     """Verify a batch. target_logits: [B, K+1, V]; base_logits: [B, K, V].
 
     The draft distribution q_k is recomputed from the base logits and the Markov
@@ -83,6 +83,10 @@ def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperat
 
     ``request_ids`` (optional [B]) gives each row's request index in the Philox
     counter when the rows are a subset of a larger batch.
+
+    ``states`` (optional [B, K, r]) selects the RNN head: q_k is then rebuilt
+    from the base logits and the bias s_k . P of the state the draft used at
+    that position, exactly as the RNN draft defined it.
 
     Returns a dict with accept_count [B], num_emitted [B], out_tokens [B, K+1]
     (-1 padded) and decisions (per request, see verify_request).
@@ -108,6 +112,9 @@ def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperat
             return row if greedy else _probs(row, T)
 
         def q_row(j, b=b, T=T):
+            if states is not None:
+                ell = as_f64(base_logits[b, j]) + as_f64(states[b, j]) @ as_f64(P)
+                return _probs(ell, T)
             prev = anchor[b] if j == 0 else tokens[b, j - 1]
             ell = markov_logits(np.asarray(base_logits[b, j])[None, :], E, P, [prev])[0]
             return _probs(ell, T)
