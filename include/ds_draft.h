@@ -106,17 +106,32 @@ ds_status ds_philox_fill(const uint32_t* ctr, uint32_t key0, uint32_t key1, uint
                          int32_t n, ds_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
-/* Draft block: Markov head + sequential sampling                            */
+/* Draft block: sequential head (Markov or RNN) + sequential sampling        */
 /* ------------------------------------------------------------------------ */
 
 /*
  * [DSpark] 방법론 › 반자기회귀 생성. For k = 1..K, with x_0 = anchor[b]:
- *     l_k = z_k + E[x_{k-1}] . P             (low-rank first-order transition bias)
+ *     l_k = z_k + E[x_{k-1}] . P             (Markov head: low-rank first-order bias)
  *     x_k ~ softmax(l_k / T_b)                (T_b = 0: argmax, lowest index on ties)
  * The draw is the inverse CDF in token order: x = min{i : u * S < C_i} with
  * u = U(seed, b, k, DS_STAGE_DRAFT). The loop is sequential over k and
  * parallel over requests and vocabulary; the V-wide logits are never stored.
+ *
+ * RNN head (head = DS_HEAD_RNN; same section: a recurrent state over the
+ * whole drafted prefix, updated from the state, the previous token's
+ * embedding and the backbone hidden state by a gated update). The state s_k
+ * (size r) replaces E[x_{k-1}] as the input of P:  l_k = z_k + s_k . P, with
+ *     g_i = W_ih [E[x_{k-1}] ; h_k] + b_ih,  g_h = W_hh s_{k-1} + b_hh  (rows:
+ *           reset, update, new; the cuDNN GRU cell),  s_0 = 0,
+ *     r = sigmoid(g_i^r + g_h^r), u = sigmoid(g_i^u + g_h^u),
+ *     n = tanh(g_i^n + r * g_h^n), s_k = (1 - u) * n + u * s_{k-1},
+ * each s_k rounded to bfloat16 (nearest even), the storage type. bfloat16
+ * only, r % 64 == 0, d % 64 == 0; the workspace is
+ * ds_draft_workspace_bytes(B, K, V, r) + ds_rnn_workspace_bytes(B, K, r)
+ * bytes. The states are returned for ds_verify.
  */
+typedef enum { DS_HEAD_MARKOV = 0, DS_HEAD_RNN = 1 } ds_head;
+
 typedef struct {
   int32_t B, K, V, r;
   int32_t dtype;              /* ds_dtype of base_logits, E and P */
@@ -131,13 +146,36 @@ typedef struct {
   int32_t* draft_tokens;      /* out [B][K] x_k */
   float* q_token;             /* out [B][K] q_k(x_k) (1.0 for greedy positions) */
   ds_row_stats* q_stats;      /* out [B][K] statistics of q_k, read by ds_verify */
-  void* workspace;            /* scratch, ds_draft_workspace_bytes(B, K, V, r) bytes */
+  void* workspace;            /* scratch, ds_draft_workspace_bytes(B, K, V, r) bytes
+                                 (+ ds_rnn_workspace_bytes for the RNN head) */
   size_t workspace_bytes;
   int32_t* status;            /* device word, see Errors above */
+  /* RNN head only (ignored for DS_HEAD_MARKOV, the value of a zeroed struct): */
+  int32_t head;               /* ds_head */
+  int32_t d;                  /* hidden size */
+  const void* h;              /* [B][K][d]  backbone hidden states h_k */
+  const void* rnn_w_ih;       /* [3r][r + d] input weights, columns [embedding ; hidden] */
+  const void* rnn_w_step;     /* [4r][2r]   W_ih and W_hh packed by ds_rnn_pack_weights */
+  const float* rnn_b_ih;      /* [3r] */
+  const float* rnn_b_hh;      /* [3r] */
+  void* states;               /* out [B][K][r] s_k of every position (bfloat16) */
 } ds_draft_args;
 
 size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
 ds_status ds_draft_block(const ds_draft_args* args, ds_stream_t stream);
+
+/* Extra workspace of the RNN head (0 if the shape is outside its limits). */
+size_t ds_rnn_workspace_bytes(int32_t B, int32_t K, int32_t r);
+
+/*
+ * Weight layout of the RNN head, once per model (like ds_transpose_projection):
+ * packs W_ih [3r][r + d] and W_hh [3r][r] into W_step [4r][2r] so that each
+ * block of 32 state units has its reset, update, new-input and new-recurrent
+ * rows over [embedding ; state] next to each other. Bit-exact copy (zeros
+ * where a gate does not read an input). bfloat16 only; r, d multiples of 64.
+ */
+ds_status ds_rnn_pack_weights(const void* W_ih, const void* W_hh, int32_t r, int32_t d, int32_t dtype,
+                              void* W_step, ds_stream_t stream);
 
 /*
  * Token-major copy of the Markov projection: P_t[v][k] = P[k][v] for
@@ -282,6 +320,8 @@ typedef struct {
   void* workspace;            /* ds_verify_workspace_bytes(B, K, V, r) bytes */
   size_t workspace_bytes;
   int32_t* status;
+  const void* states;         /* RNN head: [B][K][r] states from ds_draft_block (q_k is rebuilt
+                                 with s_k . P); NULL for the Markov head */
 } ds_verify_args;
 
 size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);

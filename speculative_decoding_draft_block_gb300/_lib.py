@@ -18,6 +18,7 @@ DS_OK = 0
 DS_F32, DS_BF16 = 0, 1
 DS_STAGE_DRAFT, DS_STAGE_ACCEPT, DS_STAGE_RESAMPLE = 0, 1, 2
 DS_SCHED_GREEDY_EARLYSTOP, DS_SCHED_FIXED_K, DS_SCHED_THRESHOLD, DS_SCHED_ASYNC = 0, 1, 2, 3
+DS_HEAD_MARKOV, DS_HEAD_RNN = 0, 1
 STATUS_NAMES = {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_UNSUPPORTED", 3: "DS_ERR_WORKSPACE",
                 4: "DS_ERR_CUDA", 5: "DS_ERR_TIMEOUT", 6: "DS_ERR_BOUNDS", 7: "DS_ERR_NONFINITE"}
 
@@ -26,7 +27,7 @@ EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspa
            "ds_draft_block", "ds_sched_workspace_bytes", "ds_confidence_schedule",
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
            "ds_version", "ds_transpose_projection", "ds_verify_static", "ds_sts_workspace_bytes",
-           "ds_sts_fit")
+           "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -37,7 +38,9 @@ class DraftArgs(ctypes.Structure):
                 ("base_logits", _vp), ("E", _vp), ("P", _vp), ("P_t", _vp), ("anchor", _vp),
                 ("temperature", _vp), ("seed", ctypes.c_uint64), ("draft_tokens", _vp),
                 ("q_token", _vp), ("q_stats", _vp), ("workspace", _vp),
-                ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
+                ("workspace_bytes", ctypes.c_size_t), ("status", _vp),
+                ("head", _i32), ("d", _i32), ("h", _vp), ("rnn_w_ih", _vp), ("rnn_w_step", _vp),
+                ("rnn_b_ih", _vp), ("rnn_b_hh", _vp), ("states", _vp)]
 
 
 class SchedArgs(ctypes.Structure):
@@ -64,7 +67,8 @@ class VerifyArgs(ctypes.Structure):
                 ("anchor", _vp), ("draft_tokens", _vp), ("q_token", _vp), ("q_stats", _vp),
                 ("sched_len", _vp), ("temperature", _vp), ("seed", ctypes.c_uint64),
                 ("out_tokens", _vp), ("accept_count", _vp), ("num_emitted", _vp),
-                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp),
+                ("states", _vp)]
 
 
 _lib = None
@@ -97,6 +101,10 @@ def load():
     lib.ds_verify_static.restype = ctypes.c_int
     for f in ("ds_draft_block", "ds_confidence_schedule", "ds_verify"):
         getattr(lib, f).restype = ctypes.c_int
+    lib.ds_rnn_workspace_bytes.argtypes = [_i32] * 3
+    lib.ds_rnn_workspace_bytes.restype = ctypes.c_size_t
+    lib.ds_rnn_pack_weights.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp]
+    lib.ds_rnn_pack_weights.restype = ctypes.c_int
     lib.ds_sts_workspace_bytes.argtypes = [_i32] * 4
     lib.ds_sts_workspace_bytes.restype = ctypes.c_size_t
     lib.ds_sts_fit.argtypes = [ctypes.POINTER(StsArgs), _vp]
@@ -189,8 +197,18 @@ def ds_verify_workspace_bytes(B, K, V, r):
 # ---- the three calls ----------------------------------------------------------
 
 def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q_token, q_stats,
-                   workspace, status, stream=None, P_t=None):
+                   workspace, status, stream=None, P_t=None, rnn=None):
+    """Draft one block. ``rnn`` selects the RNN head: a dict with h [B, K, d],
+    w_ih [3r, r + d], w_step (from ds_rnn_pack_weights), b_ih, b_hh (float32
+    [3r]) and states (output [B, K, r]); the workspace must then also hold
+    ds_rnn_workspace_bytes(B, K, r)."""
     B, K, V = base_logits.shape
+    extra = {}
+    if rnn is not None:
+        extra = dict(head=DS_HEAD_RNN, d=int(rnn["h"].shape[2]), h=_ptr(rnn["h"], "h"),
+                     rnn_w_ih=_ptr(rnn["w_ih"], "w_ih"), rnn_w_step=_ptr(rnn["w_step"], "w_step"),
+                     rnn_b_ih=_ptr(rnn["b_ih"], "b_ih"), rnn_b_hh=_ptr(rnn["b_hh"], "b_hh"),
+                     states=_ptr(rnn["states"], "states"))
     a = DraftArgs(B=B, K=K, V=V, r=E.shape[1], dtype=_dtype_code(base_logits),
                   base_logits=_ptr(base_logits, "base_logits"), E=_ptr(E, "E"), P=_ptr(P, "P"),
                   P_t=None if P_t is None else _ptr(P_t, "P_t"),
@@ -199,8 +217,20 @@ def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q
                   q_token=_ptr(q_token, "q_token"), q_stats=_ptr(q_stats, "q_stats"),
                   workspace=_ptr(workspace, "workspace"),
                   workspace_bytes=workspace.numel() * workspace.element_size(),
-                  status=_ptr(status, "status"))
+                  status=_ptr(status, "status"), **extra)
     return load().ds_draft_block(ctypes.byref(a), _stream(stream))
+
+
+def ds_rnn_workspace_bytes(B, K, r):
+    return load().ds_rnn_workspace_bytes(B, K, r)
+
+
+def ds_rnn_pack_weights(w_ih, w_hh, w_step, stream=None):
+    """W_step [4r, 2r] from W_ih [3r, r + d] and W_hh [3r, r] (once per model)."""
+    r3, rd = w_ih.shape
+    r = r3 // 3
+    return load().ds_rnn_pack_weights(_ptr(w_ih, "w_ih"), _ptr(w_hh, "w_hh"), r, rd - r,
+                                      _dtype_code(w_ih), _ptr(w_step, "w_step"), _stream(stream))
 
 
 def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp, sps, mode,
@@ -227,7 +257,7 @@ def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp,
 
 def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats, sched_len,
               temperature, seed, out_tokens, accept_count, num_emitted, workspace, status,
-              stream=None, P_t=None):
+              stream=None, P_t=None, states=None):
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
                    target_logits=_ptr(target_logits, "target_logits"),
@@ -241,7 +271,8 @@ def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q
                    num_emitted=_ptr(num_emitted, "num_emitted"),
                    workspace=_ptr(workspace, "workspace"),
                    workspace_bytes=workspace.numel() * workspace.element_size(),
-                   status=_ptr(status, "status"))
+                   status=_ptr(status, "status"),
+                   states=None if states is None else _ptr(states, "states"))
     return load().ds_verify(ctypes.byref(a), _stream(stream))
 
 
@@ -254,7 +285,7 @@ def ds_transpose_projection(P, P_t, stream=None):
 
 def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats,
                      sched_len, temperature, seed, out_tokens, accept_count, num_emitted, status,
-                     stream=None, P_t=None):
+                     stream=None, P_t=None, states=None):
     """ds_verify with the library's static scratch (no workspace argument)."""
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
@@ -267,7 +298,8 @@ def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_t
                    seed=int(seed), out_tokens=_ptr(out_tokens, "out_tokens"),
                    accept_count=_ptr(accept_count, "accept_count"),
                    num_emitted=_ptr(num_emitted, "num_emitted"),
-                   workspace=None, workspace_bytes=0, status=_ptr(status, "status"))
+                   workspace=None, workspace_bytes=0, status=_ptr(status, "status"),
+                   states=None if states is None else _ptr(states, "states"))
     return load().ds_verify_static(ctypes.byref(a), _stream(stream))
 
 

@@ -75,6 +75,25 @@ DraftLayout draft_layout(int32_t B, int32_t V, int32_t r) {
 
 size_t draft_ws(int32_t B, int32_t V, int32_t r) { return draft_layout(B, V, r).total; }
 
+// RNN head workspace, after the draft workspace: the hidden-state part of the
+// gate inputs for every position (f32 [B*K][3r]) and two input-row buffers
+// [e ; s] (bf16 [2][B][2r]), alternating by position parity.
+struct RnnLayout {
+  size_t gh, gru_in, total;
+};
+
+bool rnn_shape_ok(int32_t B, int32_t K, int32_t r) {
+  return B >= 1 && K >= 1 && K <= 64 && (int64_t)B * K <= 16384 && r >= 64 && r <= 1024 && r % 64 == 0;
+}
+
+RnnLayout rnn_layout(int32_t B, int32_t K, int32_t r) {
+  RnnLayout l;
+  l.gh = 0;
+  l.gru_in = align_up(sizeof(float) * (size_t)B * K * 3 * r);
+  l.total = l.gru_in + align_up(sizeof(__nv_bfloat16) * 2 * (size_t)B * 2 * r);
+  return l;
+}
+
 struct VerifyLayout {
   size_t vrows, desc, chunks, supers, total;
 };
@@ -115,6 +134,67 @@ StsLayout sts_layout(int32_t N, int32_t G, int32_t n_bins) {
   L.ece_all = take(sizeof(float) * (size_t)G);
   L.total = off;
   return L;
+}
+
+// The RNN head's draft loop. Per call: the hidden-state part of the gate
+// inputs for all positions, the first input rows [E[anchor] ; 0] and the
+// first state; per position p: tile and locate with the state s_p as A rows
+// (the locate stages E[x_p] into the input rows), then the update to s_{p+1}.
+ds_status draft_rnn(const ds_draft_args* a, SampleParams& p, char* rw, char* ws, const DraftLayout& l,
+                    cudaStream_t s) {
+  const int32_t B = a->B, K = a->K, r = a->r;
+  const RnnLayout rl = rnn_layout(B, K, r);
+  float* gh = reinterpret_cast<float*>(rw + rl.gh);
+  __nv_bfloat16* in[2];
+  in[0] = reinterpret_cast<__nv_bfloat16*>(rw + rl.gru_in);
+  in[1] = in[0] + (size_t)B * 2 * r;
+  const __nv_bfloat16* w_ih = reinterpret_cast<const __nv_bfloat16*>(a->rnn_w_ih);
+
+  GemmParams g;
+  memset(&g, 0, sizeof(g));
+  g.M = B * K;
+  g.N = 3 * r;
+  g.Kd = a->d;
+  g.bias = a->rnn_b_ih;
+  g.out = gh;
+  g.status = a->status;
+  if (launch_rnn_gemm(g, kGemmBias, a->h, a->d, w_ih + r, (int64_t)r + a->d, s) != cudaSuccess)
+    return DS_ERR_CUDA;
+  if (launch_rnn_init(a->E, a->anchor, B, r, a->V, in[0], a->status, s) != cudaSuccess)
+    return DS_ERR_CUDA;
+
+  GemmParams u;
+  memset(&u, 0, sizeof(u));
+  u.M = B;
+  u.N = 4 * r;
+  u.Kd = 2 * r;
+  u.gh = gh;
+  u.b_hh = a->rnn_b_hh;
+  u.states = reinterpret_cast<__nv_bfloat16*>(a->states);
+  u.r = r;
+  u.K = K;
+  u.status = a->status;
+  auto update = [&](int pos) {  // s_pos from the input rows of position pos - 1
+    u.p = pos;
+    u.s_prev = in[(pos - 1) & 1] + r;
+    u.s_next = in[pos & 1] + r;
+    return launch_rnn_gemm(u, kGemmGru, in[(pos - 1) & 1], 2 * r, a->rnn_w_step, 2 * r, s);
+  };
+  if (update(1) != cudaSuccess) return DS_ERR_CUDA;
+  p.a_stage_stride = 2 * r;
+  p.a_rows_stride = 2 * r;
+  for (int k = 1; k <= K; ++k) {
+    p.step = k;
+    p.chunks = reinterpret_cast<ChunkRec*>(ws + l.rec[k & 1]);
+    p.supers = reinterpret_cast<ChunkRec*>(ws + l.sup[k & 1]);
+    p.a_stage_in = in[k & 1] + r;
+    p.a_rows = in[k & 1] + r;
+    p.a_stage_out = (k < K) ? in[k & 1] : nullptr;
+    if (launch_tile_tc(p, s) != cudaSuccess) return DS_ERR_CUDA;
+    if (launch_sample_locate(p, s) != cudaSuccess) return DS_ERR_CUDA;
+    if (k < K && update(k + 1) != cudaSuccess) return DS_ERR_CUDA;
+  }
+  return DS_OK;
 }
 
 }  // namespace
@@ -167,8 +247,19 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
   if (a->P_t != nullptr && !aligned16(a->P_t)) return DS_ERR_INVALID_ARG;
-  if (a->workspace == nullptr || !aligned16(a->workspace) ||
-      a->workspace_bytes < draft_ws(a->B, a->V, a->r))
+  const bool rnn = a->head == DS_HEAD_RNN;
+  if (a->head != DS_HEAD_MARKOV && !rnn) return DS_ERR_INVALID_ARG;
+  size_t need = draft_ws(a->B, a->V, a->r);
+  const size_t rnn_off = align_up(need);
+  if (rnn) {
+    if (a->dtype != DS_BF16 || !rnn_shape_ok(a->B, a->K, a->r)) return DS_ERR_UNSUPPORTED;
+    if (a->d < 64 || a->d % 64 != 0) return DS_ERR_INVALID_ARG;
+    const void* rp[] = {a->h, a->rnn_w_ih, a->rnn_w_step, a->rnn_b_ih, a->rnn_b_hh, a->states};
+    for (const void* q : rp)
+      if (!aligned16(q)) return DS_ERR_INVALID_ARG;
+    need = rnn_off + rnn_layout(a->B, a->K, a->r).total;
+  }
+  if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < need)
     return DS_ERR_WORKSPACE;
   const ds_status st = device_supported();
   if (st != DS_OK) return st;
@@ -202,6 +293,8 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   else
     simt_group_layout(p);
   const cudaStream_t s = (cudaStream_t)stream;
+  p.a_stage_stride = a->r;
+  if (rnn) return draft_rnn(a, p, ws + rnn_off, ws, l, s);
   for (int k = 1; k <= a->K; ++k) {
     p.step = k;
     p.chunks = reinterpret_cast<ChunkRec*>(ws + l.rec[k & 1]);
@@ -214,6 +307,21 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
     if (e != cudaSuccess) return DS_ERR_CUDA;
   }
   return DS_OK;
+}
+
+size_t ds_rnn_workspace_bytes(int32_t B, int32_t K, int32_t r) {
+  if (!rnn_shape_ok(B, K, r)) return 0;
+  return rnn_layout(B, K, r).total;
+}
+
+ds_status ds_rnn_pack_weights(const void* W_ih, const void* W_hh, int32_t r, int32_t d, int32_t dtype,
+                              void* W_step, ds_stream_t stream) {
+  if (dtype != DS_BF16) return DS_ERR_UNSUPPORTED;
+  if (r < 64 || r > 1024 || r % 64 != 0 || d < 64 || d % 64 != 0) return DS_ERR_INVALID_ARG;
+  if (!aligned16(W_ih) || !aligned16(W_hh) || !aligned16(W_step)) return DS_ERR_INVALID_ARG;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  return from_cuda(launch_rnn_pack(W_ih, W_hh, r, d, W_step, (cudaStream_t)stream));
 }
 
 size_t ds_sched_workspace_bytes(int32_t B, int32_t K) {
@@ -338,6 +446,9 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   const bool tc = tc_path_supported(a->dtype, a->r);
   if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < l.total)
     return DS_ERR_WORKSPACE;
+  if (a->states != nullptr &&
+      (!aligned16(a->states) || !tc_path_supported(a->dtype, a->r) || a->dtype != DS_BF16))
+    return DS_ERR_INVALID_ARG;
   const ds_status st = device_supported();
   if (st != DS_OK) return st;
   char* ws = reinterpret_cast<char*>(a->workspace);
@@ -385,6 +496,11 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   p.draft_tokens = a->draft_tokens;
   p.temperature = a->temperature;
   p.final_desc = v.final_desc;
+  p.a_stage_stride = a->r;
+  if (a->states != nullptr) {  // RNN head: the residual's bias row is the draft's state
+    p.a_rows = a->states;
+    p.a_rows_stride = a->K * a->r;
+  }
   p.chunks = reinterpret_cast<ChunkRec*>(ws + l.chunks);
   p.supers = reinterpret_cast<ChunkRec*>(ws + l.supers);
   if (tc)

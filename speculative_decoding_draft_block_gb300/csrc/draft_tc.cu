@@ -284,6 +284,19 @@ __device__ __forceinline__ int a_token_for_row(const SampleParams& sp, int b) {
   return (tok >= 0 && tok < sp.V) ? tok : 0;  // out-of-range ids are reported by make_row_ctx
 }
 
+// Row b of the A operand: E[token] for the Markov head; for the RNN head the
+// current state (draft) or the state of the final-draw row (verify).
+__device__ __forceinline__ const __nv_bfloat16* a_row_src(const SampleParams& sp, int b) {
+  const __nv_bfloat16* rows = reinterpret_cast<const __nv_bfloat16*>(sp.a_rows);
+  if (rows == nullptr)
+    return reinterpret_cast<const __nv_bfloat16*>(sp.E) + (size_t)a_token_for_row(sp, b) * sp.r;
+  if (b >= sp.B) return rows;  // padding rows of the last M-tile
+  if (sp.src == 0) return rows + (size_t)b * sp.a_rows_stride;
+  int j = sp.final_desc[b].row;
+  j = j < 0 ? 0 : (j >= sp.K ? sp.K - 1 : j);  // bonus rows (j = K) need no bias
+  return rows + (size_t)b * sp.a_rows_stride + (size_t)j * sp.r;
+}
+
 template <bool kFinal>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tile_tc_kernel(const __grid_constant__ TcParams prm, const __grid_constant__ CUtensorMap tmP,
@@ -478,9 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int m = et / kThreadsPerRow, part = et % kThreadsPerRow;
           const int per_row = prm.nkb * 8;  // 16-byte chunks per row
           const int cpt = per_row / kThreadsPerRow;
-          const int tok = a_token_for_row(sp, mt * 128 + m);
-          const uint4* src = reinterpret_cast<const uint4*>(
-              reinterpret_cast<const __nv_bfloat16*>(sp.E) + (size_t)tok * sp.r) + part * cpt;
+          const uint4* src = reinterpret_cast<const uint4*>(a_row_src(sp, mt * 128 + m)) + part * cpt;
           constexpr int kMaxCpt = 32 / kThreadsPerRow;
           constexpr int kBatch = kMaxCpt < 8 ? kMaxCpt : 8;  // loads in flight per thread
 #pragma unroll
@@ -640,12 +651,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 
 bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box) {
-  auto fn = get_encoder();
-  if (!fn) return false;
-  const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tmap_bf16(m, ptr, rank, dims, strides, box);
 }
 
 int num_sms() {
@@ -656,6 +662,16 @@ int num_sms() {
 }
 
 }  // namespace
+
+bool encode_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = get_encoder();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 void tc_group_layout(SampleParams& p) {
   static const int sms = num_sms();
@@ -713,7 +729,7 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   CUtensorMap mA = mP;  // unused unless A rows are staged
   if (p.a_stage_in != nullptr) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.r, (cuuint64_t)p.B};
-    const cuuint64_t str[1] = {(cuuint64_t)p.r * 2};
+    const cuuint64_t str[1] = {(cuuint64_t)p.a_stage_stride * 2};
     const cuuint32_t box[2] = {64, 128};
     if (!encode(&mA, p.a_stage_in, 2, dims, str, box)) return cudaErrorInvalidValue;
   }

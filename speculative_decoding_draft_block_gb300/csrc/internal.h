@@ -1,5 +1,7 @@
 // Internal types shared by the kernels and the C-ABI layer (not part of the ABI).
 #pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,8 +64,14 @@ struct SampleParams {
   // Staged A operand: the locate of step k writes E[x_k] rows here
   // (a_stage_out), the tensor-core tile kernel of step k+1 loads them with TMA
   // (a_stage_in). Null where unused (first step, last step, SIMT path).
-  const void* a_stage_in;       // [B][r]
-  void* a_stage_out;            // [B][r]
+  const void* a_stage_in;       // [B] rows of r, a_stage_stride elements apart
+  void* a_stage_out;            // [B] rows of r, a_stage_stride elements apart
+  int32_t a_stage_stride;       // r for the Markov head
+  // RNN head: the bias rows are states, not E rows. Draft: row b of the
+  // current state at a_rows + b * a_rows_stride; final draw: the state of
+  // row j at a_rows + (b * K + j) * r (a_rows_stride = K * r). Null: Markov.
+  const void* a_rows;
+  int32_t a_rows_stride;
   // Group records: the chunks of a row are also combined per column group
   // (the contiguous token range one tile CTA covers), so that the locate scans
   // a few hundred group records and then the chunks of one group only.
@@ -139,6 +147,38 @@ struct StsParams {
   float* ece_all;        // [G]
   int32_t* status;
 };
+
+// RNN head (rnn.cu). One tensor-core GEMM kernel, two epilogues:
+//   kGemmBias: out[m][n] = A[m] . W[n] + bias[n]   (the hidden-state part of
+//              the gate inputs for every position, once per draft call);
+//   kGemmGru:  the gated update of one position; W is the packed step matrix
+//              (unit blocks of 32: reset, update, new-input, new-recurrent rows
+//              over [e ; s]) and the epilogue writes the new state.
+enum GemmEpilogue { kGemmBias = 0, kGemmGru = 1 };
+struct GemmParams {
+  int32_t M, N, Kd;
+  // kGemmBias
+  const float* bias;          // [N]
+  float* out;                 // [M][N]
+  // kGemmGru, producing the state of position p (1-based)
+  const float* gh;            // [B*K][3r]: W_ih[:, r:] . h + b_ih
+  const float* b_hh;          // [3r]
+  const __nv_bfloat16* s_prev;  // row b at s_prev + b * 2r (state half of the input rows)
+  __nv_bfloat16* s_next;        // row b at s_next + b * 2r
+  __nv_bfloat16* states;        // [B][K][r]
+  int32_t r, K, p;
+  int32_t* status;
+};
+cudaError_t launch_rnn_gemm(const GemmParams& g, int mode, const void* A, int64_t a_stride,
+                            const void* W, int64_t w_stride, cudaStream_t s);
+cudaError_t launch_rnn_init(const void* E, const int32_t* anchor, int32_t B, int32_t r, int32_t V,
+                            void* gru_in, int32_t* status, cudaStream_t s);
+cudaError_t launch_rnn_pack(const void* W_ih, const void* W_hh, int32_t r, int32_t d, void* W_step,
+                            cudaStream_t s);
+
+// 2-D or 3-D bfloat16 tensor map with 128-byte swizzle (draft_tc.cu).
+bool encode_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box);
 
 constexpr int kTileRows = 32;   // rows per sampling CTA
 constexpr int kTileCols = 256;  // tokens per sampling CTA (8 chunks of 32)

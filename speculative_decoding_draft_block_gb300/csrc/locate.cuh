@@ -40,7 +40,7 @@ __device__ __forceinline__ void stage_e_row(const SampleParams& p, int b, int to
   if (p.a_stage_out == nullptr) return;
   const int n16 = p.r * (int)sizeof(Tin) / 16;
   const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const Tin*>(p.E) + (size_t)tok * p.r);
-  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(p.a_stage_out) + (size_t)b * p.r);
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<Tin*>(p.a_stage_out) + (size_t)b * p.a_stage_stride);
   for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
 }
 
@@ -104,7 +104,7 @@ __device__ __forceinline__ void locate_row(const SampleParams& p, int b, int tid
   }
   const RowCtx c = make_row_ctx<Tin>(p, b);
   if (c.mode == kSkip) return;
-  const Tin* Erow = reinterpret_cast<const Tin*>(p.E) + (size_t)(c.a_token >= 0 ? c.a_token : 0) * r;
+  const Tin* Erow = bias_row<Tin>(p, b, c);
   float erow[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {

@@ -88,6 +88,19 @@ __device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
   return c;
 }
 
+// The r-vector whose product with P is the row's bias: E[a_token] for the
+// Markov head; for the RNN head the state of the step (draft) or of row zk
+// (final draw). Only meaningful when c.a_token >= 0.
+template <typename Tin>
+__device__ __forceinline__ const Tin* bias_row(const SampleParams& p, int b, const RowCtx& c) {
+  if (p.a_rows != nullptr) {
+    int j = p.src == 0 ? 0 : c.zk;
+    j = j < 0 ? 0 : (j >= p.K ? p.K - 1 : j);
+    return reinterpret_cast<const Tin*>(p.a_rows) + (size_t)b * p.a_rows_stride + (size_t)j * p.r;
+  }
+  return reinterpret_cast<const Tin*>(p.E) + (size_t)(c.a_token >= 0 ? c.a_token : 0) * p.r;
+}
+
 // Chunk reference n = rint(max_j z_j * g.hi) over finite z; kEmptyRef if none.
 __device__ __forceinline__ int chunk_ref_from_max(float amax) {
   return amax == kNegInf ? kEmptyRef : (int)rintf(amax);

@@ -35,7 +35,9 @@ INPUT_KEYS = ("base_logits", "target_logits", "E", "P", "anchor", "temperature",
 
 class DeviceCycle:
     def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0,
-                 token_major_projection=True, initial_budget=None):
+                 token_major_projection=True, initial_budget=None, rnn_weights=None):
+        """``rnn_weights`` (dict w_ih, w_hh as bfloat16 bits, b_ih, b_hh float32)
+        selects the RNN head; its step matrix is packed once here."""
         self.inp = inp
         self.device = torch.device(device)
         self.mode = mode
@@ -70,6 +72,18 @@ class DeviceCycle:
         wv = _lib.ds_verify_workspace_bytes(B, K, V, r)
         if wd == 0 or wv == 0:
             raise ValueError("shape not supported by the library")
+        self.rnn = None
+        if rnn_weights is not None:
+            wr = _lib.ds_rnn_workspace_bytes(B, K, r)
+            if wr == 0:
+                raise ValueError("shape not supported by the RNN head")
+            wd = (wd + 255) // 256 * 256 + wr
+            rw = {k: _to_device(rnn_weights[k], dev) for k in ("w_ih", "w_hh", "b_ih", "b_hh")}
+            rw["h"] = self.t["h"]
+            rw["w_step"] = torch.empty((4 * r, 2 * r), dtype=rw["w_ih"].dtype, device=dev)
+            check(_lib.ds_rnn_pack_weights(rw["w_ih"], rw["w_hh"], rw["w_step"]), "ds_rnn_pack_weights")
+            rw["states"] = torch.zeros((B, K, r), dtype=rw["w_ih"].dtype, device=dev)
+            self.rnn = rw
         self.ws_draft = torch.empty((wd,), dtype=torch.uint8, device=dev)
         self.ws_verify = torch.empty((wv,), dtype=torch.uint8, device=dev)
         # weight layout step, once per model: the token-major copy of P
@@ -84,7 +98,8 @@ class DeviceCycle:
         t = self.t
         check(_lib.ds_draft_block(t["base_logits"], t["E"], t["P"], t["anchor"], t["temperature"],
                                   seed, self.draft_tokens, self.q_token, self.q_stats,
-                                  self.ws_draft, self.status, stream, P_t=self.P_t), "ds_draft_block")
+                                  self.ws_draft, self.status, stream, P_t=self.P_t, rnn=self.rnn),
+              "ds_draft_block")
 
     def schedule(self, stream=None):
         t = self.t
@@ -102,7 +117,8 @@ class DeviceCycle:
         check(_lib.ds_verify(t["target_logits"], t["base_logits"], t["E"], t["P"], t["anchor"],
                              self.draft_tokens, self.q_token, self.q_stats, self.sched_len,
                              t["temperature"], seed, self.out_tokens, self.accept_count,
-                             self.num_emitted, self.ws_verify, self.status, stream, P_t=self.P_t),
+                             self.num_emitted, self.ws_verify, self.status, stream, P_t=self.P_t,
+                             states=None if self.rnn is None else self.rnn["states"]),
               "ds_verify")
 
     def run(self, seed, stream=None):
@@ -133,4 +149,6 @@ class DeviceCycle:
             "out_tokens": self.out_tokens.cpu().numpy().astype(np.int64),
             "accept_count": self.accept_count.cpu().numpy().astype(np.int64),
             "num_emitted": self.num_emitted.cpu().numpy().astype(np.int64),
+            "states": None if self.rnn is None else
+            self.rnn["states"].cpu().view(torch.int16).numpy().view(np.uint16),
         }

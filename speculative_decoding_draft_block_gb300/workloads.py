@@ -207,3 +207,23 @@ def make_sts_inputs(N, K, seed=7, t_true=(1.2, 2.5), noise=0.25):
 def sts_grid(lo=0.05, hi=5.0, n=256):
     """Candidate STS temperatures: n log-spaced float32 values in [lo, hi]."""
     return np.geomspace(lo, hi, n).astype(np.float32)
+
+
+def make_rnn_weights(r, d, seed=11, bf16=True):
+    """Random weights of the RNN head's gated update (deterministic in the seed).
+
+    W_ih [3r, r + d]: embedding columns ~ N(0, 1), hidden columns ~ N(0, 1/d);
+    W_hh [3r, r] ~ N(0, 4/r); biases ~ N(0, 0.1^2) (float32). The scales put
+    the gate pre-activations at O(1) for the embeddings and hidden states of
+    the workloads above. Weights are bfloat16 bit patterns when ``bf16``.
+    """
+    ss = np.random.SeedSequence(seed)
+    rng = np.random.Generator(np.random.PCG64(ss))
+    w_ih = np.empty((3 * r, r + d), dtype=np.float32)
+    w_ih[:, :r] = rng.standard_normal((3 * r, r), dtype=np.float32)
+    w_ih[:, r:] = rng.standard_normal((3 * r, d), dtype=np.float32) / np.float32(np.sqrt(d))
+    w_hh = rng.standard_normal((3 * r, r), dtype=np.float32) * np.float32(2.0 / np.sqrt(r))
+    b_ih = (rng.standard_normal(3 * r, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    b_hh = (rng.standard_normal(3 * r, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    conv = to_bf16_bits if bf16 else (lambda a: a)
+    return {"w_ih": conv(w_ih), "w_hh": conv(w_hh), "b_ih": b_ih, "b_hh": b_hh}

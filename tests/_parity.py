@@ -23,7 +23,7 @@ REL_TOL = 2e-3
 
 ROW_KEYS = ("base_logits", "target_logits", "anchor", "temperature", "h")
 GPU_ROW_KEYS = ("tokens", "q_token", "conf", "survival", "L", "out_tokens", "accept_count",
-                "num_emitted")
+                "num_emitted", "states")
 
 
 def subset(inp, g, rows):
@@ -34,7 +34,8 @@ def subset(inp, g, rows):
         si[k] = inp[k][rows]
     sg = dict(g)
     for k in GPU_ROW_KEYS:
-        sg[k] = g[k][rows]
+        if g.get(k) is not None:
+            sg[k] = g[k][rows]
     return si, sg
 
 
@@ -47,6 +48,50 @@ def compare_draft(inp, g, seed, request_ids=None):
     draws = mism.size
     rep = {"draws": int(draws), "mismatches": int(mism.sum()), "near_ties": int(near.sum()),
            "unexplained": int((mism & ~near).sum())}
+    ok = ~mism
+    rel = np.abs(g["q_token"][ok] - o["q_token"][ok]) / np.maximum(o["q_token"][ok], 1e-300)
+    rep["q_max_rel"] = float(rel.max()) if rel.size else 0.0
+    return rep, o
+
+
+# The kernel sums each gate pre-activation in float32 over 2r + d products
+# (magnitudes summing to ~10-20 for these weights: an error up to ~1e-5), and
+# the gates pass it on with slope <= 1. So each stored bfloat16 state must be
+# a correct rounding of a value within STATE_ABS of the float64 state:
+# |s_gpu - s| <= ulp(s_gpu) / 2 + STATE_ABS. Where the rounding differs from
+# the oracle's (a value near a rounding boundary, or a tiny value whose ulp is
+# below the float32 error), at most STATE_DIFF_BUDGET of the elements.
+STATE_ABS = 1e-5
+STATE_DIFF_BUDGET = 1e-2
+
+
+def compare_draft_rnn(inp, g, seed, rnn, request_ids=None):
+    """RNN head: every state and every draw checked on its own.
+
+    The oracle is teacher-forced with the GPU's tokens and states: state k is
+    recomputed from the GPU's state k-1, and draw k uses the GPU's state k.
+    Every stored state must be a bfloat16 rounding of a value within STATE_ABS
+    of the float64 state; at most STATE_DIFF_BUDGET of them may round otherwise
+    than the oracle.
+    """
+    from oracle.bf16 import as_f64
+    o = oracle.rnn_draft_block(inp["base_logits"], inp["E"], inp["P"], inp["anchor"],
+                               inp["temperature"], seed, inp["h"], rnn["w_ih"], rnn["w_hh"],
+                               rnn["b_ih"], rnn["b_hh"], bf16_state=inp["bf16"],
+                               prev_tokens=g["tokens"], prev_states=g["states"],
+                               request_ids=request_ids)
+    gs = as_f64(g["states"])
+    diff = gs != o["states"]
+    _, e = np.frexp(gs)
+    half_ulp = np.where(gs == 0, 0.0, np.ldexp(0.5, e - 8))   # bfloat16: 8 significant bits
+    excess = np.abs(gs - o["states_pre"]) - half_ulp
+    mism = o["tokens"] != g["tokens"]
+    near = o["margin"] < NEAR_TIE
+    rep = {"draws": int(mism.size), "mismatches": int(mism.sum()), "near_ties": int(near.sum()),
+           "unexplained": int((mism & ~near).sum()),
+           "state_elems": int(diff.size), "state_diffs": int(diff.sum()),
+           "state_unexplained": int((excess > STATE_ABS).sum()),
+           "state_max_excess": float(excess.max())}
     ok = ~mism
     rel = np.abs(g["q_token"][ok] - o["q_token"][ok]) / np.maximum(o["q_token"][ok], 1e-300)
     rep["q_max_rel"] = float(rel.max()) if rel.size else 0.0
@@ -70,7 +115,8 @@ def compare_schedule(inp, g):
 
 def compare_verify(inp, g, seed, request_ids=None):
     o = oracle.verify(inp["target_logits"], inp["base_logits"], inp["E"], inp["P"], inp["anchor"],
-                      g["tokens"], g["L"], inp["temperature"], seed, request_ids=request_ids)
+                      g["tokens"], g["L"], inp["temperature"], seed, request_ids=request_ids,
+                      states=g.get("states"))
     bad_req = np.nonzero((o["accept_count"] != g["accept_count"]) |
                          np.any(o["out_tokens"] != g["out_tokens"], axis=1))[0]
     decisions = sum(len(d) for d in o["decisions"])
@@ -85,8 +131,9 @@ def compare_verify(inp, g, seed, request_ids=None):
     return rep, o
 
 
-def assert_parity(inp, g, seed, check_schedule=True, check_verify=True, rows=None):
-    """Check a GPU cycle against the oracle; ``rows`` limits draft/verify to some requests."""
+def assert_parity(inp, g, seed, check_schedule=True, check_verify=True, rows=None, rnn=None):
+    """Check a GPU cycle against the oracle; ``rows`` limits draft/verify to some requests;
+    ``rnn`` (the head's weights) selects the RNN head."""
     if check_schedule:
         rs, _ = compare_schedule(inp, g)
         assert rs["conf_max_rel"] < REL_TOL and rs["surv_max_rel"] < REL_TOL, rs
@@ -97,7 +144,12 @@ def assert_parity(inp, g, seed, check_schedule=True, check_verify=True, rows=Non
     if rows is not None:
         inp, g = subset(inp, g, rows)
         rid = np.asarray(rows)
-    rd, od = compare_draft(inp, g, seed, request_ids=rid)
+    if rnn is not None:
+        rd, od = compare_draft_rnn(inp, g, seed, rnn, request_ids=rid)
+        assert rd["state_unexplained"] == 0, rd
+        assert rd["state_diffs"] <= STATE_DIFF_BUDGET * rd["state_elems"], rd
+    else:
+        rd, od = compare_draft(inp, g, seed, request_ids=rid)
     assert rd["unexplained"] == 0, rd
     assert rd["mismatches"] <= MISMATCH_BUDGET * rd["draws"], rd
     assert rd["q_max_rel"] < REL_TOL, rd

@@ -81,6 +81,20 @@ def test_host_validation_rejects_without_launching(lib):
     assert lib.ds_verify(ctypes.byref(_lib.VerifyArgs()), None) == 1
     assert lib.ds_confidence_schedule(ctypes.byref(_lib.SchedArgs()), None) == 1
     assert lib.ds_sts_fit(ctypes.byref(_lib.StsArgs()), None) == 1
+    # RNN head: checked on the host before any device work (fake, aligned, never dereferenced)
+    fake = 1 << 20
+    kw = dict(B=4, K=3, V=1024, r=64, base_logits=fake, E=fake, P=fake, anchor=fake,
+              temperature=fake, draft_tokens=fake, q_token=fake, q_stats=fake, status=fake,
+              workspace=fake, workspace_bytes=1 << 40, d=128, h=fake, rnn_w_ih=fake,
+              rnn_w_step=fake, rnn_b_ih=fake, rnn_b_hh=fake, states=fake)
+    assert lib.ds_draft_block(ctypes.byref(_lib.DraftArgs(dtype=0, head=1, **kw)), None) == 2
+    assert lib.ds_draft_block(ctypes.byref(_lib.DraftArgs(dtype=1, head=7, **kw)), None) == 1
+    kw["d"] = 100
+    assert lib.ds_draft_block(ctypes.byref(_lib.DraftArgs(dtype=1, head=1, **kw)), None) == 1
+    assert _lib.ds_rnn_workspace_bytes(128, 16, 256) >= 128 * 16 * 768 * 4 + 2 * 128 * 512 * 2
+    assert _lib.ds_rnn_workspace_bytes(128, 16, 96) == 0                   # r % 64 != 0
+    assert lib.ds_rnn_pack_weights(fake, fake, 64, 128, 0, fake, None) == 2  # f32 unsupported
+    assert lib.ds_rnn_pack_weights(fake, fake, 96, 128, 1, fake, None) == 1
     a = _lib.StsArgs(N=4, K=2, n_grid=8, n_bins=10)      # sizes fine, pointers missing
     assert lib.ds_sts_fit(ctypes.byref(a), None) == 1
     assert _lib.ds_status_string(7) == "non-finite logit or empty distribution"
