@@ -97,14 +97,26 @@ class ClockSampler:
 
 # ---- workload accounting ---------------------------------------------------------
 
-def draft_algorithmic(inp):
+def draft_algorithmic(inp, rnn=False):
     """HBM bytes and tensor FLOPs of one draft step (one block position): the
     base-logit rows z_k (B*V), the projection P (r*V, read every step), the
-    conditioning E rows (B*r) and the outputs (token, q, stats: 24 B per row)."""
+    conditioning E rows (B*r) and the outputs (token, q, stats: 24 B per row).
+    RNN head, per step in addition: the packed step matrix (4r x 2r), the input
+    rows [e ; s] (B x 2r), the hidden-state gate inputs of the position
+    (B x 3r float32) and the state written twice (B x r); per call the
+    hidden-state GEMM (h: B*K*d, W_ih's hidden columns: 3r*d, out B*K*3r
+    float32), spread over the K steps."""
     B, V, r = inp["B"], inp["V"], inp["r"]
     eb = 2 if inp["bf16"] else 4
     by = B * V * eb + r * V * eb + B * r * eb + B * (4 + 4 + 16)
-    return by, 2.0 * B * r * V
+    fl = 2.0 * B * r * V
+    if rnn:
+        K, d = inp["K"], inp["d"]
+        by += 4 * r * 2 * r * eb + B * 2 * r * eb + B * 3 * r * 4 + 2 * B * r * eb
+        fl += 2.0 * B * 4 * r * 2 * r
+        by += (B * K * d * eb + 3 * r * d * eb + B * K * 3 * r * 4) / K
+        fl += 2.0 * B * K * 3 * r * d / K
+    return by, fl
 
 
 def verify_algorithmic(inp, L, n_final_residual, n_final_bonus):
@@ -117,10 +129,13 @@ def verify_algorithmic(inp, L, n_final_residual, n_final_bonus):
     return by, 2.0 * n_final_residual * r * V
 
 
-def gpu_launches_per_cycle(w):
-    """Kernels one cycle launches: draft (tile and locate per position),
-    schedule (confidence, scheduler), verify (rows, finalize, tile, locate)."""
-    return 2 * w.K + 2 + 4
+def gpu_launches_per_cycle(w, rnn=False):
+    """Kernels one cycle launches: draft (tile and locate per position; the RNN
+    head adds the hidden-state GEMM, the first input rows and one update per
+    position), schedule (confidence, scheduler), verify (rows, finalize, tile,
+    locate)."""
+    draft = 3 * w.K + 2 if rnn else 2 * w.K
+    return draft + 2 + 4
 
 
 # Per-step inputs (copied host -> device every step in the end-to-end run).
@@ -130,8 +145,8 @@ STEP_KEYS = ("base_logits", "target_logits", "anchor", "temperature", "h")
 
 
 # Sources of the draft-step kernels (tile + locate) and everything they include.
-STEP_SOURCES = ("draft_tc.cu", "sample.cu", "common.cuh", "fastpath.cuh", "sampling.cuh",
-                "sm100.cuh", "internal.h", "philox.h")
+STEP_SOURCES = ("draft_tc.cu", "sample.cu", "locate.cuh", "common.cuh", "fastpath.cuh",
+                "sampling.cuh", "sm100.cuh", "internal.h", "philox.h")
 
 
 def sources_digest():
@@ -163,19 +178,27 @@ def recorded_traffic(workload):
 
 # ---- CPU oracle timing ------------------------------------------------------------
 
-def oracle_sample(inp, seed, n_req):
+def oracle_sample(inp, seed, n_req, rnn_w=None):
     """Time the oracle's cycle on the first n_req requests (schedule on all)."""
     import numpy as np
     import oracle
     rows = np.arange(n_req)
     t0 = time.perf_counter()
-    d = oracle.draft_block(inp["base_logits"][rows], inp["E"], inp["P"], inp["anchor"][rows],
-                           inp["temperature"][rows], seed)
+    states = None
+    if rnn_w is not None:
+        d = oracle.rnn_draft_block(inp["base_logits"][rows], inp["E"], inp["P"], inp["anchor"][rows],
+                                   inp["temperature"][rows], seed, inp["h"][rows], rnn_w["w_ih"],
+                                   rnn_w["w_hh"], rnn_w["b_ih"], rnn_w["b_hh"], inp["bf16"])
+        states = d["states"]
+    else:
+        d = oracle.draft_block(inp["base_logits"][rows], inp["E"], inp["P"], inp["anchor"][rows],
+                               inp["temperature"][rows], seed)
     c = oracle.confidence(inp["h"][rows], inp["E"], inp["anchor"][rows], d["tokens"], inp["w_h"],
                           inp["w_e"], inp["conf_bias"], inp["sts_temp"])
     sch = oracle.schedule(oracle.survival(c), inp["sps"])
     oracle.verify(inp["target_logits"][rows], inp["base_logits"][rows], inp["E"], inp["P"],
-                  inp["anchor"][rows], d["tokens"], sch["L"], inp["temperature"][rows], seed)
+                  inp["anchor"][rows], d["tokens"], sch["L"], inp["temperature"][rows], seed,
+                  states=states)
     dt = time.perf_counter() - t0
     return dt, n_req * inp["K"]
 
@@ -194,12 +217,12 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def cpu_baseline(inp, seed, budget_s=12.0):
+def cpu_baseline(inp, seed, budget_s=12.0, rnn_w=None):
     n_req = 1
-    dt, toks = oracle_sample(inp, seed, n_req)
+    dt, toks = oracle_sample(inp, seed, n_req, rnn_w)
     if dt < budget_s / 4:
         n_req = max(1, min(inp["B"], int(budget_s / max(dt, 1e-3))))
-        dt, toks = oracle_sample(inp, seed, n_req)
+        dt, toks = oracle_sample(inp, seed, n_req, rnn_w)
     return {"value": toks / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": "%d of %d requests x K=%d positions: float64 draft (bias matmul + exp/cumsum "
                       "per position), confidence + schedule, verify; %.1f s" %
@@ -391,6 +414,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--head", choices=("markov", "rnn"), default="markov",
+                    help="sequential head of the draft block (default: Markov)")
     ap.add_argument("--part", choices=("cycle", "sts"), default="cycle",
                     help="cycle: draft+schedule+verify (default); sts: the STS calibration fit")
     args = ap.parse_args()
@@ -420,7 +445,12 @@ def main():
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
     inp = make_inputs(w)
-    cyc = DeviceCycle(inp, device=dev, mode=args.mode)
+    rnn = args.head == "rnn"
+    rnn_w = None
+    if rnn:
+        from speculative_decoding_draft_block_gb300.workloads import make_rnn_weights
+        rnn_w = make_rnn_weights(w.r, w.d)
+    cyc = DeviceCycle(inp, device=dev, mode=args.mode, rnn_weights=rnn_w)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
     seed0 = 0x5EED0000 + 7919 * rank
@@ -463,11 +493,11 @@ def main():
     peaks, peak_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     tc = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    d_by, d_fl = draft_algorithmic(inp)          # per draft step
+    d_by, d_fl = draft_algorithmic(inp, rnn)     # per draft step
     d_ms = float(per[:, 0].mean()) / Kb          # average draft step (tile + locate kernels)
     t_hbm = d_by / (hbm * 1e9)
     t_tc = d_fl / (tc * 1e12)
-    traffic = recorded_traffic(w.name)
+    traffic = None if rnn else recorded_traffic(w.name)
     if t_hbm >= t_tc:
         achieved = d_by / (d_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -476,7 +506,8 @@ def main():
         achieved = d_fl / (d_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tc, "unit": "TFLOP/s",
                 "frac": achieved / tc, "traffic": traffic}
-    roof.update({"kernel": "draft step = tile_tc_kernel + sample_locate_kernel (K per ds_draft_block)",
+    roof.update({"kernel": "draft step = tile_tc_kernel + sample_locate_kernel (K per ds_draft_block)"
+                 + (" + rnn_gemm_kernel<update> (+ 1/K of the hidden-state GEMM)" if rnn else ""),
                  "peak_source": peak_src, "peak_kind": "burst copy (hbm_gbs)",
                  "algorithmic_bytes_per_step": d_by, "algorithmic_flops_per_step": d_fl,
                  "t_roof_us": 1e6 * max(t_hbm, t_tc), "t_meas_us": 1e3 * d_ms})
@@ -494,7 +525,8 @@ def main():
                    "parallelism": "replicas" if ws > 1 else "single",
                    "l2": "flushed between steps (256 MiB write, outside the timed events); "
                          "inputs also exceed L2",
-                   "mode": "greedy_earlystop" if args.mode == 0 else "fixed_k"},
+                   "mode": "greedy_earlystop" if args.mode == 0 else "fixed_k",
+                   "head": args.head},
         "components_ms": {"draft": float(per[:, 0].mean()), "schedule": float(per[:, 1].mean()),
                           "verify": float(per[:, 2].mean())},
         "emitted_tokens_per_s": ws * float(res["num_emitted"].sum()) / (total_s / K),
@@ -502,7 +534,7 @@ def main():
         "mean_sched_len": float(res["L"].mean()), "mean_accepted": float(res["accept_count"].mean()),
         "cycle_roofline_us": cycle_roof_us, "cycle_roofline_frac": cycle_roof_us / (1e3 * cycle_ms.mean()),
         "roofline": roof,
-        "gpu_launches": K * (gpu_launches_per_cycle(w)),
+        "gpu_launches": K * (gpu_launches_per_cycle(w, rnn)),
         "wall_s": wall,
         "clocks": sampler.summary(),
     }
@@ -540,7 +572,7 @@ def main():
         cyc.check_status()
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, 0x5EED0000)
+        line["cpu_baseline"] = cpu_baseline(inp, 0x5EED0000, rnn_w=rnn_w)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

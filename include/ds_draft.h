@@ -170,7 +170,7 @@ size_t ds_rnn_workspace_bytes(int32_t B, int32_t K, int32_t r);
 /*
  * Weight layout of the RNN head, once per model (like ds_transpose_projection):
  * packs W_ih [3r][r + d] and W_hh [3r][r] into W_step [4r][2r] so that each
- * block of 32 state units has its reset, update, new-input and new-recurrent
+ * block of 16 state units has its reset, update, new-input and new-recurrent
  * rows over [embedding ; state] next to each other. Bit-exact copy (zeros
  * where a gate does not read an input). bfloat16 only; r, d multiples of 64.
  */

@@ -76,7 +76,7 @@ DraftLayout draft_layout(int32_t B, int32_t V, int32_t r) {
 size_t draft_ws(int32_t B, int32_t V, int32_t r) { return draft_layout(B, V, r).total; }
 
 // RNN head workspace, after the draft workspace: the hidden-state part of the
-// gate inputs for every position (f32 [B*K][3r]) and two input-row buffers
+// gate inputs for every position (f32 [K][3r][B]) and two input-row buffers
 // [e ; s] (bf16 [2][B][2r]), alternating by position parity.
 struct RnnLayout {
   size_t gh, gru_in, total;
@@ -152,33 +152,34 @@ ds_status draft_rnn(const ds_draft_args* a, SampleParams& p, char* rw, char* ws,
 
   GemmParams g;
   memset(&g, 0, sizeof(g));
-  g.M = B * K;
+  g.B = B;
+  g.K = K;
   g.N = 3 * r;
   g.Kd = a->d;
   g.bias = a->rnn_b_ih;
   g.out = gh;
   g.status = a->status;
-  if (launch_rnn_gemm(g, kGemmBias, a->h, a->d, w_ih + r, (int64_t)r + a->d, s) != cudaSuccess)
+  if (launch_rnn_gemm(g, kGemmBias, a->h, w_ih + r, (int64_t)r + a->d, s) != cudaSuccess)
     return DS_ERR_CUDA;
   if (launch_rnn_init(a->E, a->anchor, B, r, a->V, in[0], a->status, s) != cudaSuccess)
     return DS_ERR_CUDA;
 
   GemmParams u;
   memset(&u, 0, sizeof(u));
-  u.M = B;
+  u.B = B;
+  u.K = K;
   u.N = 4 * r;
   u.Kd = 2 * r;
   u.gh = gh;
   u.b_hh = a->rnn_b_hh;
   u.states = reinterpret_cast<__nv_bfloat16*>(a->states);
   u.r = r;
-  u.K = K;
   u.status = a->status;
   auto update = [&](int pos) {  // s_pos from the input rows of position pos - 1
     u.p = pos;
     u.s_prev = in[(pos - 1) & 1] + r;
     u.s_next = in[pos & 1] + r;
-    return launch_rnn_gemm(u, kGemmGru, in[(pos - 1) & 1], 2 * r, a->rnn_w_step, 2 * r, s);
+    return launch_rnn_gemm(u, kGemmGru, in[(pos - 1) & 1], a->rnn_w_step, 2 * r, s);
   };
   if (update(1) != cudaSuccess) return DS_ERR_CUDA;
   p.a_stage_stride = 2 * r;

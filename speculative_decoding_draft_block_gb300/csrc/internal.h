@@ -156,21 +156,21 @@ struct StsParams {
 //              over [e ; s]) and the epilogue writes the new state.
 enum GemmEpilogue { kGemmBias = 0, kGemmGru = 1 };
 struct GemmParams {
-  int32_t M, N, Kd;
+  int32_t B, K, N, Kd;          // requests, positions, output columns, reduction length
   // kGemmBias
-  const float* bias;          // [N]
-  float* out;                 // [M][N]
+  const float* bias;            // [N]
+  float* out;                   // gh[K][N][B]
   // kGemmGru, producing the state of position p (1-based)
-  const float* gh;            // [B*K][3r]: W_ih[:, r:] . h + b_ih
-  const float* b_hh;          // [3r]
+  const float* gh;              // gh[K][3r][B]: W_ih[:, r:] . h + b_ih
+  const float* b_hh;            // [3r]
   const __nv_bfloat16* s_prev;  // row b at s_prev + b * 2r (state half of the input rows)
   __nv_bfloat16* s_next;        // row b at s_next + b * 2r
   __nv_bfloat16* states;        // [B][K][r]
-  int32_t r, K, p;
+  int32_t r, p;
   int32_t* status;
 };
-cudaError_t launch_rnn_gemm(const GemmParams& g, int mode, const void* A, int64_t a_stride,
-                            const void* W, int64_t w_stride, cudaStream_t s);
+cudaError_t launch_rnn_gemm(const GemmParams& g, int mode, const void* A, const void* W,
+                            int64_t w_stride, cudaStream_t s);
 cudaError_t launch_rnn_init(const void* E, const int32_t* anchor, int32_t B, int32_t r, int32_t V,
                             void* gru_in, int32_t* status, cudaStream_t s);
 cudaError_t launch_rnn_pack(const void* W_ih, const void* W_hh, int32_t r, int32_t d, void* W_step,

@@ -75,13 +75,13 @@ def test_rnn_pack_is_exact(ds):
     torch.cuda.synchronize()
     got = out.cpu().view(torch.int16).numpy().view(np.uint16)
     want = np.zeros((4 * r, 2 * r), dtype=np.uint16)
-    for t in range(r // 32):
-        u = np.arange(32 * t, 32 * t + 32)
-        blk = want[128 * t:128 * t + 128]
-        blk[0:32, :r], blk[0:32, r:] = w["w_ih"][u, :r], w["w_hh"][u]
-        blk[32:64, :r], blk[32:64, r:] = w["w_ih"][r + u, :r], w["w_hh"][r + u]
-        blk[64:96, :r] = w["w_ih"][2 * r + u, :r]
-        blk[96:128, r:] = w["w_hh"][2 * r + u]
+    for t in range(r // 16):                 # blocks of 16 units, 64 rows each
+        u = np.arange(16 * t, 16 * t + 16)
+        blk = want[64 * t:64 * t + 64]
+        blk[0:16, :r], blk[0:16, r:] = w["w_ih"][u, :r], w["w_hh"][u]
+        blk[16:32, :r], blk[16:32, r:] = w["w_ih"][r + u, :r], w["w_hh"][r + u]
+        blk[32:48, :r] = w["w_ih"][2 * r + u, :r]
+        blk[48:64, r:] = w["w_hh"][2 * r + u]
     assert np.array_equal(got, want)
 
 
