@@ -126,7 +126,8 @@ ds_status ds_philox_fill(const uint32_t* ctr, uint32_t key0, uint32_t key1, uint
  *     r = sigmoid(g_i^r + g_h^r), u = sigmoid(g_i^u + g_h^u),
  *     n = tanh(g_i^n + r * g_h^n), s_k = (1 - u) * n + u * s_{k-1},
  * each s_k rounded to bfloat16 (nearest even), the storage type. bfloat16
- * only, r % 64 == 0, d % 64 == 0; the workspace is
+ * only, 64 <= r <= 256 with r % 64 == 0, d % 64 == 0 (DS_ERR_UNSUPPORTED
+ * otherwise); the workspace is
  * ds_draft_workspace_bytes(B, K, V, r) + ds_rnn_workspace_bytes(B, K, r)
  * bytes. The states are returned for ds_verify.
  */

@@ -82,8 +82,10 @@ struct RnnLayout {
   size_t gh, gru_in, total;
 };
 
+// The RNN head runs the tensor-core tile kernel, whose A operand (128 rows of
+// r bf16) is one 64 KB shared-memory block: 64 <= r <= 256, r % 64 == 0.
 bool rnn_shape_ok(int32_t B, int32_t K, int32_t r) {
-  return B >= 1 && K >= 1 && K <= 64 && (int64_t)B * K <= 16384 && r >= 64 && r <= 1024 && r % 64 == 0;
+  return B >= 1 && K >= 1 && K <= 64 && (int64_t)B * K <= 16384 && r >= 64 && r <= 256 && r % 64 == 0;
 }
 
 RnnLayout rnn_layout(int32_t B, int32_t K, int32_t r) {

@@ -91,6 +91,9 @@ def test_host_validation_rejects_without_launching(lib):
     assert lib.ds_draft_block(ctypes.byref(_lib.DraftArgs(dtype=1, head=7, **kw)), None) == 1
     kw["d"] = 100
     assert lib.ds_draft_block(ctypes.byref(_lib.DraftArgs(dtype=1, head=1, **kw)), None) == 1
+    kw["d"], kw["r"] = 128, 512                  # above the tensor-core tile's r <= 256
+    assert lib.ds_draft_block(ctypes.byref(_lib.DraftArgs(dtype=1, head=1, **kw)), None) == 2
+    assert _lib.ds_rnn_workspace_bytes(128, 16, 512) == 0
     assert _lib.ds_rnn_workspace_bytes(128, 16, 256) >= 128 * 16 * 768 * 4 + 2 * 128 * 512 * 2
     assert _lib.ds_rnn_workspace_bytes(128, 16, 96) == 0                   # r % 64 != 0
     assert lib.ds_rnn_pack_weights(fake, fake, 64, 128, 0, fake, None) == 2  # f32 unsupported

@@ -214,6 +214,20 @@ def test_minimal_shapes(ds):
     _parity.assert_parity(inp, g, SEED)
 
 
+@pytest.mark.parametrize("B,K,V,r,bf16,rows", [
+    (8, 64, 4096, 64, True, None),      # K at its limit: 64 sequential steps (tensor-core tile)
+    (256, 64, 1024, 64, True, 24),      # B*K at its limit (16384 drafted tokens)
+    (5, 3, 2048, 1024, True, None),     # r at its limit (SIMT tile: A rows wider than 256)
+    (4, 2, 1024, 1024, False, None),    # r at its limit, float32
+])
+def test_limit_shapes(ds, B, K, V, r, bf16, rows):
+    inp = _ragged(bf16, (0.0, 0.6, 1.0), 29 + K, B=B, K=K, V=V, r=r, d=64)
+    _, g = _run(inp)
+    sel = None if rows is None else np.linspace(0, B - 1, rows).astype(np.int64)
+    rep = _parity.assert_parity(inp, g, SEED, rows=sel)
+    assert rep["draft"]["draws"] == (B if rows is None else rows) * K
+
+
 def test_device_errors_are_reported(ds):
     from speculative_decoding_draft_block_gb300 import _lib
     from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
