@@ -23,6 +23,7 @@ sys.path.insert(0, ROOT)
 METRIC = "draft+verify tokens/s at B=128,K=16,V=151936; % of HBM/tensor roofline"
 DEFAULT_WORKLOAD = "B128_K16_V151936"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 8000.0   # nominal HBM3e figure, for the second fraction the line reports
 
 
 def load_peaks():
@@ -506,6 +507,8 @@ def main():
         achieved = d_fl / (d_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tc, "unit": "TFLOP/s",
                 "frac": achieved / tc, "traffic": traffic}
+    if roof["unit"] == "GB/s":
+        roof["frac_nominal"] = roof["achieved"] / NOMINAL_HBM_GBS
     roof.update({"kernel": "draft step = tile_tc_kernel + sample_locate_kernel (K per ds_draft_block)"
                  + (" + rnn_gemm_kernel<update> (+ 1/K of the hidden-state GEMM)" if rnn else ""),
                  "peak_source": peak_src, "peak_kind": "burst copy (hbm_gbs)",
