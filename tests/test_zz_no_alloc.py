@@ -73,3 +73,33 @@ def test_static_scratch_rejects_oversized_calls(lib):
     assert lib.ds_verify_workspace_bytes(B, K, V, r) > limit
     a = lib.VerifyArgs(B=B, K=K, V=V, r=r, dtype=1)
     assert L.ds_verify_static(ctypes.byref(a), None) == 3      # DS_ERR_WORKSPACE, nothing launched
+
+
+def test_static_scratch_with_rnn_states(lib):
+    """The RNN head's states reach the residual draw through the static entry point too."""
+    from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
+    from speculative_decoding_draft_block_gb300.workloads import make_rnn_weights
+    inp = _inputs()
+    cyc = DeviceCycle(inp, rnn_weights=make_rnn_weights(inp["r"], inp["d"], seed=9))
+    cyc.reset_status()
+    cyc.draft(SEED + 1)
+    cyc.schedule()
+    cyc.check_status()
+    import torch
+    t = cyc.t
+    outs = []
+    for static in (False, True):
+        out = torch.full_like(cyc.out_tokens, -7)
+        acc = torch.full_like(cyc.accept_count, -7)
+        nem = torch.full_like(cyc.num_emitted, -7)
+        cyc.reset_status()
+        args = (t["target_logits"], t["base_logits"], t["E"], t["P"], t["anchor"], cyc.draft_tokens,
+                cyc.q_token, cyc.q_stats, cyc.sched_len, t["temperature"], SEED + 1, out, acc, nem)
+        if static:
+            code = lib.ds_verify_static(*args, cyc.status, P_t=cyc.P_t, states=cyc.rnn["states"])
+        else:
+            code = lib.ds_verify(*args, cyc.ws_verify, cyc.status, P_t=cyc.P_t, states=cyc.rnn["states"])
+        assert code == 0
+        assert lib.ds_check_status(cyc.status) == 0
+        outs.append((out.cpu().numpy(), acc.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
