@@ -404,6 +404,52 @@ def run_sts(args, rank, ws, local):
         print(json.dumps(line), flush=True)
 
 
+def time_graph_replays(args, inp, dev, rnn_w, seed0, flush, stream, ws, per):
+    """The cycle captured once (Philox key and scheduler ring on the device, the
+    key advanced inside the graph) and timed as K replays with CUDA events; the
+    per-call split and the draft-step roofline come from the launched calls."""
+    import numpy as np
+    import torch
+    from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
+    K = args.steps
+    gc = DeviceCycle(inp, device=dev, mode=args.mode, rnn_weights=rnn_w, device_seed=True)
+    gc.set_seed(seed0)
+    gc.run(0)
+    torch.cuda.synchronize(dev)
+    gc.reset_status()
+    graph = torch.cuda.CUDAGraph()
+    failed = None
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                gc.run(0)
+                gc.seed_dev[0].add_(1)
+        torch.cuda.synchronize(dev)
+    except Exception as ex:  # noqa: BLE001 - reported in the line, timing falls back
+        failed = "%s: %s" % (type(ex).__name__, str(ex)[:200])
+    # every rank takes the same path through the barriers below
+    if reduce_max(1.0 if failed else 0.0, ws) > 0:
+        raise RuntimeError(failed or "CUDA graph capture failed on another rank")
+    gc.set_seed(seed0 + 1000)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        gev[i][0].record(stream)
+        graph.replay()
+        gev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    gc.check_status()
+    return np.array([a.elapsed_time(b) for a, b in gev]), float(per.sum(axis=1).mean())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,6 +461,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time the launched calls instead of replays of one captured cycle")
     ap.add_argument("--head", choices=("markov", "rnn"), default="markov",
                     help="sequential head of the draft block (default: Markov)")
     ap.add_argument("--part", choices=("cycle", "sts"), default="cycle",
@@ -486,6 +534,14 @@ def main():
     per = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
                     for e in ev])
     cycle_ms = per.sum(axis=1)
+    graph_launch_ms = None
+    graph_error = None
+    try:
+        if args.graph:
+            cycle_ms, graph_launch_ms = time_graph_replays(args, inp, dev, rnn_w, seed0, flush, stream,
+                                                           ws, per)
+    except Exception as ex:  # the capture is refused: keep the launched timing and say why
+        graph_error = "%s: %s" % (type(ex).__name__, str(ex)[:200])
     total_s = reduce_max(float(cycle_ms.sum()) / 1e3, ws)
     B, Kb, V = w.B, w.K, w.V
     value = ws * B * Kb * K / total_s
@@ -529,9 +585,11 @@ def main():
                    "l2": "flushed between steps (256 MiB write, outside the timed events); "
                          "inputs also exceed L2",
                    "mode": "greedy_earlystop" if args.mode == 0 else "fixed_k",
-                   "head": args.head},
+                   "head": args.head, "cuda_graph": graph_launch_ms is not None,
+                   "cuda_graph_error": graph_error},
         "components_ms": {"draft": float(per[:, 0].mean()), "schedule": float(per[:, 1].mean()),
                           "verify": float(per[:, 2].mean())},
+        "launched_cycle_ms": graph_launch_ms,
         "emitted_tokens_per_s": ws * float(res["num_emitted"].sum()) / (total_s / K),
         "verified_tokens_per_s": ws * float((res["L"] + 1).sum()) / (total_s / K),
         "mean_sched_len": float(res["L"].mean()), "mean_accepted": float(res["accept_count"].mean()),

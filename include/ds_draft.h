@@ -32,7 +32,13 @@
  *     (greedy) or in [1e-3, 1e3].
  *   - Randomness: one uniform per decision, u = (w0 + 0.5) * 2^-32 where w0 is
  *     word 0 of Philox4x32-10 with key (seed & 0xffffffff, seed >> 32) and
- *     counter (request, position, stage, 0); positions are 1-based.
+ *     counter (request, position, stage, 0); positions are 1-based. The draft
+ *     and verify calls take the key by value, or from a device word
+ *     (`seed_ptr`) read when the kernels run.
+ *   - CUDA graphs: no call synchronises, allocates or reads device memory on
+ *     the host, so a whole cycle can be captured on a stream and replayed.
+ *     Per-replay state lives on the device: the Philox key behind `seed_ptr`
+ *     and the asynchronous scheduler's ring (budgets and cycle counter).
  *   - Reentrancy: stateless; calls with distinct outputs and workspaces may run
  *     concurrently on different streams.
  */
@@ -160,6 +166,7 @@ typedef struct {
   const float* rnn_b_ih;      /* [3r] */
   const float* rnn_b_hh;      /* [3r] */
   void* states;               /* out [B][K][r] s_k of every position (bfloat16) */
+  const uint64_t* seed_ptr;   /* optional device word holding the Philox key (overrides `seed`) */
 } ds_draft_args;
 
 size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
@@ -204,13 +211,17 @@ ds_status ds_transpose_projection(const void* P, int32_t r, int32_t V, int32_t d
  * iff J' = SPS(N+1) * (A + s) / (N+1) > J, and the walk stops at the first
  * candidate that is not taken. SPS(n) = sps[min(n, n_max) - 1].
  * FIXED_K: L_b = K. THRESHOLD: L_b = #{k : s_k >= threshold}.
- * ASYNC ([DSpark] 주요 결과 › 프로덕션 배포 결과, 한계와 주의사항): the number
- * of drafted tokens to verify this cycle is M = budget_ring[cycle & 1], the
+ * ASYNC ([DSpark] 주요 결과 › 프로덕션 배포 결과, 한계와 주의사항): with
+ * c = budget_ring[2] (the cycle counter, kept on the device), the number of
+ * drafted tokens to verify this cycle is M = budget_ring[c & 1], the
  * GREEDY_EARLYSTOP count computed two cycles earlier (or the caller's initial
  * value), so the verify batch B + min(M, B*K) is fixed before this cycle's
  * confidences exist; the M candidates taken are the first M of the same sorted
  * order on the current survivals (prefix-closed). The call then stores this
- * cycle's GREEDY_EARLYSTOP count in budget_ring[cycle & 1] for cycle + 2.
+ * cycle's GREEDY_EARLYSTOP count in budget_ring[c & 1] for cycle c + 2 and
+ * sets budget_ring[2] = c + 1. The caller initialises the ring once as
+ * {initial, initial, 0, 0}; nothing on the host changes between cycles, so the
+ * cycle can be replayed from a CUDA graph.
  * The objective J is evaluated in double-float arithmetic, stored as double.
  */
 typedef struct {
@@ -228,8 +239,8 @@ typedef struct {
   int32_t n_max;
   int32_t mode;               /* DS_SCHED_* */
   float threshold;            /* DS_SCHED_THRESHOLD only */
-  int32_t* budget_ring;       /* DS_SCHED_ASYNC only: [2] device words, read then overwritten */
-  int32_t cycle;              /* DS_SCHED_ASYNC only: the caller's cycle counter */
+  int32_t* budget_ring;       /* DS_SCHED_ASYNC only: [4] device words {budget, budget, cycle, 0},
+                                 16-byte aligned, updated by the call */
   float* conf;                /* out [B][K] c_k */
   float* conf_logit;          /* out [B][K] raw logit w_h.h_k + w_e.E[x_{k-1}] + b (before the
                                  temperature), the input of ds_sts_fit; may be NULL */
@@ -323,6 +334,7 @@ typedef struct {
   int32_t* status;
   const void* states;         /* RNN head: [B][K][r] states from ds_draft_block (q_k is rebuilt
                                  with s_k . P); NULL for the Markov head */
+  const uint64_t* seed_ptr;   /* optional device word holding the Philox key (overrides `seed`) */
 } ds_verify_args;
 
 size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);

@@ -40,7 +40,7 @@ class DraftArgs(ctypes.Structure):
                 ("q_token", _vp), ("q_stats", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("status", _vp),
                 ("head", _i32), ("d", _i32), ("h", _vp), ("rnn_w_ih", _vp), ("rnn_w_step", _vp),
-                ("rnn_b_ih", _vp), ("rnn_b_hh", _vp), ("states", _vp)]
+                ("rnn_b_ih", _vp), ("rnn_b_hh", _vp), ("states", _vp), ("seed_ptr", _vp)]
 
 
 class SchedArgs(ctypes.Structure):
@@ -48,7 +48,7 @@ class SchedArgs(ctypes.Structure):
                 ("h", _vp), ("E", _vp), ("anchor", _vp), ("draft_tokens", _vp), ("w_h", _vp),
                 ("w_e", _vp), ("bias", ctypes.c_float), ("sts_temp", _vp), ("sps", _vp),
                 ("n_max", _i32), ("mode", _i32), ("threshold", ctypes.c_float),
-                ("budget_ring", _vp), ("cycle", _i32),
+                ("budget_ring", _vp),
                 ("conf", _vp), ("conf_logit", _vp), ("survival", _vp), ("sched_len", _vp),
                 ("objective", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp)]
@@ -68,7 +68,7 @@ class VerifyArgs(ctypes.Structure):
                 ("sched_len", _vp), ("temperature", _vp), ("seed", ctypes.c_uint64),
                 ("out_tokens", _vp), ("accept_count", _vp), ("num_emitted", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp),
-                ("states", _vp)]
+                ("states", _vp), ("seed_ptr", _vp)]
 
 
 _lib = None
@@ -197,7 +197,7 @@ def ds_verify_workspace_bytes(B, K, V, r):
 # ---- the three calls ----------------------------------------------------------
 
 def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q_token, q_stats,
-                   workspace, status, stream=None, P_t=None, rnn=None):
+                   workspace, status, stream=None, P_t=None, rnn=None, seed_ptr=None):
     """Draft one block. ``rnn`` selects the RNN head: a dict with h [B, K, d],
     w_ih [3r, r + d], w_step (from ds_rnn_pack_weights), b_ih, b_hh (float32
     [3r]) and states (output [B, K, r]); the workspace must then also hold
@@ -217,7 +217,8 @@ def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q
                   q_token=_ptr(q_token, "q_token"), q_stats=_ptr(q_stats, "q_stats"),
                   workspace=_ptr(workspace, "workspace"),
                   workspace_bytes=workspace.numel() * workspace.element_size(),
-                  status=_ptr(status, "status"), **extra)
+                  status=_ptr(status, "status"),
+                  seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"), **extra)
     return load().ds_draft_block(ctypes.byref(a), _stream(stream))
 
 
@@ -235,8 +236,7 @@ def ds_rnn_pack_weights(w_ih, w_hh, w_step, stream=None):
 
 def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp, sps, mode,
                            conf, survival, sched_len, objective, status, threshold=0.0,
-                           workspace=None, stream=None, budget_ring=None, cycle=0,
-                           conf_logit=None):
+                           workspace=None, stream=None, budget_ring=None, conf_logit=None):
     B, K, d = h.shape
     a = SchedArgs(B=B, K=K, d=d, r=E.shape[1], V=E.shape[0], dtype=_dtype_code(h),
                   h=_ptr(h, "h"), E=_ptr(E, "E"), anchor=_ptr(anchor, "anchor"),
@@ -245,7 +245,7 @@ def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp,
                   sps=_ptr(sps, "sps"), n_max=int(sps.shape[0]), mode=int(mode),
                   threshold=float(threshold),
                   budget_ring=None if budget_ring is None else _ptr(budget_ring, "budget_ring"),
-                  cycle=int(cycle), conf=_ptr(conf, "conf"),
+                  conf=_ptr(conf, "conf"),
                   conf_logit=None if conf_logit is None else _ptr(conf_logit, "conf_logit"),
                   survival=_ptr(survival, "survival"), sched_len=_ptr(sched_len, "sched_len"),
                   objective=_ptr(objective, "objective"),
@@ -257,7 +257,7 @@ def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp,
 
 def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats, sched_len,
               temperature, seed, out_tokens, accept_count, num_emitted, workspace, status,
-              stream=None, P_t=None, states=None):
+              stream=None, P_t=None, states=None, seed_ptr=None):
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
                    target_logits=_ptr(target_logits, "target_logits"),
@@ -272,7 +272,8 @@ def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q
                    workspace=_ptr(workspace, "workspace"),
                    workspace_bytes=workspace.numel() * workspace.element_size(),
                    status=_ptr(status, "status"),
-                   states=None if states is None else _ptr(states, "states"))
+                   states=None if states is None else _ptr(states, "states"),
+                   seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"))
     return load().ds_verify(ctypes.byref(a), _stream(stream))
 
 
@@ -285,7 +286,7 @@ def ds_transpose_projection(P, P_t, stream=None):
 
 def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats,
                      sched_len, temperature, seed, out_tokens, accept_count, num_emitted, status,
-                     stream=None, P_t=None, states=None):
+                     stream=None, P_t=None, states=None, seed_ptr=None):
     """ds_verify with the library's static scratch (no workspace argument)."""
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
@@ -299,7 +300,8 @@ def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_t
                    accept_count=_ptr(accept_count, "accept_count"),
                    num_emitted=_ptr(num_emitted, "num_emitted"),
                    workspace=None, workspace_bytes=0, status=_ptr(status, "status"),
-                   states=None if states is None else _ptr(states, "states"))
+                   states=None if states is None else _ptr(states, "states"),
+                   seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"))
     return load().ds_verify_static(ctypes.byref(a), _stream(stream))
 
 

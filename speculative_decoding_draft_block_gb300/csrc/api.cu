@@ -250,6 +250,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
   if (a->P_t != nullptr && !aligned16(a->P_t)) return DS_ERR_INVALID_ARG;
+  if (a->seed_ptr != nullptr && ((uintptr_t)a->seed_ptr & 7u) != 0) return DS_ERR_INVALID_ARG;
   const bool rnn = a->head == DS_HEAD_RNN;
   if (a->head != DS_HEAD_MARKOV && !rnn) return DS_ERR_INVALID_ARG;
   size_t need = draft_ws(a->B, a->V, a->r);
@@ -287,6 +288,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   char* ws = reinterpret_cast<char*>(a->workspace);
   const bool tc = tc_path_supported(a->dtype, a->r);
   p.seed = a->seed;
+  p.seed_ptr = a->seed_ptr;
   p.tokens_out = a->draft_tokens;
   p.q_token = a->q_token;
   p.q_stats = a->q_stats;
@@ -344,7 +346,7 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
   if (a->mode != DS_SCHED_GREEDY_EARLYSTOP && a->mode != DS_SCHED_FIXED_K &&
       a->mode != DS_SCHED_THRESHOLD && a->mode != DS_SCHED_ASYNC)
     return DS_ERR_INVALID_ARG;
-  if (a->mode == DS_SCHED_ASYNC && (a->budget_ring == nullptr || (uintptr_t)a->budget_ring % 8 != 0))
+  if (a->mode == DS_SCHED_ASYNC && !aligned16(a->budget_ring))
     return DS_ERR_INVALID_ARG;
   const void* ptrs[] = {a->h, a->E, a->anchor, a->draft_tokens, a->w_h, a->w_e, a->sts_temp,
                         a->sps, a->conf, a->survival, a->sched_len, a->objective, a->status};
@@ -366,7 +368,6 @@ ds_status ds_confidence_schedule(const ds_sched_args* a, ds_stream_t stream) {
   p.bias = a->bias;
   p.threshold = a->threshold;
   p.budget_ring = a->budget_ring;
-  p.cycle = a->cycle;
   p.h = a->h;
   p.E = a->E;
   p.anchor = a->anchor;
@@ -452,6 +453,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   if (a->states != nullptr &&
       (!aligned16(a->states) || !tc_path_supported(a->dtype, a->r) || a->dtype != DS_BF16))
     return DS_ERR_INVALID_ARG;
+  if (a->seed_ptr != nullptr && ((uintptr_t)a->seed_ptr & 7u) != 0) return DS_ERR_INVALID_ARG;
   const ds_status st = device_supported();
   if (st != DS_OK) return st;
   char* ws = reinterpret_cast<char*>(a->workspace);
@@ -471,6 +473,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   v.sched_len = a->sched_len;
   v.temperature = a->temperature;
   v.seed = a->seed;
+  v.seed_ptr = a->seed_ptr;
   v.vrows = reinterpret_cast<VRow*>(ws + l.vrows);
   v.final_desc = reinterpret_cast<FinalDesc*>(ws + l.desc);
   v.out_tokens = a->out_tokens;
@@ -511,6 +514,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   else
     simt_group_layout(p);
   p.seed = a->seed;
+  p.seed_ptr = a->seed_ptr;
   p.tokens_out = a->out_tokens;
   p.status = a->status;
   if ((tc ? launch_tile_tc(p, s) : launch_sample_tile(p, s)) != cudaSuccess)

@@ -83,6 +83,7 @@ struct SampleParams {
   int32_t sup_cpt;    // 32-token chunks per tile
   int32_t sup_rows;   // rows per M-tile
   uint64_t seed;
+  const uint64_t* seed_ptr;   // when set, the key is read from the device
   int32_t* tokens_out;        // draft: draft_tokens; final: out_tokens
   float* q_token;             // draft only
   ds_row_stats* q_stats;      // draft only
@@ -99,6 +100,7 @@ struct VerifyParams {
   const int32_t* sched_len;
   const float* temperature;
   uint64_t seed;
+  const uint64_t* seed_ptr;  // when set, the key is read from the device
   VRow* vrows;  // [B][K+1]
   FinalDesc* final_desc;
   int32_t* out_tokens;
@@ -110,8 +112,7 @@ struct VerifyParams {
 struct SchedParams {
   int32_t B, K, d, r, V, dtype, n_max, mode;
   float bias, threshold;
-  int32_t* budget_ring;  // DS_SCHED_ASYNC: [2]
-  int32_t cycle;
+  int32_t* budget_ring;  // DS_SCHED_ASYNC: [4] {budget, budget, cycle, 0}
   const void* h;
   const void* E;
   const int32_t* anchor;

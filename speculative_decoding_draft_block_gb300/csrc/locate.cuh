@@ -114,7 +114,8 @@ __device__ __forceinline__ void locate_row(const SampleParams& p, int b, int tid
 
   if (wid == 0) {
     // the row's uniform does not depend on the records: draw it while they load
-    const DF u01 = uniform_df(p.seed, (uint32_t)b, c.upos, c.ustage);
+    const uint64_t seed = p.seed_ptr != nullptr ? *p.seed_ptr : p.seed;  // after the dependent wait
+    const DF u01 = uniform_df(seed, (uint32_t)b, c.upos, c.ustage);
     __syncwarp();
     const int seg = (ng + 31) / 32;
     const int c0 = min(ng, lane * seg), c1 = min(ng, c0 + seg);

@@ -330,9 +330,10 @@ template <int kMode>
 cudaError_t launch_gemm_mode(const GemmParams& g, dim3 grid, const CUtensorMap& mA,
                              const CUtensorMap& mW, cudaStream_t s) {
   using C = GemmCfg<kMode>;
-  cudaError_t e = cudaFuncSetAttribute(rnn_gemm_kernel<kMode>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-  if (e != cudaSuccess) return e;
+  // once per process (and so never inside a stream capture after a first call)
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      rnn_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  if (attr != cudaSuccess) return attr;
   return launch_pdl_cfg(rnn_gemm_kernel<kMode>, grid, dim3(kGemmThreads), C::kSmem, s, g, mA, mW);
 }
 

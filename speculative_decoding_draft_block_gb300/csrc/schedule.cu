@@ -2,8 +2,10 @@
 //
 // Asynchronous variant (DSpark summary page, 주요 결과 › 프로덕션 배포 결과):
 // the verify budget of cycle t is the early-stop count of cycle t - 2, kept in
-// a two-word device ring, and the candidates taken are the first budget-many
-// of cycle t's own sorted order.
+// a device ring {budget, budget, cycle counter, 0} that the schedule kernel
+// advances itself (nothing changes on the host between cycles, so a captured
+// cycle replays), and the candidates taken are the first budget-many of cycle
+// t's own sorted order.
 //
 // DSpark summary page, 방법론 › 신뢰도 기반 검증:
 //   c_k = sigmoid((w_h . h_k + w_e . E[x_{k-1}] + b) / T_k)   (STS temperature T_k)
@@ -117,11 +119,14 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   extern __shared__ unsigned long long keys[];
   __shared__ DF wsum[32];
   __shared__ int red[32];
-  __shared__ int s_budget;
+  __shared__ int s_budget, s_cycle;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int B = p.B, K = p.K, n = B * K;
   // asynchronous mode: this cycle's budget, written two cycles ago
-  if (tid == 0) s_budget = (p.mode == DS_SCHED_ASYNC) ? p.budget_ring[p.cycle & 1] : 0;
+  if (tid == 0) {
+    s_cycle = (p.mode == DS_SCHED_ASYNC) ? p.budget_ring[2] : 0;
+    s_budget = (p.mode == DS_SCHED_ASYNC) ? p.budget_ring[s_cycle & 1] : 0;
+  }
 
   // survival (sequential over k per request, fp32)
   for (int b = tid; b < B; b += kSchedThreads) {
@@ -242,7 +247,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   if (p.mode == DS_SCHED_ASYNC) {
     // dynamic top-k: take the budget's worth of the current order; store this
     // cycle's early-stop count as the budget of cycle + 2
-    if (tid == 0) p.budget_ring[p.cycle & 1] = M;
+    if (tid == 0) {
+      p.budget_ring[s_cycle & 1] = M;
+      p.budget_ring[2] = s_cycle + 1;
+    }
     M = min(max(s_budget, 0), n);
   }
 

@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
         // u * q(x) < p(x) = w_x / S, tested as u * q(x) * S < w_x
         const float wx = weight_rel(tx, 0.f, g, N);
         const float qx = p.q_token[(size_t)b * p.K + j];
-        const DF uq = df_mul(uniform_df(p.seed, (uint32_t)b, (uint32_t)(j + 1), DS_STAGE_ACCEPT),
+        const uint64_t seed = p.seed_ptr != nullptr ? *p.seed_ptr : p.seed;
+        const DF uq = df_mul(uniform_df(seed, (uint32_t)b, (uint32_t)(j + 1), DS_STAGE_ACCEPT),
                              DF{qx, 0.f});
         out.accept = df_lt(df_mul(uq, S), DF{wx, 0.f}) ? 1 : 0;
       }

@@ -35,9 +35,13 @@ INPUT_KEYS = ("base_logits", "target_logits", "E", "P", "anchor", "temperature",
 
 class DeviceCycle:
     def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0,
-                 token_major_projection=True, initial_budget=None, rnn_weights=None):
+                 token_major_projection=True, initial_budget=None, rnn_weights=None,
+                 device_seed=False):
         """``rnn_weights`` (dict w_ih, w_hh as bfloat16 bits, b_ih, b_hh float32)
-        selects the RNN head; its step matrix is packed once here."""
+        selects the RNN head; its step matrix is packed once here.
+        ``device_seed``: the Philox key is read from a device word (``seed_dev``,
+        set with ``set_seed``) instead of the ``seed`` argument, so that a
+        captured cycle can be replayed with a fresh key each time."""
         self.inp = inp
         self.device = torch.device(device)
         self.mode = mode
@@ -62,12 +66,13 @@ class DeviceCycle:
         self.accept_count = torch.zeros((B,), **i32)
         self.num_emitted = torch.zeros((B,), **i32)
         self.status = torch.zeros((4,), **i32)
-        # asynchronous scheduler: budgets of the next two cycles (device ring)
-        # and the cycle counter; the first two cycles use initial_budget
+        # asynchronous scheduler: budgets of the next two cycles and the cycle
+        # counter, all on the device; the first two cycles use initial_budget
         if initial_budget is None:
             initial_budget = B * K // 2
-        self.budget_ring = torch.full((2,), int(initial_budget), **i32)
-        self.sched_cycle = 0
+        self.initial_budget = int(initial_budget)
+        self.budget_ring = torch.tensor([self.initial_budget, self.initial_budget, 0, 0], **i32)
+        self.seed_dev = torch.zeros((2,), dtype=torch.int64, device=dev) if device_seed else None
         wd = _lib.ds_draft_workspace_bytes(B, K, V, r)
         wv = _lib.ds_verify_workspace_bytes(B, K, V, r)
         if wd == 0 or wv == 0:
@@ -93,12 +98,22 @@ class DeviceCycle:
             self.P_t = torch.empty((P.shape[1], P.shape[0]), dtype=P.dtype, device=dev)
             check(_lib.ds_transpose_projection(P, self.P_t), "ds_transpose_projection")
 
+    def set_seed(self, seed):
+        """Write the Philox key to the device word (a device-side fill: capturable)."""
+        seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+        self.seed_dev[0].fill_(seed - (1 << 64) if seed >= (1 << 63) else seed)  # same 64 bits
+
+    def reset_ring(self):
+        self.budget_ring.copy_(torch.tensor([self.initial_budget, self.initial_budget, 0, 0],
+                                            dtype=torch.int32))
+
     # -- the three calls ---------------------------------------------------------
     def draft(self, seed, stream=None):
         t = self.t
         check(_lib.ds_draft_block(t["base_logits"], t["E"], t["P"], t["anchor"], t["temperature"],
                                   seed, self.draft_tokens, self.q_token, self.q_stats,
-                                  self.ws_draft, self.status, stream, P_t=self.P_t, rnn=self.rnn),
+                                  self.ws_draft, self.status, stream, P_t=self.P_t, rnn=self.rnn,
+                                  seed_ptr=self.seed_dev),
               "ds_draft_block")
 
     def schedule(self, stream=None):
@@ -108,9 +123,8 @@ class DeviceCycle:
                                           self.mode, self.conf, self.survival, self.sched_len,
                                           self.objective, self.status, threshold=self.threshold,
                                           stream=stream, budget_ring=self.budget_ring,
-                                          cycle=self.sched_cycle, conf_logit=self.conf_logit),
+                                          conf_logit=self.conf_logit),
               "ds_confidence_schedule")
-        self.sched_cycle += 1
 
     def verify(self, seed, stream=None):
         t = self.t
@@ -118,7 +132,8 @@ class DeviceCycle:
                              self.draft_tokens, self.q_token, self.q_stats, self.sched_len,
                              t["temperature"], seed, self.out_tokens, self.accept_count,
                              self.num_emitted, self.ws_verify, self.status, stream, P_t=self.P_t,
-                             states=None if self.rnn is None else self.rnn["states"]),
+                             states=None if self.rnn is None else self.rnn["states"],
+                             seed_ptr=self.seed_dev),
               "ds_verify")
 
     def run(self, seed, stream=None):

@@ -204,8 +204,54 @@ def test_async_scheduler_over_cycles(ds):
             assert abs(g["objective"] - want["objective"]) <= 1e-5 * want["objective"]
         _parity.assert_parity(inp, g, SEED + t, check_schedule=False)
     # the ring holds the last two cycles' early-stop counts
-    ring = sorted(cyc.budget_ring.cpu().numpy().tolist())
-    assert ring == sorted(counts[-2:]) or near[-1] or near[-2]
+    ring = cyc.budget_ring.cpu().numpy().tolist()
+    assert ring[2] == 5                                  # the device cycle counter
+    assert sorted(ring[:2]) == sorted(counts[-2:]) or near[-1] or near[-2]
+
+
+def test_cycle_replays_from_a_cuda_graph(ds):
+    """A whole cycle (draft, asynchronous schedule, verify, and the key's
+    advance) captured once into a CUDA graph and replayed: each replay equals a
+    direct run with the same key and ring state (the per-cycle state lives on
+    the device: the Philox key word and the scheduler's ring)."""
+    import torch
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
+    inp = _ragged(True, (0.0, 0.6, 1.0), 31, B=24, K=6, V=4096, r=64, d=128)
+    kw = dict(mode=_lib.DS_SCHED_ASYNC, initial_budget=17, device_seed=True)
+    ref = DeviceCycle(inp, **kw)
+    cyc = DeviceCycle(inp, **kw)
+    cyc.set_seed(1)                      # one-time library set-up outside the capture
+    cyc.run(0)
+    torch.cuda.synchronize()
+    cyc.reset_ring()
+    cyc.reset_status()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            cyc.run(0)
+            cyc.seed_dev[0].add_(1)
+    torch.cuda.synchronize()
+    cyc.set_seed(SEED)
+    prev = None
+    for t in range(4):
+        graph.replay()
+        torch.cuda.synchronize()
+        got = cyc.results()
+        ref.set_seed(SEED + t)
+        ref.run(0)
+        torch.cuda.synchronize()
+        want = ref.results()
+        for key in ("tokens", "L", "out_tokens", "accept_count", "q_token"):
+            assert np.array_equal(got[key], want[key]), (t, key)
+        assert np.array_equal(cyc.budget_ring.cpu().numpy(), ref.budget_ring.cpu().numpy())
+        if prev is not None:
+            assert not np.array_equal(got["tokens"], prev)  # a fresh key every replay
+        prev = got["tokens"]
+    cyc.check_status()
+    ref.check_status()
 
 
 def test_minimal_shapes(ds):
