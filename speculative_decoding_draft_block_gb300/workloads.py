@@ -62,8 +62,12 @@ def _cfg(name, **kw):
     return Workload(name=name, **kw)
 
 
-# The five workloads the method is measured on (sizes, distributions and
-# schedules as stated for them; see the design doc for the readings).
+# The five workloads the method is measured on: batch B, block K, vocabulary
+# V, rank r, hidden size d, logit spread sigma_z, the true token's bump (bump0,
+# falling by bump_decay per position), per-request target noise sigma_b, STS
+# temperatures, sampling temperatures, the SPS table and the confidence bias.
+# Where a workload leaves a value open it takes the B=32 workload's (bf16
+# N(0, 1.5^2) logits, +5 bump, STS temperatures U[0.8, 1.5]).
 TINY = _cfg("tiny_B4_K4_V1024", B=4, K=4, V=1024, r=32, d=256, bf16=False, sigma_z=2.0,
             bump0=4.0, bump_decay=0.0, sigma_b=(0.5, 0.5), sts=(1.0, 1.0), temps=(1.0,),
             sps_kind="tiny", sps_nmax=4 * 5, conf_bias=0.0, seed=1000)
