@@ -450,6 +450,78 @@ def time_graph_replays(args, inp, dev, rnn_w, seed0, flush, stream, ws, per):
     return np.array([a.elapsed_time(b) for a, b in gev]), float(per.sum(axis=1).mean())
 
 
+DRAFT_KEYS = ("base_logits", "anchor", "temperature", "h")
+
+
+def time_e2e(args, cyc, inp, stream, dev, seed0, ws):
+    """End to end through the public API, as a caller holding each step's inputs
+    in pinned host memory runs it: the draft's inputs are copied in, draft and
+    schedule run, the scheduled lengths come back (4 B per request), only the
+    target rows that verify reads (rows 0..L_b of request b, one contiguous copy
+    per request) go in, verify runs, and the emitted tokens come back. Every
+    copy is inside the timed region; the bytes are counted from the copies."""
+    import numpy as np
+    import torch
+    from speculative_decoding_draft_block_gb300.cycle import to_host_pinned
+    B, K = inp["B"], inp["K"]
+    host = {k: to_host_pinned(inp[k]) for k in STEP_KEYS}
+    tgt_h, tgt_d = host["target_logits"], cyc.t["target_logits"]
+    row_bytes = tgt_d.shape[2] * tgt_d.element_size()
+    L_host = torch.empty((B,), dtype=torch.int32).pin_memory()
+    out_host = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    nem_host = torch.empty((B,), dtype=torch.int32).pin_memory()
+    # the per-request row copies go straight to the CUDA runtime the library
+    # links (a plain cudaMemcpyAsync each: a few microseconds of host time
+    # instead of a framework call per request)
+    cudart = ctypes.CDLL("libcudart.so.13")
+    cudart.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                                       ctypes.c_void_p]
+    cudart.cudaMemcpyAsync.restype = ctypes.c_int
+    h2d_kind = 1  # cudaMemcpyHostToDevice
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    req_bytes = (K + 1) * row_bytes
+    dst0, src0 = tgt_d.data_ptr(), tgt_h.data_ptr()
+
+    def step(seed):
+        h2d = 0
+        for k in DRAFT_KEYS:
+            src = host[k] if host[k].dtype == cyc.t[k].dtype else host[k].view(cyc.t[k].dtype)
+            cyc.t[k].copy_(src, non_blocking=True)
+            h2d += src.numel() * src.element_size()
+        cyc.draft(seed)
+        cyc.schedule()
+        L_host.copy_(cyc.sched_len, non_blocking=True)
+        stream.synchronize()  # the host needs the lengths to choose the rows
+        for b, lb in enumerate(L_host.tolist()):
+            n = (min(max(int(lb), 0), K) + 1) * row_bytes
+            if cudart.cudaMemcpyAsync(dst0 + b * req_bytes, src0 + b * req_bytes, n, h2d_kind, sh) != 0:
+                raise RuntimeError("cudaMemcpyAsync failed")
+            h2d += n
+        cyc.verify(seed)
+        out_host.copy_(cyc.out_tokens, non_blocking=True)
+        nem_host.copy_(cyc.num_emitted, non_blocking=True)
+        return h2d
+
+    for i in range(2):
+        step(seed0 + i)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    E = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h2d = []
+    e0.record(stream)
+    for i in range(E):
+        h2d.append(step(seed0 + 5000 + i))
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws)
+    d2h = (L_host.numel() + out_host.numel() + nem_host.numel()) * 4
+    return {"value": ws * B * K * E / e2e_s, "unit": "tokens/s",
+            "h2d_bytes_per_step": int(np.mean(h2d)), "d2h_bytes_per_step": int(d2h), "steps": E,
+            "copied": list(DRAFT_KEYS) + ["target_logits rows 0..L_b", "sched_len", "out_tokens",
+                                           "num_emitted"]}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -601,35 +673,7 @@ def main():
     }
 
     if not args.no_e2e:
-        # End to end through the public API: pinned host inputs copied in and the
-        # emitted tokens copied out inside the timed region, every step.
-        host = {k: to_host_pinned(inp[k]) for k in STEP_KEYS}
-        out_host = torch.empty((B, Kb + 1), dtype=torch.int32).pin_memory()
-        nem_host = torch.empty((B,), dtype=torch.int32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * 4 + nem_host.numel() * 4
-        for i in range(2):
-            for k in STEP_KEYS:
-                cyc.t[k].copy_(host[k].view(cyc.t[k].dtype) if host[k].dtype != cyc.t[k].dtype else host[k], non_blocking=True)
-            cyc.run(seed0 + i)
-        torch.cuda.synchronize(dev)
-        barrier(ws)
-        E = max(1, args.e2e_steps)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(E):
-            for k in STEP_KEYS:
-                src = host[k] if host[k].dtype == cyc.t[k].dtype else host[k].view(cyc.t[k].dtype)
-                cyc.t[k].copy_(src, non_blocking=True)
-            cyc.run(seed0 + 5000 + i)
-            out_host.copy_(cyc.out_tokens, non_blocking=True)
-            nem_host.copy_(cyc.num_emitted, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws)
-        line["e2e"] = {"value": ws * B * Kb * E / e2e_s, "unit": "tokens/s",
-                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                       "steps": E, "copied": list(STEP_KEYS) + ["out_tokens", "num_emitted"]}
+        line["e2e"] = time_e2e(args, cyc, inp, stream, dev, seed0, ws)
         cyc.check_status()
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -314,7 +314,7 @@ ds_status ds_sts_fit(const ds_sts_args* args, ds_stream_t stream);
 typedef struct {
   int32_t B, K, V, r;
   int32_t dtype;              /* ds_dtype of target_logits, base_logits, E and P */
-  const void* target_logits;  /* [B][K+1][V] */
+  const void* target_logits;  /* [B][K+1][V]; only rows j <= sched_len[b] of request b are read */
   const void* base_logits;    /* [B][K][V] */
   const void* E;              /* [V][r] */
   const void* P;              /* [r][V] */
