@@ -412,7 +412,8 @@ def time_graph_replays(args, inp, dev, rnn_w, seed0, flush, stream, ws, per):
     import torch
     from speculative_decoding_draft_block_gb300.cycle import DeviceCycle
     K = args.steps
-    gc = DeviceCycle(inp, device=dev, mode=args.mode, rnn_weights=rnn_w, device_seed=True)
+    gc = DeviceCycle(inp, device=dev, mode=args.mode, threshold=args.threshold, rnn_weights=rnn_w,
+                     device_seed=True)
     gc.set_seed(seed0)
     gc.run(0)
     torch.cuda.synchronize(dev)
@@ -451,6 +452,7 @@ def time_graph_replays(args, inp, dev, rnn_w, seed0, flush, stream, ws, per):
 
 
 DRAFT_KEYS = ("base_logits", "anchor", "temperature", "h")
+MODE_NAMES = {0: "greedy_earlystop", 1: "fixed_k", 2: "threshold", 3: "async"}
 
 
 def time_e2e(args, cyc, inp, stream, dev, seed0, ws):
@@ -529,7 +531,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--mode", type=int, default=0, help="0 greedy+early stop, 1 fixed K")
+    ap.add_argument("--mode", type=int, default=0, choices=(0, 1, 2, 3),
+                    help="scheduler: 0 greedy + early stop, 1 fixed K, 2 survival threshold, "
+                         "3 asynchronous (budget from two cycles back)")
+    ap.add_argument("--threshold", type=float, default=0.5, help="survival threshold of mode 2")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -571,7 +576,7 @@ def main():
     if rnn:
         from speculative_decoding_draft_block_gb300.workloads import make_rnn_weights
         rnn_w = make_rnn_weights(w.r, w.d)
-    cyc = DeviceCycle(inp, device=dev, mode=args.mode, rnn_weights=rnn_w)
+    cyc = DeviceCycle(inp, device=dev, mode=args.mode, threshold=args.threshold, rnn_weights=rnn_w)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
     seed0 = 0x5EED0000 + 7919 * rank
@@ -656,7 +661,8 @@ def main():
                    "parallelism": "replicas" if ws > 1 else "single",
                    "l2": "flushed between steps (256 MiB write, outside the timed events); "
                          "inputs also exceed L2",
-                   "mode": "greedy_earlystop" if args.mode == 0 else "fixed_k",
+                   "mode": MODE_NAMES[args.mode],
+                   "threshold": args.threshold if args.mode == 2 else None,
                    "head": args.head, "cuda_graph": graph_launch_ms is not None,
                    "cuda_graph_error": graph_error},
         "components_ms": {"draft": float(per[:, 0].mean()), "schedule": float(per[:, 1].mean()),
