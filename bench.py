@@ -456,72 +456,42 @@ MODE_NAMES = {0: "greedy_earlystop", 1: "fixed_k", 2: "threshold", 3: "async"}
 
 
 def time_e2e(args, cyc, inp, stream, dev, seed0, ws):
-    """End to end through the public API, as a caller holding each step's inputs
-    in pinned host memory runs it: the draft's inputs are copied in, draft and
-    schedule run, the scheduled lengths come back (4 B per request), only the
-    target rows that verify reads (rows 0..L_b of request b, one contiguous copy
-    per request) go in, verify runs, and the emitted tokens come back. Every
-    copy is inside the timed region; the bytes are counted from the copies."""
+    """End to end through the public API (``HostPipeline``), as a caller holding
+    each step's inputs in pinned host memory runs it: the draft's inputs are
+    copied in, draft and schedule run, the scheduled lengths come back (4 B per
+    request), only the target rows that verify reads (rows 0..L_b of request b,
+    one contiguous copy per request) go in, verify runs, and the emitted tokens
+    come back. Each step also starts the copy of the next step's draft inputs
+    (independent request groups served in turn), which overlaps the current
+    step. Every copy is inside the timed region: the copy stream waits for the
+    start event, and the last step stages nothing ahead. The bytes are counted
+    from the copies."""
     import numpy as np
     import torch
-    from speculative_decoding_draft_block_gb300.cycle import to_host_pinned
+    from speculative_decoding_draft_block_gb300.cycle import HostPipeline, to_host_pinned
     B, K = inp["B"], inp["K"]
     host = {k: to_host_pinned(inp[k]) for k in STEP_KEYS}
-    tgt_h, tgt_d = host["target_logits"], cyc.t["target_logits"]
-    row_bytes = tgt_d.shape[2] * tgt_d.element_size()
-    L_host = torch.empty((B,), dtype=torch.int32).pin_memory()
-    out_host = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
-    nem_host = torch.empty((B,), dtype=torch.int32).pin_memory()
-    # the per-request row copies go straight to the CUDA runtime the library
-    # links (a plain cudaMemcpyAsync each: a few microseconds of host time
-    # instead of a framework call per request)
-    cudart = ctypes.CDLL("libcudart.so.13")
-    cudart.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
-                                       ctypes.c_void_p]
-    cudart.cudaMemcpyAsync.restype = ctypes.c_int
-    h2d_kind = 1  # cudaMemcpyHostToDevice
-    sh = ctypes.c_void_p(stream.cuda_stream)
-    req_bytes = (K + 1) * row_bytes
-    dst0, src0 = tgt_d.data_ptr(), tgt_h.data_ptr()
-
-    def step(seed):
-        h2d = 0
-        for k in DRAFT_KEYS:
-            src = host[k] if host[k].dtype == cyc.t[k].dtype else host[k].view(cyc.t[k].dtype)
-            cyc.t[k].copy_(src, non_blocking=True)
-            h2d += src.numel() * src.element_size()
-        cyc.draft(seed)
-        cyc.schedule()
-        L_host.copy_(cyc.sched_len, non_blocking=True)
-        stream.synchronize()  # the host needs the lengths to choose the rows
-        for b, lb in enumerate(L_host.tolist()):
-            n = (min(max(int(lb), 0), K) + 1) * row_bytes
-            if cudart.cudaMemcpyAsync(dst0 + b * req_bytes, src0 + b * req_bytes, n, h2d_kind, sh) != 0:
-                raise RuntimeError("cudaMemcpyAsync failed")
-            h2d += n
-        cyc.verify(seed)
-        out_host.copy_(cyc.out_tokens, non_blocking=True)
-        nem_host.copy_(cyc.num_emitted, non_blocking=True)
-        return h2d
-
+    pipe = HostPipeline(cyc, stream)
     for i in range(2):
-        step(seed0 + i)
+        pipe.step(host, seed0 + i)
     torch.cuda.synchronize(dev)
     barrier(ws)
     E = max(1, args.e2e_steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     h2d = []
     e0.record(stream)
+    pipe.copy_stream.wait_event(e0)
     for i in range(E):
-        h2d.append(step(seed0 + 5000 + i))
+        pipe.step(host, seed0 + 5000 + i, next_host=host if i + 1 < E else None)
+        h2d.append(pipe.h2d_bytes)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws)
-    d2h = (L_host.numel() + out_host.numel() + nem_host.numel()) * 4
     return {"value": ws * B * K * E / e2e_s, "unit": "tokens/s",
-            "h2d_bytes_per_step": int(np.mean(h2d)), "d2h_bytes_per_step": int(d2h), "steps": E,
+            "h2d_bytes_per_step": int(np.mean(h2d)), "d2h_bytes_per_step": int(pipe.d2h_bytes), "steps": E,
             "copied": list(DRAFT_KEYS) + ["target_logits rows 0..L_b", "sched_len", "out_tokens",
-                                           "num_emitted"]}
+                                           "num_emitted"],
+            "overlap": "next step's draft inputs copied during the current step (copy stream)"}
 
 
 def main():

@@ -361,6 +361,28 @@ ds_status ds_verify(const ds_verify_args* args, ds_stream_t stream);
 ds_status ds_verify_static(const ds_verify_args* args, ds_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Host-resident target rows                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Copies, for every request b, rows 0..L_b of its target logits from host
+ * memory to the device buffer ds_verify reads, with L_b = min(max(lens[b], 0), K)
+ * (ds_verify reads no other row of request b: the accepted prefix ends at
+ * L_b and the final draw uses row j <= L_b; [DSpark] 배경 on the
+ * verification of a scheduled prefix, [DFlash] DFlashProposer 초기화 on the
+ * K + 1 target positions per request). One cudaMemcpyAsync per request on
+ * `stream`; the call returns once they are enqueued.
+ *   dst, src     [B][K+1][row_bytes] (same layout on both sides); `src` is host
+ *                memory (pinned for an asynchronous copy), `dst` device memory
+ *   lens         host array [B]: the scheduled lengths (ds_confidence_schedule's
+ *                sched_len, read back to the host)
+ *   bytes_out    optional host word: the number of bytes enqueued
+ * Errors: DS_ERR_INVALID_ARG for a null pointer, B < 1, K < 0 or
+ * row_bytes == 0 (nothing is enqueued); DS_ERR_CUDA if an enqueue fails
+ * (earlier requests' copies stay enqueued). */
+ds_status ds_copy_scheduled_rows(void* dst, const void* src, int32_t B, int32_t K, size_t row_bytes,
+                                 const int32_t* lens, uint64_t* bytes_out, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status and identification                                                 */
 /* ------------------------------------------------------------------------ */
 

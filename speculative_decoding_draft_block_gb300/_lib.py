@@ -27,7 +27,7 @@ EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspa
            "ds_draft_block", "ds_sched_workspace_bytes", "ds_confidence_schedule",
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
            "ds_version", "ds_transpose_projection", "ds_verify_static", "ds_sts_workspace_bytes",
-           "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights")
+           "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights", "ds_copy_scheduled_rows")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -111,6 +111,9 @@ def load():
     lib.ds_sts_fit.restype = ctypes.c_int
     lib.ds_transpose_projection.argtypes = [_vp, _i32, _i32, _i32, _vp, _vp]
     lib.ds_transpose_projection.restype = ctypes.c_int
+    lib.ds_copy_scheduled_rows.argtypes = [_vp, _vp, _i32, _i32, ctypes.c_size_t, _vp,
+                                           ctypes.POINTER(ctypes.c_uint64), _vp]
+    lib.ds_copy_scheduled_rows.restype = ctypes.c_int
     lib.ds_check_status.argtypes = [_vp, _vp]
     lib.ds_check_status.restype = ctypes.c_int
     lib.ds_status_string.argtypes = [ctypes.c_int]
@@ -325,6 +328,25 @@ def ds_sts_fit(logits, labels, grid, n_bins, sts_temp, grid_index, ece, workspac
                 workspace_bytes=workspace.numel() * workspace.element_size(),
                 status=_ptr(status, "status"))
     return load().ds_sts_fit(ctypes.byref(a), _stream(stream))
+
+
+def ds_copy_scheduled_rows(dst, src, lens, stream=None):
+    """Rows 0..L_b of each request's target logits, host ``src`` -> device
+    ``dst`` (both [B, K+1, V]); ``lens``: host int32 tensor [B]. Returns
+    (status, bytes enqueued)."""
+    if dst.dim() != 3 or tuple(src.shape) != tuple(dst.shape) or src.dtype != dst.dtype:
+        raise ValueError("dst and src must be [B, K+1, V] tensors of one dtype")
+    if src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous host tensor")
+    if lens.is_cuda or lens.dtype != torch.int32 or lens.numel() != dst.shape[0] or not lens.is_contiguous():
+        raise ValueError("lens must be a contiguous host int32 tensor [B]")
+    n = ctypes.c_uint64(0)
+    code = load().ds_copy_scheduled_rows(_ptr(dst, "dst"), ctypes.c_void_p(src.data_ptr()),
+                                         int(dst.shape[0]), int(dst.shape[1]) - 1,
+                                         int(dst.shape[2]) * dst.element_size(),
+                                         ctypes.c_void_p(lens.data_ptr()), ctypes.byref(n),
+                                         _stream(stream))
+    return code, int(n.value)
 
 
 def ds_check_status(status, stream=None):

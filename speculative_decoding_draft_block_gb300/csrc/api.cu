@@ -523,6 +523,27 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   return DS_OK;
 }
 
+ds_status ds_copy_scheduled_rows(void* dst, const void* src, int32_t B, int32_t K, size_t row_bytes,
+                                 const int32_t* lens, uint64_t* bytes_out, ds_stream_t stream) {
+  if (dst == nullptr || src == nullptr || lens == nullptr || B < 1 || K < 0 || row_bytes == 0)
+    return DS_ERR_INVALID_ARG;
+  const size_t req_bytes = (size_t)(K + 1) * row_bytes;
+  uint64_t total = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t L = lens[b] < 0 ? 0 : (lens[b] > K ? K : lens[b]);
+    const size_t n = (size_t)(L + 1) * row_bytes;
+    const size_t off = (size_t)b * req_bytes;
+    if (cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off, n,
+                        cudaMemcpyHostToDevice, (cudaStream_t)stream) != cudaSuccess) {
+      if (bytes_out) *bytes_out = total;
+      return DS_ERR_CUDA;
+    }
+    total += n;
+  }
+  if (bytes_out) *bytes_out = total;
+  return DS_OK;
+}
+
 ds_status ds_check_status(const int32_t* device_status, ds_stream_t stream) {
   if (device_status == nullptr) return DS_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DS_ERR_CUDA;

@@ -58,14 +58,6 @@ __device__ __forceinline__ DF shfl_df(DF v, int l) {
   return {__shfl_sync(0xffffffffu, v.hi, l), __shfl_sync(0xffffffffu, v.lo, l)};
 }
 
-// One CTA per row, in three levels: (1) combine the row's group records
-// (exact power-of-two rescale, double-float prefix) and find the group where
-// the CDF crosses u*S; (2) scan that group's chunk records to find the
-// crossing chunk; (3) recompute that chunk's 32 weights with the arithmetic
-// its record used and pick the token: x = min{i : u*S < C_i}. Levels 1 and 2
-// run in warp 0 alone (no block barrier); the E row of the bias is loaded by
-// every thread at the start and only stored for level 3, so its latency
-// overlaps levels 1 and 2. Each level costs one round of independent loads.
 // One row, in three levels: (1) combine the row's group records (exact
 // power-of-two rescale, double-float prefix) and find the group where the CDF
 // crosses u*S; (2) scan that group's chunk records to find the crossing chunk;

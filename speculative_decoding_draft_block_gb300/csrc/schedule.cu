@@ -16,9 +16,12 @@
 //
 //   confidence_kernel  one warp per (b, k): two dot products (d and r long,
 //                      16-byte loads, fp32 accumulation of exact bf16
-//                      products), sigmoid.
+//                      products), sigmoid. w_h . h_k reads only inputs of the
+//                      cycle and runs before the programmatic-launch wait, so
+//                      it overlaps the end of the draft.
 //   schedule_kernel    one CTA: survival cumprod, bitonic sort of 64-bit keys
-//                      (survival descending, then k, then b) in shared memory,
+//                      (survival descending, then k, then b) in shared memory
+//                      (stages of stride <= 32 synchronise one warp only),
 //                      double-float prefix scan of A, first drop of J tested
 //                      without division: J' > J <=> SPS(N+1) (A+s) N > SPS(N) A (N+1).
 //                      (double precision runs at a small fraction of the float
@@ -27,8 +30,11 @@
 #include <float.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace ds {
 
@@ -61,20 +67,80 @@ __device__ __forceinline__ float dot_warp(const Tin* a, const Tin* w, int n, int
   return acc;
 }
 
-template <typename Tin>
+// w_h . h_k for bf16: w_h staged once per CTA in shared memory, eight 16-byte
+// loads of h in flight per lane, two accumulators (exact bf16 products).
+__device__ __forceinline__ float dot_h_bf16(const __nv_bfloat16* a, const __nv_bfloat16* sw, int n,
+                                            int lane) {
+  float acc0 = 0.f, acc1 = 0.f;
+  int i = lane * 8;
+  for (; i + 7 * 256 < n; i += 8 * 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldg(reinterpret_cast<const uint4*>(a + i + u * 256));
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 w = *reinterpret_cast<const uint4*>(sw + i + u * 256);
+      const uint32_t xv[4] = {v[u].x, v[u].y, v[u].z, v[u].w}, wv[4] = {w.x, w.y, w.z, w.w};
+      float acc = (u & 1) ? acc1 : acc0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc = __fmaf_rn(__uint_as_float(xv[q] << 16), __uint_as_float(wv[q] << 16), acc);
+        acc = __fmaf_rn(__uint_as_float(xv[q] & 0xffff0000u), __uint_as_float(wv[q] & 0xffff0000u), acc);
+      }
+      if (u & 1) acc1 = acc; else acc0 = acc;
+    }
+  }
+  for (; i < n; i += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a + i));
+    const uint4 w = *reinterpret_cast<const uint4*>(sw + i);
+    const uint32_t xv[4] = {v.x, v.y, v.z, v.w}, wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc0 = __fmaf_rn(__uint_as_float(xv[q] << 16), __uint_as_float(wv[q] << 16), acc0);
+      acc0 = __fmaf_rn(__uint_as_float(xv[q] & 0xffff0000u), __uint_as_float(wv[q] & 0xffff0000u), acc0);
+    }
+  }
+  float acc = __fadd_rn(acc0, acc1);
+  for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  return acc;
+}
+
+// kStage: bf16 with w_h staged in shared memory (d up to kStageMaxD).
+constexpr int kStageMaxD = 12288;
+
+template <typename Tin, bool kStage>
 __global__ void __launch_bounds__(256) confidence_kernel(SchedParams p) {
+  extern __shared__ __align__(16) unsigned char conf_smem[];
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (item >= p.B * p.K) return;
+  static_assert(!kStage || std::is_same<Tin, __nv_bfloat16>::value, "staging is bf16 only");
+  sm100::pdl_launch_dependents();
+  // w_h and h are inputs of the cycle (no kernel of the cycle writes them), so
+  // w_h . h_k runs before the wait and overlaps the end of the draft.
+  if constexpr (kStage) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.w_h);
+    uint4* dst = reinterpret_cast<uint4*>(conf_smem);
+    for (int i = threadIdx.x; i < p.d / 8; i += 256) dst[i] = __ldg(src + i);
+    __syncthreads();
+  }
+  if (item >= p.B * p.K) {
+    sm100::pdl_wait();
+    return;
+  }
+  const Tin* h = reinterpret_cast<const Tin*>(p.h) + (size_t)item * p.d;
+  float dh;
+  if constexpr (kStage)
+    dh = dot_h_bf16(h, reinterpret_cast<const __nv_bfloat16*>(conf_smem), p.d, lane);
+  else
+    dh = dot_warp(h, reinterpret_cast<const Tin*>(p.w_h), p.d, lane);
+  sm100::pdl_wait();  // draft tokens come from the draft's kernels
   const int b = item / p.K, k = item - b * p.K;
   int prev = (k == 0) ? p.anchor[b] : p.draft_tokens[(size_t)b * p.K + k - 1];
   if (prev < 0 || prev >= p.V) {
     if (lane == 0) report(p.status, kErrBounds);
     prev = 0;
   }
-  const Tin* h = reinterpret_cast<const Tin*>(p.h) + (size_t)item * p.d;
   const Tin* E = reinterpret_cast<const Tin*>(p.E) + (size_t)prev * p.r;
-  const float dh = dot_warp(h, reinterpret_cast<const Tin*>(p.w_h), p.d, lane);
   const float de = dot_warp(E, reinterpret_cast<const Tin*>(p.w_e), p.r, lane);
   if (lane == 0) {
     const float Tk = p.sts_temp[k];
@@ -115,6 +181,19 @@ __device__ __forceinline__ bool gains(float sps1, float sps0, DF A, float s, int
 
 constexpr int kSchedThreads = 1024;
 
+// One compare-exchange of pair i at the given stride, ascending within blocks
+// of `size` keys whose index has the `size` bit clear.
+__device__ __forceinline__ void bitonic_cx(unsigned long long* keys, int i, int stride, int size) {
+  const int lo = 2 * i - (i & (stride - 1));
+  const int hi = lo + stride;
+  const bool asc = (lo & size) == 0;
+  const unsigned long long a = keys[lo], c = keys[hi];
+  if ((a > c) == asc) {
+    keys[lo] = c;
+    keys[hi] = a;
+  }
+}
+
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) {
   extern __shared__ unsigned long long keys[];
   __shared__ DF wsum[32];
@@ -122,6 +201,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   __shared__ int s_budget, s_cycle;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int B = p.B, K = p.K, n = B * K;
+  sm100::pdl_wait();  // confidences come from the confidence kernel
   // asynchronous mode: this cycle's budget, written two cycles ago
   if (tid == 0) {
     s_cycle = (p.mode == DS_SCHED_ASYNC) ? p.budget_ring[2] : 0;
@@ -132,10 +212,19 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   for (int b = tid; b < B; b += kSchedThreads) {
     float s = 1.f;
     int L = 0;
-    for (int k = 0; k < K; ++k) {
-      s = s * p.conf[(size_t)b * K + k];
-      p.survival[(size_t)b * K + k] = s;
-      if (p.mode == DS_SCHED_THRESHOLD && s >= p.threshold && L == k) L = k + 1;
+    for (int k0 = 0; k0 < K; k0 += 16) {  // a chunk's loads in flight together
+      float c[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) c[u] = (k0 + u < K) ? p.conf[(size_t)b * K + k0 + u] : 1.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int k = k0 + u;
+        if (k < K) {
+          s = s * c[u];
+          p.survival[(size_t)b * K + k] = s;
+          if (p.mode == DS_SCHED_THRESHOLD && s >= p.threshold && L == k) L = k + 1;
+        }
+      }
     }
     p.sched_len[b] = (p.mode == DS_SCHED_FIXED_K) ? K : (p.mode == DS_SCHED_THRESHOLD ? L : 0);
   }
@@ -183,20 +272,30 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
     keys[i] = key;
   }
   __syncthreads();
-  for (int size = 2; size <= n_pad; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < (n_pad >> 1); i += kSchedThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const unsigned long long a = keys[lo], c = keys[hi];
-        if ((a > c) == asc) {
-          keys[lo] = c;
-          keys[hi] = a;
-        }
+  // Bitonic network. A compare-exchange of stride <= 32 pairs keys inside the
+  // 64-key window of the warp that owns pairs [32j, 32j + 32), so those stages
+  // synchronise the warp only; wider strides synchronise the block.
+  const int half = n_pad >> 1;
+  const int local_sizes = n_pad < 64 ? n_pad : 64;
+  for (int base = wid * 32; base < half; base += kSchedThreads) {
+    for (int size = 2; size <= local_sizes; size <<= 1)
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        if (base + lane < half) bitonic_cx(keys, base + lane, stride, size);
+        __syncwarp();
       }
+  }
+  __syncthreads();
+  for (int size = 128; size <= n_pad; size <<= 1) {
+    for (int stride = size >> 1; stride > 32; stride >>= 1) {
+      for (int i = tid; i < half; i += kSchedThreads) bitonic_cx(keys, i, stride, size);
       __syncthreads();
     }
+    for (int base = wid * 32; base < half; base += kSchedThreads)
+      for (int stride = 32; stride > 0; stride >>= 1) {
+        if (base + lane < half) bitonic_cx(keys, base + lane, stride, size);
+        __syncwarp();
+      }
+    __syncthreads();
   }
 
   // A_m = B + sum of the first m sorted survivals (double-float); each thread
@@ -270,6 +369,24 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   }
 }
 
+// Launch with programmatic stream serialization: the kernel's prologue may
+// overlap its predecessor; it calls griddepcontrol.wait before reading what
+// earlier kernels wrote.
+template <typename Kern>
+cudaError_t launch_pdl(Kern kernel, int grid, int block, size_t smem, cudaStream_t s, SchedParams p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 }  // namespace
 
 size_t schedule_smem_bytes(int32_t B, int32_t K) {
@@ -281,19 +398,18 @@ size_t schedule_smem_bytes(int32_t B, int32_t K) {
 cudaError_t launch_confidence(const SchedParams& p, cudaStream_t s) {
   const int items = p.B * p.K;
   const int blocks = (items + 7) / 8;
-  if (p.dtype == DS_BF16)
-    confidence_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
-  else
-    confidence_kernel<float><<<blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  if (p.dtype == DS_BF16 && p.d <= kStageMaxD)  // at most 24 KB of w_h per CTA
+    return launch_pdl(confidence_kernel<__nv_bfloat16, true>, blocks, 256,
+                      sizeof(__nv_bfloat16) * (size_t)p.d, s, p);
+  if (p.dtype == DS_BF16) return launch_pdl(confidence_kernel<__nv_bfloat16, false>, blocks, 256, 0, s, p);
+  return launch_pdl(confidence_kernel<float, false>, blocks, 256, 0, s, p);
 }
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s) {
   static cudaError_t attr = cudaFuncSetAttribute(
       schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 8);
   if (attr != cudaSuccess) return attr;
-  schedule_kernel<<<1, kSchedThreads, schedule_smem_bytes(p.B, p.K), s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(schedule_kernel, 1, kSchedThreads, schedule_smem_bytes(p.B, p.K), s, p);
 }
 
 }  // namespace ds

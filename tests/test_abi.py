@@ -100,5 +100,15 @@ def test_host_validation_rejects_without_launching(lib):
     assert lib.ds_rnn_pack_weights(fake, fake, 96, 128, 1, fake, None) == 1
     a = _lib.StsArgs(N=4, K=2, n_grid=8, n_bins=10)      # sizes fine, pointers missing
     assert lib.ds_sts_fit(ctypes.byref(a), None) == 1
+    # host staging of target rows: argument checks enqueue nothing
+    lens = (ctypes.c_int32 * 4)(0, 1, 2, 3)
+    n = ctypes.c_uint64(7)
+    assert lib.ds_copy_scheduled_rows(None, fake, 4, 3, 64, lens, ctypes.byref(n), None) == 1
+    assert lib.ds_copy_scheduled_rows(fake, None, 4, 3, 64, lens, ctypes.byref(n), None) == 1
+    assert lib.ds_copy_scheduled_rows(fake, fake, 4, 3, 64, None, ctypes.byref(n), None) == 1
+    assert lib.ds_copy_scheduled_rows(fake, fake, 0, 3, 64, lens, ctypes.byref(n), None) == 1
+    assert lib.ds_copy_scheduled_rows(fake, fake, 4, -1, 64, lens, ctypes.byref(n), None) == 1
+    assert lib.ds_copy_scheduled_rows(fake, fake, 4, 3, 0, lens, ctypes.byref(n), None) == 1
+    assert n.value == 7                                  # untouched on a rejected call
     assert _lib.ds_status_string(7) == "non-finite logit or empty distribution"
     assert _lib.ds_version() == "0.1.0"
