@@ -99,6 +99,16 @@ def test_ragged_multitile_mixed_temperatures(ds, bf16):
 
 
 @pytest.mark.parametrize("bf16", [True, False])
+def test_ragged_all_greedy(ds, bf16):
+    """Every request greedy (T = 0): each draw is the exact argmax of z + b,
+    first index on ties, on every row of a ragged multi-tile case."""
+    inp = _ragged(bf16, (0.0,), 29)
+    _, g = _run(inp)
+    rep = _parity.assert_parity(inp, g, SEED)
+    assert rep["draft"]["draws"] == 37 * 5
+
+
+@pytest.mark.parametrize("bf16", [True, False])
 def test_ragged_strided_projection(ds, bf16):
     """The draw without the token-major copy of P (r strided rows per chunk)."""
     inp = _ragged(bf16, (0.0, 0.6, 1.0), 17, r=64)
