@@ -142,19 +142,14 @@ __device__ __forceinline__ bool sample_chunk_fast(const G16& g16, const uint32_t
   int fref = 0;
   if (!fast_chunk_ok(zp, g16, fref)) return false;
   const FastConsts k = make_fast_consts(g16, fref);
-  float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
+  float2 s = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < 16; ++i)
-    fast_pair(zp[i], make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])), k,
-              shi, slo);
-  const float hi = __fadd_rn(shi.x, shi.y);  // exact: multiples of 2^-15 below 1024
-  const float lo = __fadd_rn(slo.x, slo.y);
-  if (!(shi.x >= 0.f && shi.x < kFastHiLimit && shi.y >= 0.f && shi.y < kFastHiLimit &&
-        isfinite(lo)))
-    return false;
-  const DF r = fast_two_sum(hi, lo);
-  rec.hi = r.hi;
-  rec.lo = r.lo;
+    fast_pair(zp[i], make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])), k, s);
+  const float sum = __fadd_rn(s.x, s.y);
+  if (!(sum >= 0.f && isfinite(sum))) return false;
+  rec.hi = sum;
+  rec.lo = 0.f;
   rec.ref = fref;
   rec.idx = -2;  // fast-path record
   return true;
@@ -171,7 +166,7 @@ __device__ __forceinline__ bool final_chunk_fast(const EpiRow& c, const uint32_t
   if (!fast_span_ok(tp, c.g16.G, c.Np)) return false;
   if (res && !fast_span_ok(zp, c.g16.G, c.Nq)) return false;
   const FastConsts kp = make_fast_consts(c.g16, c.Np);
-  float2 shi = make_float2(0.f, 0.f), slo = make_float2(0.f, 0.f);
+  float2 s = make_float2(0.f, 0.f);
   if (res) {
     const FastConsts kq = make_fast_consts(c.g16, c.Nq);
 #pragma unroll
@@ -179,21 +174,16 @@ __device__ __forceinline__ bool final_chunk_fast(const EpiRow& c, const uint32_t
       const float2 wp = fast_w2(tp[i], make_float2(0.f, 0.f), kp);
       const float2 wq =
           fast_w2(zp[i], make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])), kq);
-      grid_acc(make_float2(residual_w(wp.x, wq.x, c.Rhi, c.Rlo), residual_w(wp.y, wq.y, c.Rhi, c.Rlo)),
-               kp, shi, slo);
+      s = __fadd2_rn(s, make_float2(residual_w(wp.x, wq.x, c.Rhi, c.Rlo), residual_w(wp.y, wq.y, c.Rhi, c.Rlo)));
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) fast_pair(tp[i], make_float2(0.f, 0.f), kp, shi, slo);
+    for (int i = 0; i < 16; ++i) fast_pair(tp[i], make_float2(0.f, 0.f), kp, s);
   }
-  const float hi = __fadd_rn(shi.x, shi.y);
-  const float lo = __fadd_rn(slo.x, slo.y);
-  if (!(shi.x >= 0.f && shi.x < kFastHiLimit && shi.y >= 0.f && shi.y < kFastHiLimit &&
-        isfinite(lo)))
-    return false;
-  const DF r = fast_two_sum(hi, lo);
-  rec.hi = r.hi;
-  rec.lo = r.lo;
+  const float sum = __fadd_rn(s.x, s.y);
+  if (!(sum >= 0.f && isfinite(sum))) return false;
+  rec.hi = sum;
+  rec.lo = 0.f;
   rec.ref = 0;
   rec.idx = -2;  // fast-path record
   return true;

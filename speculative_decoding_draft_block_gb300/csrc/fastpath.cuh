@@ -16,10 +16,10 @@
 // [2^23, 2^24), where the float spacing is 1); otherwise the general path of
 // common.cuh is used.
 //
-// Chunk sums on this path are exact up to ~2^-36 relative: each weight is split
-// on a fixed 2^-15 grid, w = w_hi + w_lo with w_hi = (w + 384) - 384 (exact),
-// the w_hi are summed exactly (multiples of 2^-15 below 512) and the small w_lo
-// separately. The caller checks that the high sum stayed below 512.
+// A chunk's weights are summed in float32 (each lane of a packed pair, then the
+// two lanes): a relative error of about 1e-7, the size of the weights' own
+// error (ex2.approx, and the float32 tensor-core bias). The caller sends a
+// chunk whose sum is not finite to the general path.
 //
 // Two tokens are processed per instruction with the packed .f32x2 operations
 // (IEEE round-to-nearest per lane, so a scalar evaluation gives identical bits).
@@ -32,9 +32,7 @@
 namespace ds {
 
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-constexpr float kGrid = 384.0f;        // 1.5 * 2^8: ulp 2^-15 on [256, 512)
 constexpr float kFastSpan = 96.0f;     // max (zmax - zmin) * G on the fast path
-constexpr float kFastHiLimit = 511.0f;
 
 struct G16 {
   float G, gl, gf;  // g = G + gl exactly to ~2^-40; gf = g rounded to fp32
@@ -88,32 +86,16 @@ __device__ __forceinline__ float2 fast_w2(uint32_t zw, float2 b2, const FastCons
                      __uint_as_float(__float_as_uint(p1) + (__float_as_uint(m2.y) << 23)));
 }
 
-// Exact grid-split accumulation of two weights in [0, 512).
-__device__ __forceinline__ void grid_acc(float2 w2, const FastConsts& k, float2& shi, float2& slo) {
-  const float2 tt = __fadd2_rn(w2, make_float2(kGrid, kGrid));
-  const float2 wh = __fadd2_rn(tt, make_float2(-kGrid, -kGrid));
-  const float2 wl = __ffma2_rn(wh, k.neg1, w2);
-  shi = __fadd2_rn(shi, wh);
-  slo = __fadd2_rn(slo, wl);
-}
-
-// Weights of the two tokens packed in zw, accumulated into (shi, slo).
-__device__ __forceinline__ void fast_pair(uint32_t zw, float2 b2, const FastConsts& k, float2& shi,
-                                          float2& slo) {
-  grid_acc(fast_w2(zw, b2, k), k, shi, slo);
+// Weights of the two tokens packed in zw, accumulated into s (float32, one
+// rounding per addition).
+__device__ __forceinline__ void fast_pair(uint32_t zw, float2 b2, const FastConsts& k, float2& s) {
+  s = __fadd2_rn(s, fast_w2(zw, b2, k));
 }
 
 // Residual weight max(0, wp - R * wq) of one token, R = Rhi + Rlo (two FMAs,
 // the order every side uses).
 __device__ __forceinline__ float residual_w(float wp, float wq, float Rhi, float Rlo) {
   return fmaxf(__fmaf_rn(-wq, Rlo, __fmaf_rn(-wq, Rhi, wp)), 0.f);
-}
-
-// Scalar split of one weight on the same grid (for prefix sums in the locate).
-__device__ __forceinline__ void fast_split(float w, float& wh, float& wl) {
-  const float tt = __fadd_rn(w, kGrid);
-  wh = __fadd_rn(tt, -kGrid);
-  wl = __fmaf_rn(wh, -1.0f, w);
 }
 
 // Chunk predicate against a given reference (the row-global references of the

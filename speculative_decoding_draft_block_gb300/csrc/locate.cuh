@@ -1,5 +1,5 @@
-// Draw of one row from its chunk and group records (the "locate"), shared by
-// the standalone locate kernel and the persistent draft kernel.
+// Draw of one row from its chunk and group records (the "locate"), run by
+// sample_locate_kernel with one CTA per row.
 #pragma once
 #include <cuda_bf16.h>
 #include <float.h>
