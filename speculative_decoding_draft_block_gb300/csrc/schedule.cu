@@ -20,8 +20,12 @@
 //                      cycle and runs before the programmatic-launch wait, so
 //                      it overlaps the end of the draft.
 //   schedule_kernel    one CTA: survival cumprod, bitonic sort of 64-bit keys
-//                      (survival descending, then k, then b) in shared memory
-//                      (stages of stride <= 32 synchronise one warp only),
+//                      (survival descending, then k, then b): for 2048-8192
+//                      keys each thread holds E = B*K/1024 of them in
+//                      registers (small strides in registers, middle ones by
+//                      warp shuffles, only strides >= 32E in shared memory);
+//                      otherwise in shared memory, stages of stride <= 32
+//                      synchronising one warp only;
 //                      double-float prefix scan of A, first drop of J tested
 //                      without division: J' > J <=> SPS(N+1) (A+s) N > SPS(N) A (N+1).
 //                      (double precision runs at a small fraction of the float
@@ -181,17 +185,88 @@ __device__ __forceinline__ bool gains(float sps1, float sps0, DF A, float s, int
 
 constexpr int kSchedThreads = 1024;
 
+// Shared-memory position of key w: the low four bits are XORed with bits 4-7,
+// so that a warp reading 64-bit words either contiguously or E words apart
+// (the blocked layout of bitonic_regs) touches each bank pair once per phase.
+// Positions stay inside w's own 16-word block.
+__device__ __forceinline__ int swz(int w) { return w ^ ((w >> 4) & 15); }
+
 // One compare-exchange of pair i at the given stride, ascending within blocks
 // of `size` keys whose index has the `size` bit clear.
 __device__ __forceinline__ void bitonic_cx(unsigned long long* keys, int i, int stride, int size) {
   const int lo = 2 * i - (i & (stride - 1));
   const int hi = lo + stride;
   const bool asc = (lo & size) == 0;
-  const unsigned long long a = keys[lo], c = keys[hi];
+  const unsigned long long a = keys[swz(lo)], c = keys[swz(hi)];
   if ((a > c) == asc) {
-    keys[lo] = c;
-    keys[hi] = a;
+    keys[swz(lo)] = c;
+    keys[swz(hi)] = a;
   }
+}
+
+// Sort key of candidate i = b*K + k: survival descending, then k, then b;
+// padding (i >= n) sorts last.
+__device__ __forceinline__ unsigned long long sched_key(const SchedParams& p, int i, int n, int K) {
+  if (i >= n) return ~0ull;
+  const int b = i / K, k = i - b * K;
+  const uint32_t hi = 0xffffffffu - __float_as_uint(fmaxf(p.survival[i], 0.f));
+  return ((unsigned long long)hi << 32) | ((unsigned long long)k << 16) | (unsigned long long)b;
+}
+
+// Bitonic sort of n_pad = E * kSchedThreads keys with thread t holding keys
+// t*E .. t*E + E - 1 in registers (built there from the survivals): strides below E are exchanged in registers,
+// strides E .. 32E - 1 between the lanes of a warp (shuffles), and only
+// strides of 32E and more through shared memory. Same network, same result
+// as the shared-memory sort; the keys end sorted in `keys`.
+template <int E>
+__device__ void bitonic_regs(unsigned long long* keys, int n_pad, int tid, const SchedParams& p, int n,
+                             int K) {
+  unsigned long long v[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) v[j] = sched_key(p, tid * E + j, n, K);
+  for (int size = 2; size <= n_pad; size <<= 1) {
+    int stride = size >> 1;
+    if (stride >= 32 * E) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) keys[swz(tid * E + j)] = v[j];
+      __syncthreads();
+      for (; stride >= 32 * E; stride >>= 1) {
+        for (int i = tid; i < (n_pad >> 1); i += kSchedThreads) bitonic_cx(keys, i, stride, size);
+        __syncthreads();
+      }
+#pragma unroll
+      for (int j = 0; j < E; ++j) v[j] = keys[swz(tid * E + j)];
+    }
+    for (; stride >= E; stride >>= 1) {
+      const int d = stride / E;  // partner lane distance
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const int i = tid * E + j;
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], d);
+        const bool keep_min = ((i & stride) == 0) == ((i & size) == 0);
+        v[j] = keep_min ? (o < v[j] ? o : v[j]) : (o > v[j] ? o : v[j]);
+      }
+    }
+#pragma unroll
+    for (int st = E / 2; st > 0; st >>= 1) {
+      if (st <= stride) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          if ((j & st) == 0) {
+            const bool asc = ((tid * E + j) & size) == 0;
+            const unsigned long long a = v[j], c = v[j | st];
+            if ((a > c) == asc) {
+              v[j] = c;
+              v[j | st] = a;
+            }
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < E; ++j) keys[swz(tid * E + j)] = v[j];
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) {
@@ -261,41 +336,41 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
 
   int n_pad = 1;
   while (n_pad < n) n_pad <<= 1;
-  for (int i = tid; i < n_pad; i += kSchedThreads) {
-    unsigned long long key = ~0ull;
-    if (i < n) {
-      const int b = i / K, k = i - b * K;
-      const float s = p.survival[(size_t)b * K + k];
-      const uint32_t hi = 0xffffffffu - __float_as_uint(fmaxf(s, 0.f));
-      key = ((unsigned long long)hi << 32) | ((unsigned long long)k << 16) | (unsigned long long)b;
+  // Bitonic network: registers and shuffles for 2048 to 8192 keys; otherwise
+  // in shared memory, where a compare-exchange of stride <= 32 pairs keys
+  // inside the 64-key window of the warp that owns pairs [32j, 32j + 32), so
+  // those stages synchronise the warp only.
+  if (n_pad == 2 * kSchedThreads) {
+    bitonic_regs<2>(keys, n_pad, tid, p, n, K);
+  } else if (n_pad == 4 * kSchedThreads) {
+    bitonic_regs<4>(keys, n_pad, tid, p, n, K);
+  } else if (n_pad == 8 * kSchedThreads) {
+    bitonic_regs<8>(keys, n_pad, tid, p, n, K);
+  } else {
+    for (int i = tid; i < n_pad; i += kSchedThreads) keys[swz(i)] = sched_key(p, i, n, K);
+    __syncthreads();
+    const int half = n_pad >> 1;
+    const int local_sizes = n_pad < 64 ? n_pad : 64;
+    for (int base = wid * 32; base < half; base += kSchedThreads) {
+      for (int size = 2; size <= local_sizes; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          if (base + lane < half) bitonic_cx(keys, base + lane, stride, size);
+          __syncwarp();
+        }
     }
-    keys[i] = key;
-  }
-  __syncthreads();
-  // Bitonic network. A compare-exchange of stride <= 32 pairs keys inside the
-  // 64-key window of the warp that owns pairs [32j, 32j + 32), so those stages
-  // synchronise the warp only; wider strides synchronise the block.
-  const int half = n_pad >> 1;
-  const int local_sizes = n_pad < 64 ? n_pad : 64;
-  for (int base = wid * 32; base < half; base += kSchedThreads) {
-    for (int size = 2; size <= local_sizes; size <<= 1)
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        if (base + lane < half) bitonic_cx(keys, base + lane, stride, size);
-        __syncwarp();
+    __syncthreads();
+    for (int size = 128; size <= n_pad; size <<= 1) {
+      for (int stride = size >> 1; stride > 32; stride >>= 1) {
+        for (int i = tid; i < half; i += kSchedThreads) bitonic_cx(keys, i, stride, size);
+        __syncthreads();
       }
-  }
-  __syncthreads();
-  for (int size = 128; size <= n_pad; size <<= 1) {
-    for (int stride = size >> 1; stride > 32; stride >>= 1) {
-      for (int i = tid; i < half; i += kSchedThreads) bitonic_cx(keys, i, stride, size);
+      for (int base = wid * 32; base < half; base += kSchedThreads)
+        for (int stride = 32; stride > 0; stride >>= 1) {
+          if (base + lane < half) bitonic_cx(keys, base + lane, stride, size);
+          __syncwarp();
+        }
       __syncthreads();
     }
-    for (int base = wid * 32; base < half; base += kSchedThreads)
-      for (int stride = 32; stride > 0; stride >>= 1) {
-        if (base + lane < half) bitonic_cx(keys, base + lane, stride, size);
-        __syncwarp();
-      }
-    __syncthreads();
   }
 
   // A_m = B + sum of the first m sorted survivals (double-float); each thread
@@ -304,7 +379,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
   DF local = {0.f, 0.f};
   for (int i = i0; i < i1; ++i)
-    local = df_add(local, DF{__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32)), 0.f});
+    local = df_add(local, DF{__uint_as_float(0xffffffffu - (uint32_t)(keys[swz(i)] >> 32)), 0.f});
   // block exclusive scan of `local`
   DF incl = local;
   for (int o = 1; o < 32; o <<= 1) {
@@ -329,7 +404,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   int first_drop = INT_MAX;
   DF a_prev = df_add(DF{(float)B, 0.f}, excl);
   for (int i = i0; i < i1; ++i) {
-    const float sv = __uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32));
+    const float sv = __uint_as_float(0xffffffffu - (uint32_t)(keys[swz(i)] >> 32));
     const int nb = B + i;  // verified tokens before adding candidate i
     if (!gains(sps_at(p.sps, p.n_max, nb + 1), sps_at(p.sps, p.n_max, nb), a_prev, sv, nb)) {
       first_drop = i;
@@ -354,7 +429,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   }
 
   for (int i = tid; i < M; i += kSchedThreads) {
-    const unsigned long long key = keys[i];
+    const unsigned long long key = keys[swz(i)];
     const int k = (int)((key >> 16) & 0xffff), b = (int)(key & 0xffff);
     atomicMax(&p.sched_len[b], k + 1);
   }
@@ -364,7 +439,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedParams p) 
   } else if (M - 1 >= i0 && M - 1 < i1) {
     DF a = df_add(DF{(float)B, 0.f}, excl);
     for (int i = i0; i < M; ++i)
-      a = df_add(a, DF{__uint_as_float(0xffffffffu - (uint32_t)(keys[i] >> 32)), 0.f});
+      a = df_add(a, DF{__uint_as_float(0xffffffffu - (uint32_t)(keys[swz(i)] >> 32)), 0.f});
     p.objective[0] = objective_of(sps_at(p.sps, p.n_max, B + M), a, B + M);
   }
 }
