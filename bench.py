@@ -458,14 +458,14 @@ MODE_NAMES = {0: "greedy_earlystop", 1: "fixed_k", 2: "threshold", 3: "async"}
 def time_e2e(args, cyc, inp, stream, dev, seed0, ws):
     """End to end through the public API (``HostPipeline``), as a caller holding
     each step's inputs in pinned host memory runs it: the draft's inputs are
-    copied in, draft and schedule run, the scheduled lengths come back (4 B per
-    request), only the target rows that verify reads (rows 0..L_b of request b,
-    one contiguous copy per request) go in, verify runs, and the emitted tokens
-    come back. Each step also starts the copy of the next step's draft inputs
+    copied in, draft and schedule run, only the target rows that verify reads
+    (rows 0..L_b of request b) are fetched from the pinned host tensor by a
+    kernel that reads L_b on the device, verify runs, and the scheduled lengths
+    and emitted tokens come back. Each step also starts the copy of the next step's draft inputs
     (independent request groups served in turn), which overlaps the current
     step. Every copy is inside the timed region: the copy stream waits for the
     start event, and the last step stages nothing ahead. The bytes are counted
-    from the copies."""
+    from the copies (the fetched rows on a device counter)."""
     import numpy as np
     import torch
     from speculative_decoding_draft_block_gb300.cycle import HostPipeline, to_host_pinned
@@ -478,20 +478,22 @@ def time_e2e(args, cyc, inp, stream, dev, seed0, ws):
     barrier(ws)
     E = max(1, args.e2e_steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h2d = []
+    pipe.reset_counts()
     e0.record(stream)
     pipe.copy_stream.wait_event(e0)
     for i in range(E):
         pipe.step(host, seed0 + 5000 + i, next_host=host if i + 1 < E else None)
-        h2d.append(pipe.h2d_bytes)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws)
     return {"value": ws * B * K * E / e2e_s, "unit": "tokens/s",
-            "h2d_bytes_per_step": int(np.mean(h2d)), "d2h_bytes_per_step": int(pipe.d2h_bytes), "steps": E,
+            "h2d_bytes_per_step": int(pipe.h2d_bytes() / E), "d2h_bytes_per_step": int(pipe.d2h_bytes),
+            "steps": E,
             "copied": list(DRAFT_KEYS) + ["target_logits rows 0..L_b", "sched_len", "out_tokens",
                                            "num_emitted"],
-            "overlap": "next step's draft inputs copied during the current step (copy stream)"}
+            "overlap": "next step's draft inputs copied during the current step (copy stream); "
+                       "target rows 0..L_b fetched by a kernel from pinned host memory, L_b read "
+                       "on the device"}
 
 
 def main():
@@ -505,7 +507,7 @@ def main():
                     help="scheduler: 0 greedy + early stop, 1 fixed K, 2 survival threshold, "
                          "3 asynchronous (budget from two cycles back)")
     ap.add_argument("--threshold", type=float, default=0.5, help="survival threshold of mode 2")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",

@@ -382,6 +382,24 @@ ds_status ds_verify_static(const ds_verify_args* args, ds_stream_t stream);
 ds_status ds_copy_scheduled_rows(void* dst, const void* src, int32_t B, int32_t K, size_t row_bytes,
                                  const int32_t* lens, uint64_t* bytes_out, ds_stream_t stream);
 
+/* The same rows, fetched by a kernel that reads the host buffer over the
+ * CPU-GPU link, with L_b taken from the device: `sched_len` is
+ * ds_confidence_schedule's device output, so the call can follow the schedule
+ * on the same stream with no host round trip (and no per-request copy set-up).
+ *   dst          device [B][K+1][row_bytes]
+ *   src          pinned host memory of the same layout, mapped into the
+ *                device's address space (memory from cudaHostAlloc or
+ *                cudaMallocHost on a system with unified addressing)
+ *   sched_len    device [B]; L_b = min(max(sched_len[b], 0), K)
+ *   bytes_total  optional device counter (unsigned 64-bit): the bytes fetched
+ *                are added to it
+ * Errors: DS_ERR_INVALID_ARG for a null pointer, B < 1, K < 0, row_bytes
+ * not a positive multiple of 16, `dst` or `src` not 16-byte aligned, or `src`
+ * not host memory the runtime maps for the device (cudaHostGetDevicePointer
+ * fails); nothing is launched then. */
+ds_status ds_fetch_scheduled_rows(void* dst, const void* src, int32_t B, int32_t K, size_t row_bytes,
+                                  const int32_t* sched_len, uint64_t* bytes_total, ds_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status and identification                                                 */
 /* ------------------------------------------------------------------------ */

@@ -27,7 +27,8 @@ EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspa
            "ds_draft_block", "ds_sched_workspace_bytes", "ds_confidence_schedule",
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
            "ds_version", "ds_transpose_projection", "ds_verify_static", "ds_sts_workspace_bytes",
-           "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights", "ds_copy_scheduled_rows")
+           "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights", "ds_copy_scheduled_rows",
+           "ds_fetch_scheduled_rows")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -114,6 +115,8 @@ def load():
     lib.ds_copy_scheduled_rows.argtypes = [_vp, _vp, _i32, _i32, ctypes.c_size_t, _vp,
                                            ctypes.POINTER(ctypes.c_uint64), _vp]
     lib.ds_copy_scheduled_rows.restype = ctypes.c_int
+    lib.ds_fetch_scheduled_rows.argtypes = [_vp, _vp, _i32, _i32, ctypes.c_size_t, _vp, _vp, _vp]
+    lib.ds_fetch_scheduled_rows.restype = ctypes.c_int
     lib.ds_check_status.argtypes = [_vp, _vp]
     lib.ds_check_status.restype = ctypes.c_int
     lib.ds_status_string.argtypes = [ctypes.c_int]
@@ -347,6 +350,27 @@ def ds_copy_scheduled_rows(dst, src, lens, stream=None):
                                          ctypes.c_void_p(lens.data_ptr()), ctypes.byref(n),
                                          _stream(stream))
     return code, int(n.value)
+
+
+def ds_fetch_scheduled_rows(dst, src, sched_len, bytes_total=None, stream=None):
+    """Rows 0..L_b of each request's target logits, fetched by a kernel from
+    the pinned host tensor ``src`` into device ``dst`` (both [B, K+1, V]);
+    ``sched_len``: device int32 [B]; ``bytes_total``: optional device int64
+    counter the fetched bytes are added to."""
+    if dst.dim() != 3 or tuple(src.shape) != tuple(dst.shape) or src.dtype != dst.dtype:
+        raise ValueError("dst and src must be [B, K+1, V] tensors of one dtype")
+    if src.is_cuda or not src.is_contiguous() or not src.is_pinned():
+        raise ValueError("src must be a contiguous pinned host tensor")
+    if sched_len.dtype != torch.int32 or sched_len.numel() != dst.shape[0]:
+        raise ValueError("sched_len must be a device int32 tensor [B]")
+    if bytes_total is not None and (bytes_total.dtype != torch.int64 or bytes_total.numel() < 1):
+        raise ValueError("bytes_total must be a device int64 tensor")
+    return load().ds_fetch_scheduled_rows(_ptr(dst, "dst"), ctypes.c_void_p(src.data_ptr()),
+                                          int(dst.shape[0]), int(dst.shape[1]) - 1,
+                                          int(dst.shape[2]) * dst.element_size(),
+                                          _ptr(sched_len, "sched_len"),
+                                          None if bytes_total is None else _ptr(bytes_total, "bytes_total"),
+                                          _stream(stream))
 
 
 def ds_check_status(status, stream=None):

@@ -544,6 +544,25 @@ ds_status ds_copy_scheduled_rows(void* dst, const void* src, int32_t B, int32_t 
   return DS_OK;
 }
 
+ds_status ds_fetch_scheduled_rows(void* dst, const void* src, int32_t B, int32_t K, size_t row_bytes,
+                                  const int32_t* sched_len, uint64_t* bytes_total, ds_stream_t stream) {
+  if (dst == nullptr || src == nullptr || sched_len == nullptr || B < 1 || K < 0 || row_bytes == 0 ||
+      row_bytes % 16 != 0 || !aligned16(dst) || !aligned16(src) || ((uintptr_t)sched_len & 3u) != 0 ||
+      ((uintptr_t)bytes_total & 7u) != 0)
+    return DS_ERR_INVALID_ARG;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  void* src_dev = nullptr;
+  if (cudaHostGetDevicePointer(&src_dev, const_cast<void*>(src), 0) != cudaSuccess) {
+    (void)cudaGetLastError();  // not mapped host memory: clear the error, launch nothing
+    return DS_ERR_INVALID_ARG;
+  }
+  if (!aligned16(src_dev)) return DS_ERR_INVALID_ARG;
+  return from_cuda(launch_fetch_rows(dst, src_dev, B, K, row_bytes, sched_len,
+                                     reinterpret_cast<unsigned long long*>(bytes_total),
+                                     (cudaStream_t)stream));
+}
+
 ds_status ds_check_status(const int32_t* device_status, ds_stream_t stream) {
   if (device_status == nullptr) return DS_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DS_ERR_CUDA;

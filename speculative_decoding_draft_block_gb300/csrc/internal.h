@@ -216,6 +216,10 @@ cudaError_t launch_sample_tile(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_sample_locate(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s);
+// Rows 0..L_b of each request, host (mapped, src_dev its device address) ->
+// device, L_b from the device word array sched_len; bytes (optional) += count.
+cudaError_t launch_fetch_rows(void* dst, const void* src_dev, int32_t B, int32_t K, size_t row_bytes,
+                              const int32_t* sched_len, unsigned long long* bytes, cudaStream_t s);
 cudaError_t launch_confidence(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t s);

@@ -324,4 +324,52 @@ cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+namespace {
+
+constexpr int kFetchThreads = 256;
+constexpr int kFetchChunk16 = 4096;  // 16-byte words per CTA (64 KB)
+
+// Target rows 0..L_b of request b from host memory mapped into the device's
+// address space: CTA (x, b) copies words [x * kFetchChunk16, ...) of the
+// request's first L_b + 1 rows, four 16-byte loads in flight per thread.
+// L_b comes from the device (the schedule's output), so no host round trip
+// sits between the schedule and verify.
+__global__ void __launch_bounds__(kFetchThreads)
+    fetch_rows_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int K, size_t row16,
+                      const int32_t* __restrict__ sched_len, unsigned long long* bytes) {
+  const int b = blockIdx.y;
+  int L = sched_len[b];
+  L = L < 0 ? 0 : (L > K ? K : L);
+  const size_t n16 = (size_t)(L + 1) * row16;
+  if (bytes != nullptr && blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(bytes, (unsigned long long)n16 * 16);
+  const size_t c0 = (size_t)blockIdx.x * kFetchChunk16;
+  if (c0 >= n16) return;
+  const size_t c1 = c0 + kFetchChunk16 < n16 ? c0 + kFetchChunk16 : n16;
+  const size_t base = (size_t)b * (size_t)(K + 1) * row16;
+  const uint4* sp = src + base;
+  uint4* dp = dst + base;
+  size_t i = c0 + threadIdx.x;
+  for (; i + 3 * kFetchThreads < c1; i += 4 * kFetchThreads) {
+    const uint4 v0 = sp[i], v1 = sp[i + kFetchThreads], v2 = sp[i + 2 * kFetchThreads],
+                v3 = sp[i + 3 * kFetchThreads];
+    dp[i] = v0;
+    dp[i + kFetchThreads] = v1;
+    dp[i + 2 * kFetchThreads] = v2;
+    dp[i + 3 * kFetchThreads] = v3;
+  }
+  for (; i < c1; i += kFetchThreads) dp[i] = sp[i];
+}
+
+}  // namespace
+
+cudaError_t launch_fetch_rows(void* dst, const void* src_dev, int32_t B, int32_t K, size_t row_bytes,
+                              const int32_t* sched_len, unsigned long long* bytes, cudaStream_t s) {
+  const size_t row16 = row_bytes / 16;
+  const size_t req16 = (size_t)(K + 1) * row16;
+  dim3 grid((unsigned)((req16 + kFetchChunk16 - 1) / kFetchChunk16), (unsigned)B);
+  fetch_rows_kernel<<<grid, kFetchThreads, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src_dev),
+                                                   K, row16, sched_len, bytes);
+  return cudaGetLastError();
+}
+
 }  // namespace ds

@@ -177,15 +177,16 @@ class HostPipeline:
 
     A step copies its draft inputs (base logits, anchor, temperatures, h) into
     one of two device slots on a copy stream, runs the draft and the schedule,
-    reads the scheduled lengths back, copies only the target rows that verify
-    reads (rows 0..L_b of request b, ``ds_copy_scheduled_rows``), verifies and
-    copies the emitted tokens back. Given ``next_host``, a step also starts the
-    copy of the next step's draft inputs into the other slot at once, so that
-    it overlaps this step's kernels and target-row copies; that needs the next
-    step's inputs to be known already (for instance two request groups served
-    in turn). Events order every reuse: a slot is refilled only after the
-    verify that last read it, and a draft waits for its slot's copy. Weights
-    and tables stay resident in the ``DeviceCycle``.
+    then ``ds_fetch_scheduled_rows`` pulls the target rows that verify reads
+    (rows 0..L_b of request b) straight from the pinned host tensor, with L_b
+    read on the device: nothing waits on the host inside a step. Verify runs
+    and the scheduled lengths and emitted tokens are copied back. Given
+    ``next_host``, a step also starts the copy of the next step's draft inputs
+    into the other slot at once, so that it overlaps this step; that needs the
+    next step's inputs to be known already (for instance two request groups
+    served in turn). Events order every reuse: a slot is refilled only after
+    the verify that last read it, and a draft waits for its slot's copy.
+    Weights and tables stay resident in the ``DeviceCycle``.
     """
 
     def __init__(self, cyc, stream=None):
@@ -199,18 +200,27 @@ class HostPipeline:
         self.free = [torch.cuda.Event(), torch.cuda.Event()]
         self.done = [torch.cuda.Event(), torch.cuda.Event()]
         B, K = cyc.B, cyc.K
-        self.lens = torch.empty((B,), dtype=torch.int32).pin_memory()
+        self.lens = [torch.empty((B,), dtype=torch.int32).pin_memory() for _ in range(2)]
         self.out_tokens = [torch.empty((B, K + 1), dtype=torch.int32).pin_memory() for _ in range(2)]
         self.num_emitted = [torch.empty((B,), dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.rows_bytes = torch.zeros((1,), dtype=torch.int64, device=dev)  # fetched target-row bytes
+        self.input_bytes = 0    # staged draft-input bytes
         self._next = 0          # slot of the next unstaged step
-        self._staged = None     # (slot, host inputs, bytes) of a copy already enqueued
-        self.h2d_bytes = 0      # bytes copied in by the last step
-        self.d2h_bytes = (self.lens.numel() + self.out_tokens[0].numel() + self.num_emitted[0].numel()) * 4
+        self._staged = None     # (slot, host inputs) of a copy already enqueued
+        self.d2h_bytes = (B + B * (K + 1) + B) * 4  # per step: lengths, tokens, counts
+
+    def reset_counts(self):
+        self.input_bytes = 0
+        self.rows_bytes.zero_()
+
+    def h2d_bytes(self):
+        """Bytes copied to the device since the last reset (reads the device
+        counter: call once the steps are done)."""
+        return self.input_bytes + int(self.rows_bytes.item())
 
     def _stage(self, slot, host):
         cs = self.copy_stream
         cs.wait_event(self.free[slot])
-        n = 0
         with torch.cuda.stream(cs):
             for k in DRAFT_INPUT_KEYS:
                 dst, src = self.slots[slot][k], host[k]
@@ -220,44 +230,40 @@ class HostPipeline:
                                          (k, src.dtype, dst.dtype))
                     src = src.view(dst.dtype)
                 dst.copy_(src, non_blocking=True)
-                n += src.numel() * src.element_size()
+                self.input_bytes += src.numel() * src.element_size()
         self.ready[slot].record(cs)
-        return n
 
     def step(self, host, seed, next_host=None):
         """One cycle on ``host`` (pinned tensors: the draft inputs and
         ``target_logits`` [B, K+1, V]). Returns the pinned host tensors
-        (out_tokens, num_emitted) and the event after which they hold this
-        step's results; they are reused two steps later."""
+        (lengths, out_tokens, num_emitted) and the event after which they hold
+        this step's results; they are reused two steps later."""
         cyc, s = self.cyc, self.stream
         if self._staged is not None and self._staged[1] is host:
-            slot, _, n_in = self._staged
+            slot = self._staged[0]
         else:
             slot = self._next
-            n_in = self._stage(slot, host)
+            self._stage(slot, host)
         self._staged = None
         self._next = slot ^ 1
         if next_host is not None:
-            self._staged = (slot ^ 1, next_host, self._stage(slot ^ 1, next_host))
+            self._stage(slot ^ 1, next_host)
+            self._staged = (slot ^ 1, next_host)
         s.wait_event(self.ready[slot])
         resident = {k: cyc.t[k] for k in DRAFT_INPUT_KEYS}
         cyc.t.update(self.slots[slot])
         try:
             cyc.draft(seed, s)
             cyc.schedule(s)
-            with torch.cuda.stream(s):
-                self.lens.copy_(cyc.sched_len, non_blocking=True)
-            s.synchronize()  # the host picks the rows from the lengths
-            code, n_rows = _lib.ds_copy_scheduled_rows(cyc.t["target_logits"], host["target_logits"],
-                                                       self.lens, s)
-            check(code, "ds_copy_scheduled_rows")
+            check(_lib.ds_fetch_scheduled_rows(cyc.t["target_logits"], host["target_logits"], cyc.sched_len,
+                                               self.rows_bytes, s), "ds_fetch_scheduled_rows")
             cyc.verify(seed, s)
             self.free[slot].record(s)
             with torch.cuda.stream(s):
+                self.lens[slot].copy_(cyc.sched_len, non_blocking=True)
                 self.out_tokens[slot].copy_(cyc.out_tokens, non_blocking=True)
                 self.num_emitted[slot].copy_(cyc.num_emitted, non_blocking=True)
             self.done[slot].record(s)
         finally:
             cyc.t.update(resident)
-        self.h2d_bytes = n_in + n_rows
-        return self.out_tokens[slot], self.num_emitted[slot], self.done[slot]
+        return self.lens[slot], self.out_tokens[slot], self.num_emitted[slot], self.done[slot]

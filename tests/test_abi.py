@@ -110,5 +110,9 @@ def test_host_validation_rejects_without_launching(lib):
     assert lib.ds_copy_scheduled_rows(fake, fake, 4, -1, 64, lens, ctypes.byref(n), None) == 1
     assert lib.ds_copy_scheduled_rows(fake, fake, 4, 3, 0, lens, ctypes.byref(n), None) == 1
     assert n.value == 7                                  # untouched on a rejected call
+    assert lib.ds_fetch_scheduled_rows(None, fake, 4, 3, 64, fake, None, None) == 1
+    assert lib.ds_fetch_scheduled_rows(fake, fake, 4, 3, 24, fake, None, None) == 1  # row % 16
+    assert lib.ds_fetch_scheduled_rows(fake, fake + 8, 4, 3, 64, fake, None, None) == 1  # alignment
+    assert lib.ds_fetch_scheduled_rows(fake, fake, 0, 3, 64, fake, None, None) == 1
     assert _lib.ds_status_string(7) == "non-finite logit or empty distribution"
     assert _lib.ds_version() == "0.1.0"
