@@ -99,35 +99,47 @@ class ClockSampler:
 # ---- workload accounting ---------------------------------------------------------
 
 def draft_algorithmic(inp, rnn=False):
-    """HBM bytes and tensor FLOPs of one draft step (one block position): the
-    base-logit rows z_k (B*V), the projection P (r*V, read every step), the
-    conditioning E rows (B*r) and the outputs (token, q, stats: 24 B per row).
-    RNN head, per step in addition: the packed step matrix (4r x 2r), the input
-    rows [e ; s] (B x 2r), the hidden-state gate inputs of the position
-    (B x 3r float32) and the state written twice (B x r); per call the
-    hidden-state GEMM (h: B*K*d, W_ih's hidden columns: 3r*d, out B*K*3r
-    float32), spread over the K steps."""
-    B, V, r = inp["B"], inp["V"], inp["r"]
+    """Algorithmic HBM bytes and tensor FLOPs of one ds_draft_block call (K
+    block positions), counted as the measurement section of the survey defines
+    them: every input byte once per cycle. The base logits z (B*K*V), the
+    projection P once (r*V: its K-1 re-reads within the call are L2 traffic,
+    reported separately), the conditioning rows and hidden states
+    (B*K*(r + d): h feeds the confidence head of the same cycle) and the
+    outputs (token, q, stats: 24 B per position). FLOPs: the bias product
+    2*B*K*r*V.
+    RNN head in addition: the packed step matrix (4r x 2r) and W_ih's hidden
+    columns (3r x d) once, and per position the input rows [e ; s] (B x 2r),
+    the gate inputs (B x 3r float32, written once and read once) and the state
+    (B x r, written, read back as the next input); FLOPs of the gated update
+    (2*B*4r*2r per position) and of the hidden-state GEMM (2*B*K*3r*d)."""
+    B, K, V, r, d = inp["B"], inp["K"], inp["V"], inp["r"], inp["d"]
     eb = 2 if inp["bf16"] else 4
-    by = B * V * eb + r * V * eb + B * r * eb + B * (4 + 4 + 16)
-    fl = 2.0 * B * r * V
+    by = B * K * V * eb + r * V * eb + B * K * (r + d) * eb + B * K * (4 + 4 + 16)
+    fl = 2.0 * B * K * r * V
     if rnn:
-        K, d = inp["K"], inp["d"]
-        by += 4 * r * 2 * r * eb + B * 2 * r * eb + B * 3 * r * 4 + 2 * B * r * eb
-        fl += 2.0 * B * 4 * r * 2 * r
-        by += (B * K * d * eb + 3 * r * d * eb + B * K * 3 * r * 4) / K
-        fl += 2.0 * B * K * 3 * r * d / K
+        by += 4 * r * 2 * r * eb + 3 * r * d * eb
+        by += K * (B * 2 * r * eb + 2 * B * 3 * r * 4 + 2 * B * r * eb)
+        fl += K * 2.0 * B * 4 * r * 2 * r + 2.0 * B * K * 3 * r * d
     return by, fl
 
 
-def verify_algorithmic(inp, L, n_final_residual, n_final_bonus):
-    B, K, V, r = inp["B"], inp["K"], inp["V"], inp["r"]
+def verify_algorithmic(inp, L, accept, temperature):
+    """Algorithmic bytes and FLOPs of one ds_verify call: the target rows up to
+    the first rejection (or the bonus row), sum_b min(a_b + 1, L_b + 1) rows;
+    for each sampling request that rejects (a_b < L_b, T_b > 0) its base row
+    at the rejection (q is rebuilt there), and P once if any request rejects;
+    FLOPs: one bias row per rejecting request (2*r*V each). Greedy requests
+    rebuild nothing. a_b and L_b are the run's (equal to the oracle's by the
+    parity tests)."""
+    import numpy as np
+    V, r = inp["V"], inp["r"]
     eb = 2 if inp["bf16"] else 4
-    rows = int(sum(int(l) + 1 for l in L))
-    by = rows * V * eb + n_final_bonus * V * eb + n_final_residual * 2 * V * eb
-    if n_final_residual:
-        by += r * V * eb
-    return by, 2.0 * n_final_residual * r * V
+    L = np.asarray(L, dtype=np.int64)
+    a = np.asarray(accept, dtype=np.int64)
+    rows = int(np.minimum(a + 1, L + 1).sum())
+    n_rej = int(np.sum((a < L) & (np.asarray(temperature) > 0)))
+    by = rows * V * eb + n_rej * V * eb + (r * V * eb if n_rej else 0)
+    return by, 2.0 * n_rej * r * V, rows, n_rej
 
 
 def gpu_launches_per_cycle(w, rnn=False):
@@ -448,7 +460,7 @@ def time_graph_replays(args, inp, dev, rnn_w, seed0, flush, stream, ws, per):
     torch.cuda.synchronize(dev)
     barrier(ws)
     gc.check_status()
-    return np.array([a.elapsed_time(b) for a, b in gev]), float(per.sum(axis=1).mean())
+    return np.array([a.elapsed_time(b) for a, b in gev]), float(np.median(per.sum(axis=1)))
 
 
 DRAFT_KEYS = ("base_logits", "anchor", "temperature", "h")
@@ -597,42 +609,55 @@ def main():
                                                            ws, per)
     except Exception as ex:  # the capture is refused: keep the launched timing and say why
         graph_error = "%s: %s" % (type(ex).__name__, str(ex)[:200])
-    total_s = reduce_max(float(cycle_ms.sum()) / 1e3, ws)
+    # the median timed cycle (the survey's protocol), the slowest rank's
+    med_ms = reduce_max(float(np.median(cycle_ms)), ws)
     B, Kb, V = w.B, w.K, w.V
-    value = ws * B * Kb * K / total_s
+    value = ws * B * Kb / (med_ms * 1e-3)
     res = cyc.results()
 
     peaks, peak_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     tc = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    d_by, d_fl = draft_algorithmic(inp, rnn)     # per draft step
-    d_ms = float(per[:, 0].mean()) / Kb          # average draft step (tile + locate kernels)
-    t_hbm = d_by / (hbm * 1e9)
-    t_tc = d_fl / (tc * 1e12)
+    d_by, d_fl = draft_algorithmic(inp, rnn)     # per ds_draft_block call (K steps)
+    s_by, s_fl = d_by / Kb, d_fl / Kb            # per draft step
+    d_ms = float(np.median(per[:, 0])) / Kb      # median draft step (tile + locate kernels)
+    t_hbm = s_by / (hbm * 1e9)
+    t_tc = s_fl / (tc * 1e12)
     traffic = None if rnn else recorded_traffic(w.name)
     if t_hbm >= t_tc:
-        achieved = d_by / (d_ms * 1e-3) / 1e9
+        achieved = s_by / (d_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic}
     else:
-        achieved = d_fl / (d_ms * 1e-3) / 1e12
+        achieved = s_fl / (d_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tc, "unit": "TFLOP/s",
                 "frac": achieved / tc, "traffic": traffic}
     if roof["unit"] == "GB/s":
         roof["frac_nominal"] = roof["achieved"] / NOMINAL_HBM_GBS
+    eb = 2 if w.bf16 else 4
+    p_rereads = (Kb - 1) * w.r * V * eb / Kb     # per step: P read again by steps 2..K
     roof.update({"kernel": "draft step = tile_tc_kernel + sample_locate_kernel (K per ds_draft_block)"
                  + (" + rnn_gemm_kernel<update> (+ 1/K of the hidden-state GEMM)" if rnn else ""),
-                 "peak_source": peak_src, "peak_kind": "burst copy (hbm_gbs)",
-                 "algorithmic_bytes_per_step": d_by, "algorithmic_flops_per_step": d_fl,
-                 "t_roof_us": 1e6 * max(t_hbm, t_tc), "t_meas_us": 1e3 * d_ms})
-    n_res = int(np.sum((res["accept_count"] < res["L"]) & (inp["temperature"] > 0)))
-    n_bon = int(np.sum((res["accept_count"] >= res["L"]) & (inp["temperature"] > 0)))
-    v_by, v_fl = verify_algorithmic(inp, res["L"], n_res, n_bon)
-    cycle_roof_us = 1e6 * (Kb * max(t_hbm, t_tc) + max(v_by / (hbm * 1e9), v_fl / (tc * 1e12)))
+                 "peak_source": peak_src, "peak_kind": "burst copy (hbm_gbs); sustained bf16 GEMM",
+                 "algorithmic_bytes_per_step": s_by, "algorithmic_flops_per_step": s_fl,
+                 "bytes_rule": "per cycle B*K*V + r*V (P once) + B*K*(r+d) elements + outputs, / K",
+                 "t_roof_us": 1e6 * max(t_hbm, t_tc), "t_meas_us": 1e3 * d_ms,
+                 "traffic_over_algorithmic": None if traffic is None else traffic / s_by,
+                 # the same step if P had to come from DRAM at every step (the L2 misses
+                 # this accounting leaves to the kernel)
+                 "p_every_step": {"bytes_per_step": s_by + p_rereads,
+                                  "achieved_gbs": (s_by + p_rereads) / (d_ms * 1e-3) / 1e9,
+                                  "frac": (s_by + p_rereads) / (d_ms * 1e-3) / 1e9 / hbm}})
+    v_by, v_fl, v_rows, n_rej = verify_algorithmic(inp, res["L"], res["accept_count"], inp["temperature"])
+    t_draft_roof = max(d_by / (hbm * 1e9), d_fl / (tc * 1e12))
+    t_verify_roof = max(v_by / (hbm * 1e9), v_fl / (tc * 1e12))
+    cycle_roof_us = 1e6 * (t_draft_roof + t_verify_roof)
+    comp_med = {"draft": float(np.median(per[:, 0])), "schedule": float(np.median(per[:, 1])),
+                "verify": float(np.median(per[:, 2]))}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
-        "warmup": args.warmup, "ms_per_step": float(cycle_ms.mean()), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": med_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.bf16 else "f32",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
         "config": {"workload": w.name, "B": B, "K": Kb, "V": V, "r": w.r, "d": w.d,
@@ -642,14 +667,19 @@ def main():
                    "mode": MODE_NAMES[args.mode],
                    "threshold": args.threshold if args.mode == 2 else None,
                    "head": args.head, "cuda_graph": graph_launch_ms is not None,
+                   "timing": "median of the timed cycles (CUDA events; max over ranks)",
                    "cuda_graph_error": graph_error},
-        "components_ms": {"draft": float(per[:, 0].mean()), "schedule": float(per[:, 1].mean()),
-                          "verify": float(per[:, 2].mean())},
+        "ms_per_step_mean": float(cycle_ms.mean()),
+        "components_ms": comp_med,
+        "components_roofline_us": {"draft": 1e6 * t_draft_roof, "verify": 1e6 * t_verify_roof,
+                                   "verify_target_rows": v_rows, "verify_rejecting_requests": n_rej},
+        "components_roofline_frac": {"draft": 1e3 * t_draft_roof / comp_med["draft"],
+                                     "verify": 1e3 * t_verify_roof / comp_med["verify"]},
         "launched_cycle_ms": graph_launch_ms,
-        "emitted_tokens_per_s": ws * float(res["num_emitted"].sum()) / (total_s / K),
-        "verified_tokens_per_s": ws * float((res["L"] + 1).sum()) / (total_s / K),
+        "emitted_tokens_per_s": ws * float(res["num_emitted"].sum()) / (med_ms * 1e-3),
+        "verified_tokens_per_s": ws * float((res["L"] + 1).sum()) / (med_ms * 1e-3),
         "mean_sched_len": float(res["L"].mean()), "mean_accepted": float(res["accept_count"].mean()),
-        "cycle_roofline_us": cycle_roof_us, "cycle_roofline_frac": cycle_roof_us / (1e3 * cycle_ms.mean()),
+        "cycle_roofline_us": cycle_roof_us, "cycle_roofline_frac": cycle_roof_us / (1e3 * med_ms),
         "roofline": roof,
         "gpu_launches": K * (gpu_launches_per_cycle(w, rnn)),
         "wall_s": wall,

@@ -335,6 +335,10 @@ typedef struct {
   const void* states;         /* RNN head: [B][K][r] states from ds_draft_block (q_k is rebuilt
                                  with s_k . P); NULL for the Markov head */
   const uint64_t* seed_ptr;   /* optional device word holding the Philox key (overrides `seed`) */
+  float* p_token;             /* optional out [B][K], or NULL: p_k(x_k), the target probability
+                                 the accept test reads, for every k <= L_b (rows after the first
+                                 rejection included); -1 for k > L_b. Greedy requests (T = 0):
+                                 1 if x_k is the target argmax, else 0 (the point mass). */
 } ds_verify_args;
 
 size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
@@ -353,6 +357,8 @@ ds_status ds_verify(const ds_verify_args* args, ds_stream_t stream);
  *     r = 256 needs about 11 MB and fits);
  *   - the first call on a device (with that device current) looks up the
  *     array's address once; make one call per device before any stream capture;
+ *     cudaDeviceReset gives the device a new context, where the array may sit
+ *     elsewhere: the first call in the new context looks it up again;
  *   - calls whose executions overlap on the same device race on the array:
  *     order them on one stream or with events;
  *   - nothing in the array needs to start at zero.
@@ -407,6 +413,24 @@ ds_status ds_fetch_scheduled_rows(void* dst, const void* src, int32_t B, int32_t
 /* Synchronises `stream`, reads the device status word and returns it (or
  * DS_ERR_CUDA if the stream reports an error). */
 ds_status ds_check_status(const int32_t* device_status, ds_stream_t stream);
+
+/*
+ * Test hook for the bounded device waits (not for production use). For every
+ * later launch of the tensor-core tile kernel in this process (the draft
+ * steps and the final draw of ds_verify, bfloat16 with 64 <= r <= 256):
+ *   wait_polls    the number of suspended polls (each up to ~20 us) a wait makes
+ *                 before it gives up; 0 restores the default (about a second);
+ *   withhold_cta  the index of one CTA whose first epilogue warp withholds its
+ *                 arrival at the group-record exchange of that CTA's last tile,
+ *                 so that the other epilogue threads' wait runs out; -1: none.
+ * At that exchange every TMA copy and MMA of the CTA has completed, so the CTA
+ * records DS_ERR_TIMEOUT in the status word, releases its tensor memory and
+ * returns with nothing in flight; the context stays usable, and later calls
+ * (with the hook cleared) run normally. The records that CTA did not write
+ * leave the call's outputs undefined. Process-wide, not synchronised with
+ * launches already enqueued: set it between calls on an idle device.
+ */
+ds_status ds_test_set_wait_hooks(uint32_t wait_polls, int32_t withhold_cta);
 
 /* Static description of a status code. */
 const char* ds_status_string(ds_status s);

@@ -75,7 +75,7 @@ def verify_request(tokens, L, p_row, q_row, u_accept, u_resample, greedy=False):
 
 
 def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperature, seed,
-           request_ids=None, states=None):
+           request_ids=None, states=None, with_p=False):
     """Verify a batch. target_logits: [B, K+1, V]; base_logits: [B, K, V].
 
     The draft distribution q_k is recomputed from the base logits and the Markov
@@ -88,6 +88,12 @@ def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperat
     from the base logits and the bias s_k . P of the state the draft used at
     that position, exactly as the RNN draft defined it.
 
+    ``with_p`` adds ``p_token`` [B, K]: the target probability p_k(x_k) of
+    every scheduled drafted token (k <= L_b, whether or not an earlier position
+    rejected; NaN beyond L_b). For a greedy request (T = 0) the target law is
+    the point mass on its argmax, so p_k(x_k) is 1 if x_k is the argmax and 0
+    otherwise. The accept rule reads exactly this p_k(x_k).
+
     Returns a dict with accept_count [B], num_emitted [B], out_tokens [B, K+1]
     (-1 padded) and decisions (per request, see verify_request).
     """
@@ -98,6 +104,7 @@ def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperat
     temperature = np.asarray(temperature, dtype=np.float32)
     out = -np.ones((B, K + 1), dtype=np.int64)
     acc = np.zeros(B, dtype=np.int64)
+    p_token = np.full((B, K), np.nan)
     decisions = []
     rid = np.arange(B) if request_ids is None else np.asarray(request_ids, dtype=np.int64)
     for b in range(B):
@@ -127,5 +134,15 @@ def verify(target_logits, base_logits, E, P, anchor, tokens, sched_len, temperat
         acc[b] = a
         out[b, :len(emitted)] = emitted
         decisions.append(dec)
-    return {"accept_count": acc, "num_emitted": acc + 1, "out_tokens": out,
-            "decisions": decisions}
+        if with_p:
+            for j in range(L):
+                x = int(tokens[b, j])
+                if greedy:
+                    p_token[b, j] = 1.0 if argmax_first(p_row(j))[0] == x else 0.0
+                else:
+                    p_token[b, j] = p_row(j)[x]
+    res = {"accept_count": acc, "num_emitted": acc + 1, "out_tokens": out,
+           "decisions": decisions}
+    if with_p:
+        res["p_token"] = p_token
+    return res

@@ -28,7 +28,7 @@ EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspa
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
            "ds_version", "ds_transpose_projection", "ds_verify_static", "ds_sts_workspace_bytes",
            "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights", "ds_copy_scheduled_rows",
-           "ds_fetch_scheduled_rows")
+           "ds_fetch_scheduled_rows", "ds_test_set_wait_hooks")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -69,7 +69,7 @@ class VerifyArgs(ctypes.Structure):
                 ("sched_len", _vp), ("temperature", _vp), ("seed", ctypes.c_uint64),
                 ("out_tokens", _vp), ("accept_count", _vp), ("num_emitted", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp),
-                ("states", _vp), ("seed_ptr", _vp)]
+                ("states", _vp), ("seed_ptr", _vp), ("p_token", _vp)]
 
 
 _lib = None
@@ -117,6 +117,8 @@ def load():
     lib.ds_copy_scheduled_rows.restype = ctypes.c_int
     lib.ds_fetch_scheduled_rows.argtypes = [_vp, _vp, _i32, _i32, ctypes.c_size_t, _vp, _vp, _vp]
     lib.ds_fetch_scheduled_rows.restype = ctypes.c_int
+    lib.ds_test_set_wait_hooks.argtypes = [ctypes.c_uint32, _i32]
+    lib.ds_test_set_wait_hooks.restype = ctypes.c_int
     lib.ds_check_status.argtypes = [_vp, _vp]
     lib.ds_check_status.restype = ctypes.c_int
     lib.ds_status_string.argtypes = [ctypes.c_int]
@@ -263,7 +265,7 @@ def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp,
 
 def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats, sched_len,
               temperature, seed, out_tokens, accept_count, num_emitted, workspace, status,
-              stream=None, P_t=None, states=None, seed_ptr=None):
+              stream=None, P_t=None, states=None, seed_ptr=None, p_token=None):
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
                    target_logits=_ptr(target_logits, "target_logits"),
@@ -279,7 +281,8 @@ def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q
                    workspace_bytes=workspace.numel() * workspace.element_size(),
                    status=_ptr(status, "status"),
                    states=None if states is None else _ptr(states, "states"),
-                   seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"))
+                   seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"),
+                   p_token=None if p_token is None else _ptr(p_token, "p_token"))
     return load().ds_verify(ctypes.byref(a), _stream(stream))
 
 
@@ -290,9 +293,14 @@ def ds_transpose_projection(P, P_t, stream=None):
                                           _stream(stream))
 
 
+def ds_test_set_wait_hooks(wait_polls, withhold_cta):
+    """Test hook of the bounded device waits (see ds_draft.h); (0, -1) clears it."""
+    return load().ds_test_set_wait_hooks(int(wait_polls), int(withhold_cta))
+
+
 def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats,
                      sched_len, temperature, seed, out_tokens, accept_count, num_emitted, status,
-                     stream=None, P_t=None, states=None, seed_ptr=None):
+                     stream=None, P_t=None, states=None, seed_ptr=None, p_token=None):
     """ds_verify with the library's static scratch (no workspace argument)."""
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
@@ -307,7 +315,8 @@ def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_t
                    num_emitted=_ptr(num_emitted, "num_emitted"),
                    workspace=None, workspace_bytes=0, status=_ptr(status, "status"),
                    states=None if states is None else _ptr(states, "states"),
-                   seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"))
+                   seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"),
+                   p_token=None if p_token is None else _ptr(p_token, "p_token"))
     return load().ds_verify_static(ctypes.byref(a), _stream(stream))
 
 

@@ -454,6 +454,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
       (!aligned16(a->states) || !tc_path_supported(a->dtype, a->r) || a->dtype != DS_BF16))
     return DS_ERR_INVALID_ARG;
   if (a->seed_ptr != nullptr && ((uintptr_t)a->seed_ptr & 7u) != 0) return DS_ERR_INVALID_ARG;
+  if (a->p_token != nullptr && !aligned16(a->p_token)) return DS_ERR_INVALID_ARG;
   const ds_status st = device_supported();
   if (st != DS_OK) return st;
   char* ws = reinterpret_cast<char*>(a->workspace);
@@ -479,6 +480,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   v.out_tokens = a->out_tokens;
   v.accept_count = a->accept_count;
   v.num_emitted = a->num_emitted;
+  v.p_token = a->p_token;
   v.status = a->status;
   const cudaStream_t s = (cudaStream_t)stream;
   if (launch_verify_rows(v, s) != cudaSuccess) return DS_ERR_CUDA;
@@ -561,6 +563,11 @@ ds_status ds_fetch_scheduled_rows(void* dst, const void* src, int32_t B, int32_t
   return from_cuda(launch_fetch_rows(dst, src_dev, B, K, row_bytes, sched_len,
                                      reinterpret_cast<unsigned long long*>(bytes_total),
                                      (cudaStream_t)stream));
+}
+
+ds_status ds_test_set_wait_hooks(uint32_t wait_polls, int32_t withhold_cta) {
+  set_tile_test_hooks(wait_polls, withhold_cta);
+  return DS_OK;
 }
 
 ds_status ds_check_status(const int32_t* device_status, ds_stream_t stream) {

@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -60,10 +61,16 @@ constexpr uint32_t kOffP = kASize;
 constexpr uint32_t kOffZ = kOffP + kPStages * kPStage;
 constexpr uint32_t kSmemBytes = kOffZ + kZSlots * kZSlot + 1024;
 constexpr uint32_t kTmemCols = kAccum * kTileN;
+// tcgen05.alloc takes a power-of-two column count from 32 to 512: three
+// 128-column accumulators (384 columns) would be an illegal allocation.
+static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+              "TMEM allocation must be a power of two in [32, 512] columns");
 
 struct TcParams {
   SampleParams sp;
   int32_t n_mt, n_nt, nkb, tiles;
+  uint32_t wait_polls;   // polls of a bounded wait before it gives up
+  int32_t withhold_cta;  // test hook (-1: none), see set_tile_test_hooks
 };
 
 struct Shared {
@@ -76,14 +83,14 @@ struct Shared {
   int abort_flag;
 };
 
-// Bounded wait (about a second at most): the thread sleeps in try_wait with a
-// 20 us hint (it wakes as soon as the phase completes), so waiting warps do
-// not take issue slots from the epilogue.
+// Bounded wait (about a second at most with the default kWaitPolls): the
+// thread sleeps in try_wait with a 20 us hint (it wakes as soon as the phase
+// completes), so waiting warps do not take issue slots from the epilogue.
 constexpr uint32_t kWaitPolls = 1u << 16;
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int32_t* status) {
+                                         int32_t* status, uint32_t polls) {
   if (mbar_try_wait(bar, parity)) return true;
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((i & 15) == 15 && *abort_flag) return false;
   }
@@ -93,10 +100,11 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // Barrier over the epilogue threads only, bounded like every other wait.
+// `arrive` false withholds this thread's arrival (test hook only).
 __device__ __forceinline__ bool epi_barrier(Shared& sh, uint32_t& ph, volatile int* abort_flag,
-                                            int32_t* status) {
-  mbar_arrive(&sh.x_bar);
-  const bool ok = wait_bar(&sh.x_bar, ph & 1, abort_flag, status);
+                                            int32_t* status, uint32_t polls, bool arrive = true) {
+  if (arrive) mbar_arrive(&sh.x_bar);
+  const bool ok = wait_bar(&sh.x_bar, ph & 1, abort_flag, status, polls);
   ++ph;
   return ok;
 }
@@ -352,7 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
         const uint32_t ps = pc % kPStages;
         if (lane == 0) {
-          ok = wait_bar(&sh.p_empty[ps], ((pc / kPStages) & 1) ^ 1, abort_flag, sp.status);
+          ok = wait_bar(&sh.p_empty[ps], ((pc / kPStages) & 1) ^ 1, abort_flag, sp.status, prm.wait_polls);
           if (ok) {
             mbar_expect_tx(&sh.p_full[ps], kPStage);
             tma_load_2d(sP + ps * kPStage, &tmP, &sh.p_full[ps], n0, c * 64, pol_p);
@@ -366,7 +374,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int nb = 0; nb < 2 && ok; ++nb, ++zc) {
           const uint32_t zs = zc % kZSlots;
           if (lane == 0) {
-            ok = wait_bar(&sh.z_empty[zs], ((zc / kZSlots) & 1) ^ 1, abort_flag, sp.status);
+            ok = wait_bar(&sh.z_empty[zs], ((zc / kZSlots) & 1) ^ 1, abort_flag, sp.status, prm.wait_polls);
             if (ok) {
               mbar_expect_tx(&sh.z_full[zs], kZSlot);
               tma_load_3d(sZ + zs * kZSlot, &tmZ, &sh.z_full[zs], n0 + nb * 64, sp.step - 1,
@@ -385,7 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           waited = true;
         }
         if (lane == 0) {
-          ok = a_loads == 0 || wait_bar(&sh.a_empty, (a_loads - 1) & 1, abort_flag, sp.status);
+          ok = a_loads == 0 || wait_bar(&sh.a_empty, (a_loads - 1) & 1, abort_flag, sp.status, prm.wait_polls);
           if (ok) {
             mbar_expect_tx(&sh.a_full, (uint32_t)prm.nkb * 16384u);
             for (int c = 0; c < prm.nkb; ++c)
@@ -411,20 +419,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int mt = t / prm.n_nt;
         if (mt != cur_mt) {
           if (cur_mt >= 0) mma_commit(&sh.a_empty);
-          ok = wait_bar(&sh.a_full, a_uses & 1, abort_flag, sp.status);
+          ok = wait_bar(&sh.a_full, a_uses & 1, abort_flag, sp.status, prm.wait_polls);
           if (!ok) break;
           ++a_uses;
           cur_mt = mt;
           tc_fence_after();
         }
         const uint32_t buf = i % kAccum;
-        ok = wait_bar(&sh.t_empty[buf], ((i / kAccum) & 1) ^ 1, abort_flag, sp.status);
+        ok = wait_bar(&sh.t_empty[buf], ((i / kAccum) & 1) ^ 1, abort_flag, sp.status, prm.wait_polls);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kTileN;
         for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
           const uint32_t ps = pc % kPStages;
-          ok = wait_bar(&sh.p_full[ps], (pc / kPStages) & 1, abort_flag, sp.status);
+          ok = wait_bar(&sh.p_full[ps], (pc / kPStages) & 1, abort_flag, sp.status, prm.wait_polls);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -474,7 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           c.trow = reinterpret_cast<const __nv_bfloat16*>(rc.trow);
         }
         if (!staged) {
-          if (a_uses > 0 && !wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status)) break;
+          if (a_uses > 0 && !wait_bar(&sh.a_empty, (a_uses - 1) & 1, abort_flag, sp.status, prm.wait_polls)) break;
           // kThreadsPerRow threads per A row, each a contiguous run of its
           // 16-byte chunks, all loads in flight before the first store
           constexpr int kThreadsPerRow = 32 * kEpiWarps / 128;
@@ -511,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t zc = 2u * i + nb;
       const uint32_t zs = draft ? zc % kZSlots : nb;
       const uint32_t zph = draft ? (zc / kZSlots) & 1 : (i & 1);
-      if (draft && !wait_bar(&sh.z_full[zs], zph, abort_flag, sp.status)) break;
+      if (draft && !wait_bar(&sh.z_full[zs], zph, abort_flag, sp.status, prm.wait_polls)) break;
       // final draw: each thread loads its own row's 2 x 64 tokens (base and
       // target) straight from global memory, issued before the MMA wait
       uint4 fz[kChunks][4], ft[kChunks][4];
@@ -529,7 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      if (!wait_bar(&sh.t_full[buf], (i / kAccum) & 1, abort_flag, sp.status)) break;
+      if (!wait_bar(&sh.t_full[buf], (i / kAccum) & 1, abort_flag, sp.status, prm.wait_polls)) break;
       tc_fence_after();
       __syncwarp();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * kTileN;
@@ -594,9 +602,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // column groups' partial records meet in the row's line of the tile's
         // first logit slot (consumed, and not released until after this).
         uint8_t* xb = sZ + (draft ? (2u * i) % kZSlots : 0u) * kZSlot + r_local * 128;
-        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
+        // test hook: one warp of one CTA withholds its arrival here, at a point
+        // where every copy and MMA of the CTA has completed (this is its last
+        // tile and its accumulator and logits were waited for), so the others'
+        // bounded wait runs out and the CTA returns with nothing in flight
+        const bool withhold = blockIdx.x == prm.withhold_cta && ew == 0 && t + 1 == t1;
+        if (!epi_barrier(sh, xph, abort_flag, sp.status, prm.wait_polls, !withhold)) break;
         if (cg > 0) *reinterpret_cast<ChunkRec*>(xb + 16 * cg) = gacc;
-        if (!epi_barrier(sh, xph, abort_flag, sp.status)) break;
+        if (!epi_barrier(sh, xph, abort_flag, sp.status, prm.wait_polls)) break;
         if (cg == 0 && row < sp.B && c.mode != kSkip) {
           ChunkRec g = gacc;
 #pragma unroll
@@ -644,6 +657,9 @@ bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
   return encode_tmap_bf16(m, ptr, rank, dims, strides, box);
 }
 
+std::atomic<uint32_t> g_wait_polls{kWaitPolls};
+std::atomic<int32_t> g_withhold_cta{-1};
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -674,6 +690,11 @@ void tc_group_layout(SampleParams& p) {
   p.sup_cpt = kTileN / 32;
 }
 
+void set_tile_test_hooks(uint32_t wait_polls, int32_t withhold_cta) {
+  g_wait_polls.store(wait_polls == 0 ? kWaitPolls : wait_polls, std::memory_order_relaxed);
+  g_withhold_cta.store(withhold_cta < 0 ? -1 : withhold_cta, std::memory_order_relaxed);
+}
+
 bool tc_path_supported(int32_t dtype, int32_t r) {
   return dtype == DS_BF16 && r % 64 == 0 && r >= 64 && r <= 256;
 }
@@ -691,6 +712,8 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   prm.n_nt = (p.V + kTileN - 1) / kTileN;
   prm.nkb = p.r / 64;
   prm.tiles = prm.n_mt * prm.n_nt;
+  prm.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
+  prm.withhold_cta = g_withhold_cta.load(std::memory_order_relaxed);
 
   CUtensorMap mP, mZ, mT;
   const cuuint64_t V = (cuuint64_t)p.V;

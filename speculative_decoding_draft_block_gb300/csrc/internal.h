@@ -106,6 +106,7 @@ struct VerifyParams {
   int32_t* out_tokens;
   int32_t* accept_count;
   int32_t* num_emitted;
+  float* p_token;  // optional [B][K]: p_k(x_k) for k <= L_b, -1 beyond
   int32_t* status;
 };
 
@@ -211,6 +212,8 @@ void simt_group_layout(SampleParams& p);
 size_t sample_tile_smem_bytes(int32_t r);
 size_t locate_smem_bytes(int32_t V);
 bool tc_path_supported(int32_t dtype, int32_t r);
+// Test hooks of the tensor-core tile kernel (ds_test_set_wait_hooks).
+void set_tile_test_hooks(uint32_t wait_polls, int32_t withhold_cta);
 cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_sample_tile(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_sample_locate(const SampleParams& p, cudaStream_t s);

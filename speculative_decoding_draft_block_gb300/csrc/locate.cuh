@@ -121,10 +121,11 @@ __device__ __forceinline__ void locate_row(const SampleParams& p, int b, int tid
         const ChunkRec ov = shfl_xor_rec(best, o);
         if (greedy_better(ov, best)) best = ov;
       }
-      const int bx = best.idx < 0 ? 0 : best.idx;
+      const bool bad_idx = best.idx < 0 || best.idx >= p.V;  // no finite logit (or a bad record)
+      const int bx = bad_idx ? 0 : best.idx;
       stage_e_row<Tin>(p, b, bx, lane);
       if (lane == 0) {
-        if (best.idx < 0) report(p.status, kErrNonfinite);
+        if (bad_idx) report(p.status, kErrNonfinite);
         p.tokens_out[c.out_index] = bx;
         if (p.src == 0) {
           p.q_token[c.out_index] = 1.f;

@@ -12,9 +12,11 @@
 // allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
 //
 // Set-up: the first call on each device (with that device current) takes the
-// array's device address with cudaGetSymbolAddress and caches it per device.
-// Make one call on every device before capturing work into a CUDA graph, so
-// that the capture does not include the set-up query.
+// array's device address with cudaGetSymbolAddress and caches it per device,
+// together with the id of the context it belongs to; a call in a later
+// context (after cudaDeviceReset) looks the address up again. Make one call
+// on every device before capturing work into a CUDA graph, so that the
+// capture does not include the set-up query.
 //
 // Zero-initialisation: none is needed. ds_verify writes every scratch word it
 // reads within the same call (per-row results for rows 0..L_b, the final-draw
@@ -26,6 +28,7 @@
 //
 // Limit: calls whose ds_verify_workspace_bytes(B, K, V, r) exceeds
 // kScratchBytes return DS_ERR_WORKSPACE without launching anything.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,21 +44,56 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
+// The driver's id of the current context (unique for the life of the
+// process), or 0 if it cannot be read; taken through the runtime's
+// entry-point query so the library needs no link to the driver library.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+unsigned long long g_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once per device).
+// Device address of the scratch array on the current device. It is looked up
+// once per device and context: after cudaDeviceReset the device gets a new
+// primary context, where the module (and the array) may sit elsewhere, so a
+// changed context id triggers a new lookup.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // 0 when no context is current yet (the lookup below creates it) or the id
+  // cannot be read: then the address is looked up again
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
+  if (g_addr[dev] == nullptr || ctx == 0 || ctx != g_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_verify_scratch);
     if (e != cudaSuccess) return e;
     g_addr[dev] = p;
+    g_ctx[dev] = ctx;
   }
   *out = g_addr[dev];
   return cudaSuccess;

@@ -10,7 +10,8 @@
 //                           (per-thread power-of-two references merged
 //                           exactly, double-float sums), evaluates p(x_k) and
 //                           takes the accept decision u * q(x_k) < p(x_k) in
-//                           double-float (greedy rows: target argmax and exact match).
+//                           double-float (greedy rows: target argmax and exact match);
+//                           optionally stores p(x_k) itself.
 //   verify_finalize_kernel  one thread per request: accepted prefix length,
 //                           emitted tokens, and the descriptor of the final
 //                           draw (residual at the first rejection, or bonus
@@ -182,7 +183,11 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
           bx = si[w];
         }
       out.argmax = bx;
-      if (j < L) out.accept = (p.draft_tokens[(size_t)b * p.K + j] == bx) ? 1 : 0;
+      if (j < L) {
+        out.accept = (p.draft_tokens[(size_t)b * p.K + j] == bx) ? 1 : 0;
+        // the greedy target law is the point mass on its argmax
+        if (p.p_token != nullptr) p.p_token[(size_t)b * p.K + j] = out.accept ? 1.f : 0.f;
+      }
     }
   } else {
     if (!(T >= 1e-3f && T <= 1e3f)) {
@@ -248,6 +253,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
         const DF uq = df_mul(uniform_df(seed, (uint32_t)b, (uint32_t)(j + 1), DS_STAGE_ACCEPT),
                              DF{qx, 0.f});
         out.accept = df_lt(df_mul(uq, S), DF{wx, 0.f}) ? 1 : 0;
+        if (p.p_token != nullptr) p.p_token[(size_t)b * p.K + j] = div_by_df(wx, S);
       }
     }
   }
@@ -270,6 +276,8 @@ __global__ void __launch_bounds__(128) verify_finalize_kernel(VerifyParams p) {
   while (a < L && vr[a].accept) ++a;
   int32_t* out = p.out_tokens + (size_t)b * (K + 1);
   for (int i = lane; i <= K; i += 32) out[i] = i < a ? p.draft_tokens[(size_t)b * K + i] : -1;
+  if (p.p_token != nullptr)  // positions past L_b were not verified (the rows kernel wrote k < L_b)
+    for (int i = L + lane; i < K; i += 32) p.p_token[(size_t)b * K + i] = -1.f;
   FinalDesc d;
   d.mode = kSkip;
   d.row = a;

@@ -33,15 +33,22 @@ INPUT_KEYS = ("base_logits", "target_logits", "E", "P", "anchor", "temperature",
               "w_e", "sts_temp", "sps")
 
 
+GUARD_BYTES = 256                 # per side of a guarded buffer (a multiple of 16)
+GUARD_BYTE = 0xA5                 # the sentinel byte of the guard regions
+
+
 class DeviceCycle:
     def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0,
                  token_major_projection=True, initial_budget=None, rnn_weights=None,
-                 device_seed=False):
+                 device_seed=False, guards=False):
         """``rnn_weights`` (dict w_ih, w_hh as bfloat16 bits, b_ih, b_hh float32)
         selects the RNN head; its step matrix is packed once here.
         ``device_seed``: the Philox key is read from a device word (``seed_dev``,
         set with ``set_seed``) instead of the ``seed`` argument, so that a
-        captured cycle can be replayed with a fresh key each time."""
+        captured cycle can be replayed with a fresh key each time.
+        ``guards``: every buffer the library writes (outputs and workspaces) sits
+        between two GUARD_BYTES regions of sentinel bytes; ``guard_damage()``
+        lists the buffers whose guards changed (a write out of bounds)."""
         self.inp = inp
         self.device = torch.device(device)
         self.mode = mode
@@ -49,29 +56,31 @@ class DeviceCycle:
         B, K, V, r = inp["B"], inp["K"], inp["V"], inp["r"]
         self.B, self.K, self.V, self.r, self.d = B, K, V, r, inp["d"]
         dev = self.device
+        self._guarded = [] if guards else None
         self.t = {k: _to_device(inp[k], dev) for k in INPUT_KEYS}
         self.t["anchor"] = self.t["anchor"].to(torch.int32)
         self.conf_bias = float(inp["conf_bias"])
-        i32 = dict(dtype=torch.int32, device=dev)
-        f32 = dict(dtype=torch.float32, device=dev)
-        self.draft_tokens = torch.zeros((B, K), **i32)
-        self.q_token = torch.zeros((B, K), **f32)
-        self.q_stats = torch.zeros((B, K, 4), **i32)
-        self.conf = torch.zeros((B, K), **f32)
-        self.conf_logit = torch.zeros((B, K), **f32)   # raw logit: the STS fit's input
-        self.survival = torch.zeros((B, K), **f32)
-        self.sched_len = torch.zeros((B,), **i32)
-        self.objective = torch.zeros((2,), dtype=torch.float64, device=dev)
-        self.out_tokens = torch.zeros((B, K + 1), **i32)
-        self.accept_count = torch.zeros((B,), **i32)
-        self.num_emitted = torch.zeros((B,), **i32)
-        self.status = torch.zeros((4,), **i32)
+        i32, f32 = torch.int32, torch.float32
+        self.draft_tokens = self._out("draft_tokens", (B, K), i32)
+        self.q_token = self._out("q_token", (B, K), f32)
+        self.q_stats = self._out("q_stats", (B, K, 4), i32)
+        self.conf = self._out("conf", (B, K), f32)
+        self.conf_logit = self._out("conf_logit", (B, K), f32)   # raw logit: the STS fit's input
+        self.survival = self._out("survival", (B, K), f32)
+        self.sched_len = self._out("sched_len", (B,), i32)
+        self.objective = self._out("objective", (2,), torch.float64)
+        self.out_tokens = self._out("out_tokens", (B, K + 1), i32)
+        self.accept_count = self._out("accept_count", (B,), i32)
+        self.num_emitted = self._out("num_emitted", (B,), i32)
+        self.p_token = self._out("p_token", (B, K), f32)   # target probability of each verified token
+        self.status = self._out("status", (4,), i32)
         # asynchronous scheduler: budgets of the next two cycles and the cycle
         # counter, all on the device; the first two cycles use initial_budget
         if initial_budget is None:
             initial_budget = B * K // 2
         self.initial_budget = int(initial_budget)
-        self.budget_ring = torch.tensor([self.initial_budget, self.initial_budget, 0, 0], **i32)
+        self.budget_ring = self._out("budget_ring", (4,), i32)
+        self.budget_ring.copy_(torch.tensor([self.initial_budget, self.initial_budget, 0, 0], dtype=i32))
         self.seed_dev = torch.zeros((2,), dtype=torch.int64, device=dev) if device_seed else None
         wd = _lib.ds_draft_workspace_bytes(B, K, V, r)
         wv = _lib.ds_verify_workspace_bytes(B, K, V, r)
@@ -85,18 +94,46 @@ class DeviceCycle:
             wd = (wd + 255) // 256 * 256 + wr
             rw = {k: _to_device(rnn_weights[k], dev) for k in ("w_ih", "w_hh", "b_ih", "b_hh")}
             rw["h"] = self.t["h"]
-            rw["w_step"] = torch.empty((4 * r, 2 * r), dtype=rw["w_ih"].dtype, device=dev)
+            rw["w_step"] = self._out("w_step", (4 * r, 2 * r), rw["w_ih"].dtype)
             check(_lib.ds_rnn_pack_weights(rw["w_ih"], rw["w_hh"], rw["w_step"]), "ds_rnn_pack_weights")
-            rw["states"] = torch.zeros((B, K, r), dtype=rw["w_ih"].dtype, device=dev)
+            rw["states"] = self._out("states", (B, K, r), rw["w_ih"].dtype)
             self.rnn = rw
-        self.ws_draft = torch.empty((wd,), dtype=torch.uint8, device=dev)
-        self.ws_verify = torch.empty((wv,), dtype=torch.uint8, device=dev)
+        self.ws_draft = self._out("ws_draft", (wd,), torch.uint8)
+        self.ws_verify = self._out("ws_verify", (wv,), torch.uint8)
         # weight layout step, once per model: the token-major copy of P
         self.P_t = None
         if token_major_projection:
             P = self.t["P"]
-            self.P_t = torch.empty((P.shape[1], P.shape[0]), dtype=P.dtype, device=dev)
+            self.P_t = self._out("P_t", (P.shape[1], P.shape[0]), P.dtype)
             check(_lib.ds_transpose_projection(P, self.P_t), "ds_transpose_projection")
+
+    def _out(self, name, shape, dtype):
+        """A zeroed device buffer; with guards, the middle of a larger buffer
+        whose GUARD_BYTES on each side hold the sentinel byte."""
+        n = 1
+        for x in shape:
+            n *= x
+        if self._guarded is None:
+            return torch.zeros(shape, dtype=dtype, device=self.device)
+        esz = torch.empty((), dtype=dtype).element_size()
+        nbytes = n * esz
+        body = (nbytes + 15) // 16 * 16
+        raw = torch.full((GUARD_BYTES + body + GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8,
+                         device=self.device)
+        raw[GUARD_BYTES:GUARD_BYTES + nbytes].zero_()
+        self._guarded.append((name, raw, nbytes))
+        return raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(shape)
+
+    def guard_damage(self):
+        """Names of the guarded buffers whose guard bytes (before the buffer, or
+        after its last element up to the guard's end) are no longer the
+        sentinel. Empty without guards."""
+        bad = []
+        for name, raw, nbytes in self._guarded or []:
+            host = raw.cpu().numpy()
+            if (host[:GUARD_BYTES] != GUARD_BYTE).any() or (host[GUARD_BYTES + nbytes:] != GUARD_BYTE).any():
+                bad.append(name)
+        return bad
 
     def set_seed(self, seed):
         """Write the Philox key to the device word (a device-side fill: capturable)."""
@@ -133,7 +170,7 @@ class DeviceCycle:
                              t["temperature"], seed, self.out_tokens, self.accept_count,
                              self.num_emitted, self.ws_verify, self.status, stream, P_t=self.P_t,
                              states=None if self.rnn is None else self.rnn["states"],
-                             seed_ptr=self.seed_dev),
+                             seed_ptr=self.seed_dev, p_token=self.p_token),
               "ds_verify")
 
     def run(self, seed, stream=None):
@@ -164,6 +201,7 @@ class DeviceCycle:
             "out_tokens": self.out_tokens.cpu().numpy().astype(np.int64),
             "accept_count": self.accept_count.cpu().numpy().astype(np.int64),
             "num_emitted": self.num_emitted.cpu().numpy().astype(np.int64),
+            "p_token": self.p_token.cpu().numpy().astype(np.float64),
             "states": None if self.rnn is None else
             self.rnn["states"].cpu().view(torch.int16).numpy().view(np.uint16),
         }

@@ -137,15 +137,38 @@ def test_transpose_projection_exact(ds, bf16):
 
 
 def test_independent_cycle_matches_oracle_cycle(ds):
-    """No teacher forcing: the oracle's own cycle and the GPU's agree end to end."""
+    """No teacher forcing: the oracle's own cycle and the GPU's agree end to end.
+
+    Each request's drafted tokens are compared up to its first near-tie draw
+    (after it the two may diverge legitimately). The schedule is compared when
+    no draft draw anywhere was a near tie (it reads every request's survivals),
+    and each request's verify outcome when, in addition, none of its own verify
+    decisions is a near tie."""
     import oracle
     inp = _ragged(True, (0.0, 1.0), 11, B=16, K=6, V=4096, r=64, d=128)
     _, g = _run(inp)
     o = oracle.cycle(inp, SEED)
-    if np.all(o["draft"]["margin"] > 1e-6):
-        assert np.array_equal(o["draft"]["tokens"], g["tokens"])
-        assert np.array_equal(o["schedule"]["L"], g["L"])
-        assert np.array_equal(o["verify"]["out_tokens"], g["out_tokens"])
+    B, K = inp["B"], inp["K"]
+    near = o["draft"]["margin"] < _parity.NEAR_TIE
+    compared = 0
+    for b in range(B):
+        k0 = int(np.argmax(near[b])) if near[b].any() else K
+        assert np.array_equal(o["draft"]["tokens"][b, :k0], g["tokens"][b, :k0]), b
+        compared += k0
+    assert compared >= 0.75 * B * K, compared
+    if near.any():
+        return
+    sch = o["schedule"]
+    if min(sch["stop_rel_gain"], sch["survival_gap"]) >= _parity.SCHED_NEAR_TIE:
+        assert np.array_equal(sch["L"], g["L"])
+    else:
+        return
+    checked = 0
+    for b in range(B):
+        if all(m >= _parity.NEAR_TIE for _, m in o["verify"]["decisions"][b]):
+            assert np.array_equal(o["verify"]["out_tokens"][b], g["out_tokens"][b]), b
+            checked += 1
+    assert checked >= B // 2, checked
 
 
 def test_masked_tokens_never_drawn(ds):
@@ -328,3 +351,43 @@ def test_full_size_workloads(ds, name, rows):
         sel = np.linspace(0, inp["B"] - 1, rows).astype(np.int64)
     rep = _parity.assert_parity(inp, g, SEED, rows=sel)
     print(name, json.dumps(rep))
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged_bf16", "ragged_f32", "k_limit", "r_limit_f32",
+                                  "B128_K16_V151936"])
+def test_no_write_outside_the_buffers(ds, case):
+    """Every buffer the library writes (outputs, workspaces, the token-major P
+    copy, the scheduler ring) sits between guard regions of sentinel bytes;
+    after a cycle, and after two cycles with the asynchronous scheduler, the
+    guards are intact, and the guarded cycle still matches the oracle. A
+    stand-in for a memory checker, which this pool does not offer."""
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.workloads import TINY, WORKLOADS, make_inputs
+    if case == "tiny":
+        inp = make_inputs(TINY)
+    elif case == "ragged_bf16":
+        inp = _ragged(True, (0.0, 0.6, 1.0), 41)
+    elif case == "ragged_f32":
+        inp = _ragged(False, (0.0, 0.6, 1.0), 43)
+    elif case == "k_limit":
+        inp = _ragged(True, (0.0, 1.0), 45, B=8, K=64, V=4096, r=64, d=64)
+    elif case == "r_limit_f32":
+        inp = _ragged(False, (0.6, 1.0), 47, B=5, K=3, V=2048, r=1024, d=64)
+    else:
+        inp = make_inputs(WORKLOADS[case])
+    cyc, g = _run(inp, guards=True)
+    assert cyc.guard_damage() == [], case
+    rows = None if inp["B"] <= 64 else np.linspace(0, inp["B"] - 1, 16).astype(np.int64)
+    _parity.assert_parity(inp, g, SEED, rows=rows)
+    cyc, _ = _run(inp, mode=_lib.DS_SCHED_ASYNC, guards=True)
+    cyc.reset_status()
+    cyc.run(SEED + 1)
+    cyc.check_status()
+    assert cyc.guard_damage() == [], (case, "async")
+
+
+def test_rnn_head_writes_nothing_outside_its_buffers(ds):
+    from speculative_decoding_draft_block_gb300.workloads import make_rnn_weights
+    inp = _ragged(True, (0.0, 0.6, 1.0), 49, B=20, K=4, V=4096, r=64, d=128)
+    cyc, _ = _run(inp, guards=True, rnn_weights=make_rnn_weights(64, 128))
+    assert cyc.guard_damage() == []

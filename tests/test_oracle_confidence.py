@@ -64,3 +64,61 @@ def test_survival_cumprod_and_monotone():
     rng = np.random.default_rng(3)
     s = survival(rng.random((50, 16)))
     assert np.all(np.diff(s, axis=1) <= 0)
+
+
+def test_hidden_state_term_reads_h_k_of_its_own_position():
+    """The w_h . h_k term, pinned in closed form with w_e = 0.
+
+    w_h is the unit vector e_j and h[b, k, j] = ln m[b, k] with m distinct for
+    every (b, k); the other hidden components are random (weight 0). Then
+    sigmoid(w_h . h_k) = m / (1 + m) exactly for that k, and sigmoid(ln m / T)
+    = m^(1/T) / (1 + m^(1/T)) under an STS temperature T. Reading h_{k+1} or
+    h_{k-1}, another request's row, or contracting the wrong axis gives
+    another m (or a random value) and fails.
+    """
+    B, K, d = 3, 5, 7
+    rng = np.random.default_rng(11)
+    m = 1.0 + np.arange(B * K, dtype=np.float64).reshape(B, K) * 0.37   # distinct, > 0
+    for j in (0, 4):
+        a = _setup(12, B=B, K=K, d=d)
+        a["w_e"][:] = 0.0
+        a["h"] = rng.normal(size=(B, K, d)) * 3.0
+        a["h"][:, :, j] = np.log(m)
+        a["w_h"] = np.zeros(d)
+        a["w_h"][j] = 1.0
+        c = confidence(bias=0.0, sts_temp=np.ones(K), **a)
+        for b in range(B):
+            for k in range(K):
+                assert abs(c[b, k] - m[b, k] / (1.0 + m[b, k])) < 1e-15, (j, b, k)
+        temps = np.array([0.5, 1.0, 2.0, 4.0, 0.8])
+        c = confidence(bias=0.0, sts_temp=temps, **a)
+        for b in range(B):
+            for k in range(K):
+                mt = m[b, k] ** (1.0 / temps[k])
+                assert abs(c[b, k] - mt / (1.0 + mt)) < 1e-14, (j, b, k)
+
+
+def test_hidden_and_embedding_terms_add_inside_the_sigmoid():
+    """Both terms and the bias together: w_h . h_k = ln a, w_e . E[x_{k-1}] = ln e,
+    b = ln 2 give c = 2ae / (1 + 2ae) (a product inside one sigmoid, not two
+    sigmoids or a sum of them)."""
+    B, K, d, V, r = 2, 4, 5, 9, 3
+    rng = np.random.default_rng(13)
+    a_val = 1.0 + rng.random((B, K))
+    e_val = 0.5 + rng.random(V)
+    h = rng.normal(size=(B, K, d))
+    h[:, :, 2] = np.log(a_val)
+    w_h = np.zeros(d)
+    w_h[2] = 1.0
+    E = rng.normal(size=(V, r))
+    E[:, 1] = np.log(e_val)
+    w_e = np.zeros(r)
+    w_e[1] = 1.0
+    anchor = rng.integers(0, V, size=B)
+    tokens = rng.integers(0, V, size=(B, K))
+    c = confidence(h, E, anchor, tokens, w_h, w_e, math.log(2.0), np.ones(K))
+    for b in range(B):
+        for k in range(K):
+            prev = anchor[b] if k == 0 else tokens[b, k - 1]
+            x = 2.0 * a_val[b, k] * e_val[prev]
+            assert abs(c[b, k] - x / (1.0 + x)) < 1e-15, (b, k)

@@ -226,3 +226,38 @@ def test_batch_verify_uses_right_rows_and_streams():
     for j in range(a):
         assert tokens[b, j] == np.argmax(tgt[b, j])
     assert out["out_tokens"][b, a] == np.argmax(tgt[b, a])
+
+
+def test_p_token_closed_form():
+    """p_k(x_k) of every scheduled position, pinned on hand-built target rows.
+
+    Target logits T * ln(1, 2, 3, 4) give p = (0.1, 0.2, 0.3, 0.4) at any
+    temperature T > 0; rows after a rejection are still reported (they are
+    scheduled), positions past L are NaN. Greedy requests report the point mass
+    of their argmax (token 3)."""
+    V, K = 4, 3
+    base = np.zeros((3, K, V))
+    E = np.zeros((V, 2))
+    P = np.zeros((2, V))
+    temps = np.array([1.0, 2.5, 0.0], dtype=np.float32)
+    tgt = np.zeros((3, K + 1, V))
+    for b, T in enumerate(temps):
+        tgt[b, :, :] = (T if T > 0 else 1.0) * np.log(np.arange(1.0, V + 1.0))
+    tokens = np.array([[2, 0, 1], [1, 3, 3], [3, 1, 3]])
+    res = verify(tgt, base, E, P, np.zeros(3, dtype=np.int64), tokens, np.array([3, 2, 3]), temps,
+                 seed=5, with_p=True)
+    p = res["p_token"]
+    want = np.array([0.3, 0.1, 0.2])
+    assert np.all(np.abs(p[0] - want) < 1e-15)
+    assert np.all(np.abs(p[1, :2] - np.array([0.2, 0.4])) < 1e-15) and np.isnan(p[1, 2])
+    assert p[2].tolist() == [1.0, 0.0, 1.0]
+    # the accept decisions read exactly these probabilities: q = 1/4 (uniform draft)
+    for j in range(res["accept_count"][0]):
+        assert oracle_uniform_accept(5, 0, j) * 0.25 < p[0, j]
+    assert "p_token" not in verify(tgt, base, E, P, np.zeros(3, dtype=np.int64), tokens,
+                                   np.array([3, 2, 3]), temps, seed=5)
+
+
+def oracle_uniform_accept(seed, b, j):
+    from oracle.philox import uniform, STAGE_ACCEPT
+    return uniform(seed, b, j + 1, STAGE_ACCEPT)
