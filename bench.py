@@ -532,6 +532,9 @@ def main():
                     help="time the launched calls instead of replays of one captured cycle")
     ap.add_argument("--head", choices=("markov", "rnn"), default="markov",
                     help="sequential head of the draft block (default: Markov)")
+    ap.add_argument("--l2-persist", type=float, default=None,
+                    help="MB of L2 to set aside for persisting lines (keeps P resident across "
+                         "the draft steps); default: P's size; 0 disables")
     ap.add_argument("--part", choices=("cycle", "sts"), default="cycle",
                     help="cycle: draft+schedule+verify (default); sts: the STS calibration fit")
     args = ap.parse_args()
@@ -567,6 +570,9 @@ def main():
         from speculative_decoding_draft_block_gb300.workloads import make_rnn_weights
         rnn_w = make_rnn_weights(w.r, w.d)
     cyc = DeviceCycle(inp, device=dev, mode=args.mode, threshold=args.threshold, rnn_weights=rnn_w)
+    p_bytes = w.r * w.V * (2 if w.bf16 else 4)
+    want = p_bytes if args.l2_persist is None else int(args.l2_persist * 1e6)
+    l2_persist = _lib.ds_reserve_persisting_l2(want)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
     seed0 = 0x5EED0000 + 7919 * rank
@@ -668,6 +674,7 @@ def main():
                    "threshold": args.threshold if args.mode == 2 else None,
                    "head": args.head, "cuda_graph": graph_launch_ms is not None,
                    "timing": "median of the timed cycles (CUDA events; max over ranks)",
+                   "l2_persisting_bytes": l2_persist,
                    "cuda_graph_error": graph_error},
         "ms_per_step_mean": float(cycle_ms.mean()),
         "components_ms": comp_med,

@@ -286,7 +286,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   p.temperature = a->temperature;
   const DraftLayout l = draft_layout(a->B, a->V, a->r);
   char* ws = reinterpret_cast<char*>(a->workspace);
-  const bool tc = tc_path_supported(a->dtype, a->r);
+  const bool tc = tc_path_supported(a->dtype, a->r, a->V);
   p.seed = a->seed;
   p.seed_ptr = a->seed_ptr;
   p.tokens_out = a->draft_tokens;
@@ -447,11 +447,11 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
   if (a->P_t != nullptr && !aligned16(a->P_t)) return DS_ERR_INVALID_ARG;
   const VerifyLayout l = verify_layout(a->B, a->K, a->V, a->r);
-  const bool tc = tc_path_supported(a->dtype, a->r);
+  const bool tc = tc_path_supported(a->dtype, a->r, a->V);
   if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < l.total)
     return DS_ERR_WORKSPACE;
   if (a->states != nullptr &&
-      (!aligned16(a->states) || !tc_path_supported(a->dtype, a->r) || a->dtype != DS_BF16))
+      (!aligned16(a->states) || !tc_path_supported(a->dtype, a->r, a->V) || a->dtype != DS_BF16))
     return DS_ERR_INVALID_ARG;
   if (a->seed_ptr != nullptr && ((uintptr_t)a->seed_ptr & 7u) != 0) return DS_ERR_INVALID_ARG;
   if (a->p_token != nullptr && !aligned16(a->p_token)) return DS_ERR_INVALID_ARG;
@@ -563,6 +563,23 @@ ds_status ds_fetch_scheduled_rows(void* dst, const void* src, int32_t B, int32_t
   return from_cuda(launch_fetch_rows(dst, src_dev, B, K, row_bytes, sched_len,
                                      reinterpret_cast<unsigned long long*>(bytes_total),
                                      (cudaStream_t)stream));
+}
+
+size_t ds_reserve_persisting_l2(size_t bytes) {
+  int dev = 0, maxp = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&maxp, cudaDevAttrMaxPersistingL2CacheSize, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  const size_t b = bytes < (size_t)(maxp > 0 ? maxp : 0) ? bytes : (size_t)(maxp > 0 ? maxp : 0);
+  if (cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, b) != cudaSuccess) (void)cudaGetLastError();
+  size_t cur = 0;
+  if (cudaDeviceGetLimit(&cur, cudaLimitPersistingL2CacheSize) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return cur;
 }
 
 ds_status ds_test_set_wait_hooks(uint32_t wait_polls, int32_t withhold_cta) {

@@ -8,12 +8,15 @@
 //
 //   warp 0      producer: TMA loads of P tiles (64 k-rows x 128 tokens per
 //               stage, 128B-swizzled, MN-major, L2 evict-last: P is re-read
-//               every step) and of the base-logit tiles (128 rows x 64 tokens
-//               per slot, evict-first).
+//               every step; it stays in L2 when the process has set aside
+//               persisting L2, see ds_reserve_persisting_l2) and of the
+//               staged A rows.
 //   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> f32),
 //               M = 128 requests, N = 128 tokens, K = r in steps of 16, into one
 //               of two TMEM accumulators (double-buffered against the epilogue).
-//   warps 2..   epilogue (kEpiWarps warps): gather the A operand (E rows of the
+//   warp 2      producer of the base-logit tiles (draft steps), in their own ring
+//   warp 3      idle (warpgroup 0 releases its registers to the epilogue)
+//   warps 4..   epilogue (kEpiWarps warps, 112 registers each): gather the A operand (E rows of the
 //               conditioning tokens, stored 128B-swizzled K-major) with 16-byte
 //               loads at each M-tile; then per tile tcgen05.ld of their TMEM
 //               slice, add the base logits from shared memory, and reduce every
@@ -45,10 +48,18 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kEpiWarps = 8;                    // multiple of 4 (TMEM lane quadrants)
+constexpr int kEpiWarps = 16;                   // multiple of 4 (TMEM lane quadrants)
+constexpr int kCtrlWarps = 4;                   // warpgroup 0: producer, MMA issuer, two idle warps
 constexpr int kColGroups = kEpiWarps / 4;       // column groups per lane quadrant
 constexpr int kChunks = 4 / kColGroups;         // 32-token chunks per thread per tile
-constexpr int kTcThreads = 64 + 32 * kEpiWarps;
+constexpr int kTcThreads = 32 * (kCtrlWarps + kEpiWarps);
+// Register split: warpgroup 0 (control) gives registers to the epilogue
+// warpgroups. The block launches with kLaunchRegs per thread (65536 / 640,
+// rounded down to the allocation unit of 8); the split uses exactly that pool.
+constexpr uint32_t kLaunchRegs = 96, kCtrlRegs = 32, kEpiRegs = 112;
+static_assert(32 * kCtrlWarps * kCtrlRegs + 32 * kEpiWarps * kEpiRegs <= kTcThreads * kLaunchRegs,
+              "register split exceeds the launch pool");
+static_assert(kTcThreads * kLaunchRegs <= 65536, "launch pool exceeds the register file");
 constexpr int kUnrollChunks = 1;                // code size over TMEM-load overlap
 constexpr int kTileN = 128;
 constexpr int kPStages = 6;           // 64 k-rows x 128 tokens of P each
@@ -69,6 +80,7 @@ static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1
 struct TcParams {
   SampleParams sp;
   int32_t n_mt, n_nt, nkb, tiles;
+
   uint32_t wait_polls;   // polls of a bounded wait before it gives up
   int32_t withhold_cta;  // test hook (-1: none), see set_tile_test_hooks
 };
@@ -143,26 +155,6 @@ __device__ __forceinline__ EpiRow epi_row_draft(const SampleParams& sp, int row)
   return c;
 }
 
-// Fast path of a full sampling chunk (bf16 logits; see fastpath.cuh). False
-// when the chunk needs the general path.
-__device__ __forceinline__ bool sample_chunk_fast(const G16& g16, const uint32_t* zp,
-                                                  const uint32_t* braw, ChunkRec& rec) {
-  int fref = 0;
-  if (!fast_chunk_ok(zp, g16, fref)) return false;
-  const FastConsts k = make_fast_consts(g16, fref);
-  float2 s = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    fast_pair(zp[i], make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])), k, s);
-  const float sum = __fadd_rn(s.x, s.y);
-  if (!(sum >= 0.f && isfinite(sum))) return false;
-  rec.hi = sum;
-  rec.lo = 0.f;
-  rec.ref = fref;
-  rec.idx = -2;  // fast-path record
-  return true;
-}
-
 // Fast path of a full chunk of the final draw (bf16; see fastpath.cuh): bonus
 // weights 2^(t g - Np), or residual weights max(0, 2^(t g - Np) - R 2^((z + b) g - Nq)),
 // both against the rows' global references. False when the chunk needs the
@@ -197,31 +189,32 @@ __device__ __forceinline__ bool final_chunk_fast(const EpiRow& c, const uint32_t
   return true;
 }
 
-// Greedy chunk: the largest z + bias as a double-float and its first token.
-// Same ordering as the general path; false on a NaN/+inf input, which the
-// general path then reports.
-__device__ __forceinline__ bool greedy_chunk_fast(const uint32_t* zp, const uint32_t* braw,
-                                                  int col0, ChunkRec& rec) {
-  DF best = {kNegInf, 0.f};
-  int bj = 0;
-  bool bad = false;
+// One 16-token half of a sampling chunk's fast path: tokens 16h .. 16h + 15,
+// zp8 their 8 packed logit words, b16 their bias columns. The pairs are
+// added in token order, as a whole-chunk pass would add them.
+__device__ __forceinline__ void sample_half(const uint32_t* zp8, const uint32_t* b16, const FastConsts& k,
+                                            float2& s) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t w = zp[j >> 1];
-    const float zj = __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
-    const float bb = __uint_as_float(braw[j]);
+  for (int i = 0; i < 8; ++i)
+    fast_pair(zp8[i], make_float2(__uint_as_float(b16[2 * i]), __uint_as_float(b16[2 * i + 1])), k, s);
+}
+
+// One 16-token half of a greedy chunk: the largest z + bias as a double-float
+// and its first token, continuing from the previous half (j0 = 16h).
+__device__ __forceinline__ void greedy_half(const uint32_t* zp8, const uint32_t* b16, int j0, DF& best,
+                                            int& bj, bool& bad) {
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    const uint32_t w = zp8[jj >> 1];
+    const float zj = __uint_as_float((jj & 1) ? (w & 0xffff0000u) : (w << 16));
+    const float bb = __uint_as_float(b16[jj]);
     bad |= bad_logit(zj) || !(bb == bb);
     const DF l = (zj == kNegInf) ? DF{kNegInf, 0.f} : two_sum(zj, bb);
-    if (j == 0 || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
+    if ((j0 == 0 && jj == 0) || l.hi > best.hi || (l.hi == best.hi && l.lo > best.lo)) {
       best = l;
-      bj = j;
+      bj = j0 + jj;
     }
   }
-  rec.hi = best.hi;
-  rec.lo = best.lo;
-  rec.ref = 0;
-  rec.idx = col0 + bj;
-  return !bad;
 }
 
 // The general path for the lanes with need set (greedy and sampling chunks
@@ -342,16 +335,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int t1 = (int)((long long)(blockIdx.x + 1) * prm.tiles / G);
   volatile int* abort_flag = &sh.abort_flag;
 
+  if (warp < kCtrlWarps) {
+    // warpgroup 0 hands registers to the epilogue warpgroups
+    setmaxnreg_dec<kCtrlRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_p = policy_evict_last();
-    const uint64_t pol_z = policy_evict_first();
-    if (lane == 0) {
-      prefetch_tmap(&tmP);
-      if (draft) prefetch_tmap(&tmZ);
-    }
+    if (lane == 0) prefetch_tmap(&tmP);
     if (lane == 0 && staged) prefetch_tmap(&tmA);
-    uint32_t pc = 0, zc = 0, a_loads = 0;
+    uint32_t pc = 0, a_loads = 0;
     int a_mt = -1;
     bool waited = draft && !staged, ok = true;  // a draft step's P and logits are inputs
     for (int t = t0, i = 0; t < t1 && ok; ++t, ++i) {
@@ -370,20 +362,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (!ok) break;
-      if (draft) {
-        for (int nb = 0; nb < 2 && ok; ++nb, ++zc) {
-          const uint32_t zs = zc % kZSlots;
-          if (lane == 0) {
-            ok = wait_bar(&sh.z_empty[zs], ((zc / kZSlots) & 1) ^ 1, abort_flag, sp.status, prm.wait_polls);
-            if (ok) {
-              mbar_expect_tx(&sh.z_full[zs], kZSlot);
-              tma_load_3d(sZ + zs * kZSlot, &tmZ, &sh.z_full[zs], n0 + nb * 64, sp.step - 1,
-                          mt * 128, pol_z);
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-      }
       if (ok && staged && mt != a_mt) {
         // this M-tile's A rows, written by the previous step's locate; issued after
         // the tile's P and logit loads so those are in flight during the wait, and
@@ -404,6 +382,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         ++a_loads;
         a_mt = mt;
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ logit producer
+    // the draft step's base-logit tiles (inputs: no dependent wait), in a ring
+    // of their own so they run ahead of the projection stream
+    if (draft) {
+      const uint64_t pol_z = policy_evict_first();
+      if (lane == 0) prefetch_tmap(&tmZ);
+      uint32_t zc = 0;
+      bool ok = true;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
+        const int n0 = nt * kTileN;
+        for (int nb = 0; nb < 2 && ok; ++nb, ++zc) {
+          const uint32_t zs = zc % kZSlots;
+          if (lane == 0) {
+            ok = wait_bar(&sh.z_empty[zs], ((zc / kZSlots) & 1) ^ 1, abort_flag, sp.status, prm.wait_polls);
+            if (ok) {
+              mbar_expect_tx(&sh.z_full[zs], kZSlot);
+              tma_load_3d(sZ + zs * kZSlot, &tmZ, &sh.z_full[zs], n0 + nb * 64, sp.step - 1,
+                          mt * 128, pol_z);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
       }
     }
   } else if (warp == 1) {
@@ -447,9 +451,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     __syncwarp();
+  }
   } else {
+    setmaxnreg_inc<kEpiRegs>();
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2, et = threadIdx.x - 64;
+    const int ew = warp - kCtrlWarps, et = threadIdx.x - 32 * kCtrlWarps;
     const int q = warp & 3, cg = ew >> 2;
     const int r_local = q * 32 + lane;
     int cur_mt = -1, pre_mt = -1;
@@ -541,22 +547,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       __syncwarp();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * kTileN;
-      const uint8_t* zb = sZ + zs * kZSlot + r_local * 128;
-      const uint8_t* tb = sZ + (draft ? zs : 2 + nb) * kZSlot + r_local * 128;
+      const uint8_t* zb = sZ + zs * kZSlot + r_local * 128;  // this row's line in its logit box
       const int sw = r_local & 7;
       // the final draw indexes its prefetched rows by j: fully unrolled there
 #pragma unroll(kFinal ? kChunks : kUnrollChunks)
       for (int j = 0; j < kChunks; ++j) {
-        uint32_t braw[32];
-        tmem_ld32_issue(tbase + (cg * kChunks + j) * 32, braw);
-        tmem_ld_wait(braw);
         const int ch0 = ((cg * kChunks + j) & 1) * 4;
         const int col0 = nt * kTileN + (cg * kChunks + j) * 32;
         const bool active = row < sp.B && c.mode != kSkip && col0 < sp.V;
         const int n = min(32, sp.V - col0);
         ChunkRec* out = sp.chunks + (size_t)(col0 >> 5) * sp.B + row;  // chunk-major: coalesced
         bool done = !active;
-        if (kFinal) {
+        if constexpr (kFinal) {
+          uint32_t braw[32];
+          tmem_ld32_issue(tbase + (cg * kChunks + j) * 32, braw);
+          tmem_ld_wait(braw);
           if (active && n == 32 && (c.mode == kResidual || c.mode == kBonus)) {
             uint32_t zp[16], tp[16];
 #pragma unroll
@@ -572,27 +577,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               group_merge(c.mode, gacc, rec);
             }
           }
-        } else if (active && n == 32 && (c.mode == kSampleMarkov || c.mode == kGreedyMarkov)) {
+        } else {
+          // the bias in two 16-column loads (warp-collective: every lane issues
+          // them), so only 16 bias registers are live
+          const bool fast = active && n == 32 && (c.mode == kSampleMarkov || c.mode == kGreedyMarkov);
+          const bool samp = c.mode == kSampleMarkov;
           uint32_t zp[16];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint4 v = *reinterpret_cast<const uint4*>(zb + (((ch0 + u) ^ sw) << 4));
+            const uint4 v = fast ? *reinterpret_cast<const uint4*>(zb + (((ch0 + u) ^ sw) << 4))
+                                 : make_uint4(0u, 0u, 0u, 0u);
             zp[4 * u] = v.x;
             zp[4 * u + 1] = v.y;
             zp[4 * u + 2] = v.z;
             zp[4 * u + 3] = v.w;
           }
-          ChunkRec rec;
-          done = (c.mode == kSampleMarkov) ? sample_chunk_fast(c.g16, zp, braw, rec)
-                                           : greedy_chunk_fast(zp, braw, col0, rec);
-          if (done) {
-            *out = rec;
-            group_merge(c.mode, gacc, rec);
+          int fref = 0;
+          bool ok = fast && (!samp || fast_chunk_ok(zp, c.g16, fref));
+          const FastConsts k = make_fast_consts(c.g16, fref);
+          float2 sum2 = make_float2(0.f, 0.f);
+          DF best = {kNegInf, 0.f};
+          int bj = 0;
+          bool bad = false;
+          const uint32_t taddr = tbase + (cg * kChunks + j) * 32;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t b16[16];
+            tmem_ld16_issue(taddr + 16 * h, b16);
+            tmem_ld16_wait(b16);
+            if (ok) {
+              if (samp)
+                sample_half(zp + 8 * h, b16, k, sum2);
+              else
+                greedy_half(zp + 8 * h, b16, 16 * h, best, bj, bad);
+            }
           }
+          if (ok) {
+            ChunkRec rec;
+            if (samp) {
+              const float sum = __fadd_rn(sum2.x, sum2.y);
+              ok = sum >= 0.f && isfinite(sum);
+              rec = {sum, 0.f, fref, -2};  // fast-path record
+            } else {
+              ok = !bad;
+              rec = {best.hi, best.lo, 0, col0 + bj};
+            }
+            if (ok) {
+              *out = rec;
+              group_merge(c.mode, gacc, rec);
+            }
+          }
+          done = !active || ok;
         }
         if (__any_sync(0xffffffffu, !done)) {
           const ChunkRec rec = slow_chunk_warp(&sp, row, !done, tbase + (cg * kChunks + j) * 32,
-                                               kFinal ? nullptr : zb, kFinal ? nullptr : tb, ch0, sw,
+                                               kFinal ? nullptr : zb, kFinal ? nullptr : zb, ch0, sw,
                                                col0, out);
           if (!done) group_merge(c.mode, gacc, rec);
         }
@@ -617,10 +656,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             group_merge(c.mode, g, *reinterpret_cast<const ChunkRec*>(xb + 16 * k));
           sp.supers[(size_t)row * sp.sup_stride + (blockIdx.x - first_group(sp, mt))] = g;
         }
-        // With two column groups the exchange line lies in the slot that only
-        // column group 0 releases, after these reads; more groups would share
-        // slots and need one more barrier here.
-        static_assert(kColGroups == 2, "the flush exchange assumes two column groups");
+        // The exchange line lies in the first logit slot of the tile. Only the
+        // column groups that read that slot release it (z_empty counts their
+        // warps), column group 0 among them, after these reads; the other
+        // groups wrote their records between the two barriers.
+        static_assert(kColGroups <= 8, "one 128-byte line holds the exchanged records");
       }
       // this warp is done with the tile's accumulator and logit slots
       tc_fence_before();
@@ -657,6 +697,15 @@ bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
   return encode_tmap_bf16(m, ptr, rank, dims, strides, box);
 }
 
+cudaError_t register_split_ok(const void* fn) {
+  cudaFuncAttributes a;
+  const cudaError_t e = cudaFuncGetAttributes(&a, fn);
+  if (e != cudaSuccess) return e;
+  const long long pool = (long long)kTcThreads * a.numRegs;
+  const long long need = 32LL * kCtrlWarps * kCtrlRegs + 32LL * kEpiWarps * kEpiRegs;
+  return (a.numRegs == (int)kLaunchRegs && need <= pool) ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 std::atomic<uint32_t> g_wait_polls{kWaitPolls};
 std::atomic<int32_t> g_withhold_cta{-1};
 
@@ -673,7 +722,7 @@ bool encode_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_
                       const cuuint64_t* strides, const cuuint32_t* box) {
   auto fn = get_encoder();
   if (!fn) return false;
-  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};  // up to rank 5
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -695,7 +744,8 @@ void set_tile_test_hooks(uint32_t wait_polls, int32_t withhold_cta) {
   g_withhold_cta.store(withhold_cta < 0 ? -1 : withhold_cta, std::memory_order_relaxed);
 }
 
-bool tc_path_supported(int32_t dtype, int32_t r) {
+bool tc_path_supported(int32_t dtype, int32_t r, int32_t V) {
+  (void)V;  // any V % 8 == 0 (the ABI's rule)
   return dtype == DS_BF16 && r % 64 == 0 && r >= 64 && r <= 256;
 }
 
@@ -706,11 +756,19 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
       tile_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (attr_d != cudaSuccess) return attr_d;
   if (attr_f != cudaSuccess) return attr_f;
+  // the register split inside the kernel needs exactly the launch pool it was
+  // planned for: refuse to launch a build whose launch count differs (an
+  // increase that cannot be satisfied would never return)
+  static cudaError_t regs_d = register_split_ok(reinterpret_cast<const void*>(tile_tc_kernel<false>));
+  static cudaError_t regs_f = register_split_ok(reinterpret_cast<const void*>(tile_tc_kernel<true>));
+  if (regs_d != cudaSuccess) return regs_d;
+  if (regs_f != cudaSuccess) return regs_f;
   TcParams prm;
   prm.sp = p;
   prm.n_mt = (p.B + 127) / 128;
   prm.n_nt = (p.V + kTileN - 1) / kTileN;
   prm.nkb = p.r / 64;
+  if (p.r % 64 != 0 || p.r > 256) return cudaErrorInvalidValue;
   prm.tiles = prm.n_mt * prm.n_nt;
   prm.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
   prm.withhold_cta = g_withhold_cta.load(std::memory_order_relaxed);
@@ -726,19 +784,10 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   {
     const cuuint64_t dims[3] = {V, (cuuint64_t)p.K, (cuuint64_t)p.B};
     const cuuint64_t str[2] = {V * 2, V * 2 * (cuuint64_t)p.K};
-    const cuuint32_t box_draft[3] = {64, 1, 128};
-    const cuuint32_t box_row[3] = {64, 1, 1};
-    if (!encode(&mZ, p.base_logits, 3, dims, str, p.src == 0 ? box_draft : box_row))
-      return cudaErrorInvalidValue;
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)(p.src == 0 ? 128 : 1)};  // final draw: plain loads
+    if (!encode(&mZ, p.base_logits, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  if (p.src == 0) {
-    mT = mZ;
-  } else {
-    const cuuint64_t dims[3] = {V, (cuuint64_t)(p.K + 1), (cuuint64_t)p.B};
-    const cuuint64_t str[2] = {V * 2, V * 2 * (cuuint64_t)(p.K + 1)};
-    const cuuint32_t box[3] = {64, 1, 1};
-    if (!encode(&mT, p.target_logits, 3, dims, str, box)) return cudaErrorInvalidValue;
-  }
+  mT = mZ;  // the final draw reads its rows with ordinary loads
   CUtensorMap mA = mP;  // unused unless A rows are staged
   if (p.a_stage_in != nullptr) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.r, (cuuint64_t)p.B};
@@ -759,6 +808,7 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+
   if (p.src == 0) return cudaLaunchKernelEx(&cfg, tile_tc_kernel<false>, prm, mP, mZ, mT, mA);
   return cudaLaunchKernelEx(&cfg, tile_tc_kernel<true>, prm, mP, mZ, mT, mA);
 }

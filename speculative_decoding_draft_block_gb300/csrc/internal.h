@@ -211,7 +211,7 @@ void tc_group_layout(SampleParams& p);
 void simt_group_layout(SampleParams& p);
 size_t sample_tile_smem_bytes(int32_t r);
 size_t locate_smem_bytes(int32_t V);
-bool tc_path_supported(int32_t dtype, int32_t r);
+bool tc_path_supported(int32_t dtype, int32_t r, int32_t V);
 // Test hooks of the tensor-core tile kernel (ds_test_set_wait_hooks).
 void set_tile_test_hooks(uint32_t wait_polls, int32_t withhold_cta);
 cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s);
