@@ -309,7 +309,9 @@ ds_status ds_sts_fit(const ds_sts_args* args, ds_stream_t stream);
  * y ~ p_{L_b+1} with u = U(seed, b, L_b+1, DS_STAGE_RESAMPLE) ([DFlash]: the
  * target scores K+1 positions per request). T_b = 0: accept iff x_k is the
  * target argmax; emit the target argmax. q_k is rebuilt from base_logits, E,
- * P and q_stats exactly as ds_draft_block defined it.
+ * P and q_stats exactly as ds_draft_block defined it. Target rows are read in
+ * position order across requests, and a request's rows after its first
+ * rejection are skipped once that rejection is known.
  */
 typedef struct {
   int32_t B, K, V, r;
@@ -336,9 +338,12 @@ typedef struct {
                                  with s_k . P); NULL for the Markov head */
   const uint64_t* seed_ptr;   /* optional device word holding the Philox key (overrides `seed`) */
   float* p_token;             /* optional out [B][K], or NULL: p_k(x_k), the target probability
-                                 the accept test reads, for every k <= L_b (rows after the first
-                                 rejection included); -1 for k > L_b. Greedy requests (T = 0):
-                                 1 if x_k is the target argmax, else 0 (the point mass). */
+                                 the accept test reads, for every position verify evaluated:
+                                 always k <= a_b + 1 (up to and including the first rejection);
+                                 a later scheduled position holds it too if its row was read
+                                 before the rejection was known, else -1; -1 for k > L_b.
+                                 Greedy requests (T = 0): 1 if x_k is the target argmax, else
+                                 0 (the point mass). */
 } ds_verify_args;
 
 size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);

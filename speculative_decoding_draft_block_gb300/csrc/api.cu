@@ -97,12 +97,13 @@ RnnLayout rnn_layout(int32_t B, int32_t K, int32_t r) {
 }
 
 struct VerifyLayout {
-  size_t vrows, desc, chunks, supers, total;
+  size_t queue, vrows, desc, chunks, supers, total;
 };
 
 VerifyLayout verify_layout(int32_t B, int32_t K, int32_t V, int32_t r) {
   VerifyLayout l;
-  l.vrows = 0;
+  l.queue = 0;  // first_reject[B]
+  l.vrows = l.queue + align_up((size_t)B * sizeof(uint32_t));
   l.desc = l.vrows + align_up((size_t)B * (K + 1) * sizeof(VRow));
   l.chunks = l.desc + align_up((size_t)B * sizeof(FinalDesc));
   (void)r;
@@ -481,8 +482,12 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   v.accept_count = a->accept_count;
   v.num_emitted = a->num_emitted;
   v.p_token = a->p_token;
+  v.first_reject = reinterpret_cast<uint32_t*>(ws + l.queue);
   v.status = a->status;
   const cudaStream_t s = (cudaStream_t)stream;
+  // no rejection recorded yet: first-rejection words all ones
+  if (cudaMemsetAsync(ws + l.queue, 0xff, (size_t)a->B * sizeof(uint32_t), s) != cudaSuccess)
+    return DS_ERR_CUDA;
   if (launch_verify_rows(v, s) != cudaSuccess) return DS_ERR_CUDA;
   if (launch_verify_finalize(v, s) != cudaSuccess) return DS_ERR_CUDA;
 

@@ -106,7 +106,10 @@ struct VerifyParams {
   int32_t* out_tokens;
   int32_t* accept_count;
   int32_t* num_emitted;
-  float* p_token;  // optional [B][K]: p_k(x_k) for k <= L_b, -1 beyond
+  float* p_token;  // optional [B][K]: p_k(x_k) of the rows evaluated, -1 elsewhere
+  // Per request, the lowest position whose accept test rejected (workspace,
+  // set to all ones -- none yet -- before the call).
+  uint32_t* first_reject;  // [B]
   int32_t* status;
 };
 

@@ -5,8 +5,10 @@
 // discards everything after it, and the rejection rule keeps the target's
 // distribution exactly. Per (request b, scheduled position k <= L_b + 1):
 //
-//   verify_rows_kernel      one CTA per target row: streams the row once with
-//                           16-byte loads, builds S_p = sum 2^(t_i g - ref)
+//   verify_rows_kernel      one CTA per target row, dispatched in position
+//                           order; a request's rows after its first recorded
+//                           rejection return at once; per row: streams it once
+//                           with 16-byte loads, builds S_p = sum 2^(t_i g - ref)
 //                           (per-thread power-of-two references merged
 //                           exactly, double-float sums), evaluates p(x_k) and
 //                           takes the accept decision u * q(x_k) < p(x_k) in
@@ -40,32 +42,28 @@ constexpr int kRowThreads = 512;
 // Only the normaliser S_p is needed here (for p(x) = w_x / S_p and the
 // residual ratio S_p / S_q), not a CDF, so each weight is 2^(z g_hi - R) with
 // one rounded FMA for the exponent and ex2.approx (relative error a few 1e-7
-// for the weights that carry the sum, unbiased), accumulated with Kahan
-// compensation in packed pairs. S_p then agrees with float64 to ~1e-7, far
-// inside the 1e-6 accept-test margin. A group that raises R rescales the sums
-// by an exact power of two; a group with a non-finite or out-of-range logit
-// takes the general path. Returns false if nothing was finite.
+// for the weights that carry the sum, unbiased); each 8-token group is summed
+// in float32 and added to a double-float total. S_p then agrees with float64
+// to ~1e-7, far inside the 1e-6 accept-test margin. A group that raises R
+// rescales the total by an exact power of two; a group with a non-finite or
+// out-of-range logit takes the general path. Returns false if nothing was
+// finite.
 __device__ __forceinline__ bool row_sum_bf16(const __nv_bfloat16* row, int V, int tid, Gscale g,
                                              DF& total, int& R, bool& bad) {
   R = INT_MIN;
   total = {0.f, 0.f};
-  float2 s2 = make_float2(0.f, 0.f), c2 = make_float2(0.f, 0.f);  // Kahan sum and compensation
-  const float2 G2 = make_float2(g.hi, g.hi), NEG1 = make_float2(-1.f, -1.f);
+  const float2 G2 = make_float2(g.hi, g.hi);
   float2 NR2 = make_float2(0.f, 0.f);  // -R
-  // fold the packed sums into the double-float total, then move the reference up to nr
-  auto fold = [&](int nr) {
-    total = df_add(total, df_add(DF{s2.x, -c2.x}, DF{s2.y, -c2.y}));
-    s2 = c2 = make_float2(0.f, 0.f);
-    if (nr > R) {
-      if (R != INT_MIN) {
-        const float f = pow2_clamped(R - nr);
-        total = {__fmul_rn(total.hi, f), __fmul_rn(total.lo, f)};
-      }
-      R = nr;
-      NR2 = make_float2(-(float)R, -(float)R);
+  // move the reference up to nr: the total so far is rescaled by an exact power of two
+  auto raise = [&](int nr) {
+    if (R != INT_MIN) {
+      const float f = pow2_clamped(R - nr);
+      total = {__fmul_rn(total.hi, f), __fmul_rn(total.lo, f)};
     }
+    R = nr;
+    NR2 = make_float2(-(float)R, -(float)R);
   };
-  auto group = [&](const uint4 v, int i) {
+  auto group = [&](const uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&w[0]);
 #pragma unroll
@@ -74,17 +72,18 @@ __device__ __forceinline__ bool row_sum_bf16(const __nv_bfloat16* row, int V, in
     const float amax = __fmul_rn(zmax, g.hi);
     if (fabsf(amax) < 4.0e6f) {  // finite and in range (NaN fails too)
       const int gref = (int)rintf(amax);
-      if (gref > R) fold(gref);
+      if (gref > R) raise(gref);
+      // the 8 weights (each <= 2) summed in float32 (one rounding per addition,
+      // relative error ~1e-7 per group, unbiased), then added exactly to the
+      // double-float total
+      float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float2 z2 = unpack_bf16x2(w[q]);
         const float2 a2 = __ffma2_rn(z2, G2, NR2);
-        const float2 w2 = make_float2(ex2_approx(a2.x), ex2_approx(a2.y));
-        const float2 y2 = __ffma2_rn(c2, NEG1, w2);
-        const float2 t2 = __fadd2_rn(s2, y2);
-        c2 = __ffma2_rn(y2, NEG1, __ffma2_rn(s2, NEG1, t2));
-        s2 = t2;
+        s2 = __fadd2_rn(s2, make_float2(ex2_approx(a2.x), ex2_approx(a2.y)));
       }
+      df_accumulate(total, __fadd_rn(s2.x, s2.y));
       return;
     }
     // general path for this group (relative to R, or to a new R if none yet)
@@ -102,39 +101,43 @@ __device__ __forceinline__ bool row_sum_bf16(const __nv_bfloat16* row, int V, in
     }
     if (am == kNegInf) return;
     const int ng = (int)rintf(am);
-    if (ng > R) fold(ng);
+    if (ng > R) raise(ng);
 #pragma unroll
     for (int q = 0; q < 8; ++q) df_accumulate(total, weight_rel(f8[q], 0.f, g, R));
   };
-  // four 16-byte loads in flight per thread
-  constexpr int kStride = kRowThreads * 8;
-  for (int i0 = tid * 8; i0 < V; i0 += 4 * kStride) {
-    uint4 v[4];
+  // kLoads 16-byte loads in flight per thread
+  constexpr int kStride = kRowThreads * 8, kLoads = 4;
+  for (int i0 = tid * 8; i0 < V; i0 += kLoads * kStride) {
+    uint4 v[kLoads];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kLoads; ++u)
       if (i0 + u * kStride < V) v[u] = __ldcs(reinterpret_cast<const uint4*>(row + i0 + u * kStride));
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (i0 + u * kStride < V) group(v[u], i0 + u * kStride);
+    for (int u = 0; u < kLoads; ++u)
+      if (i0 + u * kStride < V) group(v[u]);
   }
-  fold(R);
   return R != INT_MIN;
 }
 
+struct RowShared {
+  float sv[kRowThreads / 32];
+  int si[kRowThreads / 32];
+  int sref[kRowThreads / 32];
+  DF sdf[kRowThreads];
+  int len, skip;  // the row's scheduled length and skip decision, from thread 0
+};
+
+// Target row j of request b (j <= L): S_p, and for j < L the accept test of
+// the drafted token at position j + 1 (greedy: exact match with the argmax).
+// Called by the whole CTA; returns the accept flag (thread 0's copy).
 template <typename Tin>
-__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p) {
-  __shared__ float sv[kRowThreads / 32];
-  __shared__ int si[kRowThreads / 32];
-  __shared__ int sref[kRowThreads / 32];
-  __shared__ DF sdf[kRowThreads];
-  const int j = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+__device__ __forceinline__ bool verify_row(const VerifyParams& p, int b, int j, int L, RowShared& sh) {
+  float* sv = sh.sv;
+  int* si = sh.si;
+  int* sref = sh.sref;
+  DF* sdf = sh.sdf;
+  const int tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5;
-  int L = p.sched_len[b];
-  if (L < 0 || L > p.K) {
-    if (tid == 0) report(p.status, kErrInvalidArg);
-    L = L < 0 ? 0 : p.K;
-  }
-  if (j > L) return;
   const float T = p.temperature[b];
   const Tin* row = reinterpret_cast<const Tin*>(p.target_logits) + ((size_t)b * (p.K + 1) + j) * (size_t)p.V;
   VRow out;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
   } else {
     if (!(T >= 1e-3f && T <= 1e3f)) {
       if (tid == 0) report(p.status, kErrInvalidArg);
-      return;
+      return false;
     }
     const Gscale g = make_gscale(T);
     int nt = INT_MIN;
@@ -259,6 +262,44 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p
   }
   if (bad) report(p.status, kErrNonfinite);
   if (tid == 0) p.vrows[(size_t)b * (p.K + 1) + j] = out;
+  return out.accept != 0;
+}
+
+// One CTA per target row, launched position-major (blockIdx.y is the position),
+// so every request's row 0 is dispatched first, then row 1, and so on. A CTA
+// whose request already recorded a rejection at an earlier position returns at
+// once (verification stops at the first rejection), so the rows streamed
+// approach sum_b min(a_b + 1, L_b + 1). A row started before the earlier
+// result is known is still evaluated: the finalize kernel reads rows only up
+// to the first rejection.
+template <typename Tin>
+__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyParams p) {
+  __shared__ RowShared sh;
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x, j = blockIdx.y;
+  // thread 0 decides for the CTA: first_reject changes under other CTAs, so no
+  // other thread reads it (every thread must take the same path)
+  if (tid == 0) {
+    int L = p.sched_len[b];
+    if (L < 0 || L > p.K) {
+      if (j == 0) report(p.status, kErrInvalidArg);
+      L = L < 0 ? 0 : p.K;
+    }
+    int skip = 0;
+    if (j > L) {
+      skip = 2;  // not scheduled
+    } else if (*reinterpret_cast<volatile uint32_t*>(p.first_reject + b) < (uint32_t)j) {
+      skip = 1;  // an earlier row rejected
+      if (j < L && p.p_token != nullptr) p.p_token[(size_t)b * p.K + j] = -1.f;  // not evaluated
+    }
+    sh.len = L;
+    sh.skip = skip;
+  }
+  __syncthreads();
+  const int L = sh.len;
+  if (sh.skip) return;
+  const bool acc = verify_row<Tin>(p, b, j, L, sh);
+  if (tid == 0 && j < L && !acc) atomicMin(p.first_reject + b, (uint32_t)j);
 }
 
 // One warp per request: lane 0 walks the accept flags and writes the final
@@ -319,7 +360,7 @@ __global__ void __launch_bounds__(128) verify_finalize_kernel(VerifyParams p) {
 }  // namespace
 
 cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s) {
-  dim3 grid(p.K + 1, p.B);
+  dim3 grid(p.B, p.K + 1);  // position-major dispatch order
   if (p.dtype == DS_BF16)
     verify_rows_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, s>>>(p);
   else

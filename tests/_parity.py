@@ -153,16 +153,25 @@ def compare_verify(inp, g, seed, request_ids=None):
            "mismatched_requests": int(len(bad_req)), "unexplained": unexplained,
            "near_ties": int(near)}
     if g.get("p_token") is not None:
-        # p_k(x_k) of every verified position (k <= L_b) against float64; -1 beyond L_b
+        # p_k(x_k) of the positions verify evaluated, against float64: every
+        # position up to and including the first rejection must be evaluated;
+        # later scheduled positions may be (-1 when skipped); -1 past L_b
         K = g["tokens"].shape[1]
-        sched = np.arange(K)[None, :] < np.asarray(g["L"])[:, None]
+        pos = np.arange(K)[None, :]
+        L = np.asarray(g["L"])[:, None]
+        a = np.asarray(g["accept_count"])[:, None]
+        sched = pos < L
         gp, op = g["p_token"], o["p_token"]
         assert np.all(gp[~sched] == -1.0), "p_token not -1 past the scheduled length"
-        greedy = (np.asarray(inp["temperature"]) == 0)[:, None] & sched
+        must = sched & (pos <= a)
+        assert np.all(gp[must] != -1.0), "a position up to the first rejection was not evaluated"
+        ev = sched & (gp != -1.0)
+        greedy = (np.asarray(inp["temperature"]) == 0)[:, None] & ev
         assert np.array_equal(gp[greedy], op[greedy]), "greedy p_token is not the point mass"
-        samp = sched & ~greedy
+        samp = ev & ~greedy
         rel = np.abs(gp[samp] - op[samp]) / np.maximum(op[samp], 1e-30)
         rep["p_compared"] = int(samp.sum())
+        rep["p_skipped"] = int((sched & (gp == -1.0)).sum())
         rep["p_max_rel"] = float(rel.max()) if rel.size else 0.0
     return rep, o
 
