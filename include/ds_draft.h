@@ -294,6 +294,25 @@ typedef struct {
 } ds_sts_args;
 
 size_t ds_sts_workspace_bytes(int32_t N, int32_t K, int32_t n_grid, int32_t n_bins);
+
+/*
+ * The STS fit's soft labels ([DSpark] 방법론 › 신뢰도 기반 검증: the calibration
+ * is supervised by the analytic acceptance 1 - TV; [DSpark] 배경: the accept
+ * rule min(1, p / q)). For each of `rows` rows n:
+ *     alpha[n] = sum_i min(p_n(i), q_n(i)),  p_n = softmax(target[n] / T_n),
+ *                                            q_n = softmax(draft[n] / T_n),
+ * the probability that a token drawn from q_n passes verification against
+ * p_n. T_n = 0 (greedy): 1 if both rows' argmax (lowest index on ties) agree,
+ * else 0. target_logits and draft_logits are [rows][V] (dtype), temperature
+ * [rows] float32, alpha out [rows] float32 in [0, 1]; all device pointers,
+ * 16-byte aligned; V % 8 == 0. Float32 arithmetic (relative error ~1e-5).
+ * Device errors: a NaN or +inf logit, or a row without a finite logit ->
+ * DS_ERR_NONFINITE; a temperature outside {0} u [1e-3, 1e3] ->
+ * DS_ERR_INVALID_ARG (that row's alpha is 0).
+ */
+ds_status ds_acceptance_rate(const void* target_logits, const void* draft_logits, int32_t rows, int32_t V,
+                             int32_t dtype, const float* temperature, float* alpha, int32_t* status,
+                             ds_stream_t stream);
 ds_status ds_sts_fit(const ds_sts_args* args, ds_stream_t stream);
 
 /* ------------------------------------------------------------------------ */

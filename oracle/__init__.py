@@ -38,6 +38,10 @@ Parity status per function (see the pins in tests/test_oracle_*.py):
                                   form, exact recovery of the true temperatures
                                   with zero ECE, prefix and causality
                                   metamorphic tests, first-index ties)
+  acceptance_rate ............... pinned (equals the verify rule's accept
+                                  probability integrated exactly over u;
+                                  p = q gives 1, disjoint supports 0; T = 0
+                                  argmax agreement)
   gru_cell, rnn_draft_block ..... pinned (torch.nn.GRUCell in float64, closed
                                   forms with saturated gates, a frozen zero
                                   state drawing from the base logits alone,
@@ -57,6 +61,7 @@ from .cycle import cycle
 from .bf16 import bf16_bits_to_f64
 from .sts import sts_fit, sts_curves, ece
 from .rnn import gru_cell, rnn_draft_block
+from .acceptance import acceptance_rate
 
 __all__ = [
     "philox4x32_10", "uniform", "STAGE_DRAFT", "STAGE_ACCEPT", "STAGE_RESAMPLE",
@@ -66,5 +71,5 @@ __all__ = [
     "schedule", "sps_at", "async_budgets", "SCHED_GREEDY_EARLYSTOP", "SCHED_FIXED_K",
     "SCHED_THRESHOLD", "SCHED_ASYNC",
     "verify", "verify_request", "cycle", "bf16_bits_to_f64",
-    "sts_fit", "sts_curves", "ece", "gru_cell", "rnn_draft_block",
+    "sts_fit", "sts_curves", "ece", "gru_cell", "rnn_draft_block", "acceptance_rate",
 ]

@@ -28,7 +28,8 @@ EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspa
            "ds_verify_workspace_bytes", "ds_verify", "ds_check_status", "ds_status_string",
            "ds_version", "ds_transpose_projection", "ds_verify_static", "ds_sts_workspace_bytes",
            "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights", "ds_copy_scheduled_rows",
-           "ds_fetch_scheduled_rows", "ds_test_set_wait_hooks", "ds_reserve_persisting_l2")
+           "ds_fetch_scheduled_rows", "ds_test_set_wait_hooks", "ds_reserve_persisting_l2",
+           "ds_acceptance_rate")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -117,6 +118,8 @@ def load():
     lib.ds_copy_scheduled_rows.restype = ctypes.c_int
     lib.ds_fetch_scheduled_rows.argtypes = [_vp, _vp, _i32, _i32, ctypes.c_size_t, _vp, _vp, _vp]
     lib.ds_fetch_scheduled_rows.restype = ctypes.c_int
+    lib.ds_acceptance_rate.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
+    lib.ds_acceptance_rate.restype = ctypes.c_int
     lib.ds_reserve_persisting_l2.argtypes = [ctypes.c_size_t]
     lib.ds_reserve_persisting_l2.restype = ctypes.c_size_t
     lib.ds_test_set_wait_hooks.argtypes = [ctypes.c_uint32, _i32]
@@ -293,6 +296,14 @@ def ds_transpose_projection(P, P_t, stream=None):
     r, V = P.shape
     return load().ds_transpose_projection(_ptr(P, "P"), r, V, _dtype_code(P), _ptr(P_t, "P_t"),
                                           _stream(stream))
+
+
+def ds_acceptance_rate(target_logits, draft_logits, temperature, alpha, status, stream=None):
+    """alpha[n] = sum_i min(p_n(i), q_n(i)) of [rows, V] target and draft logits."""
+    rows, V = target_logits.shape
+    return load().ds_acceptance_rate(_ptr(target_logits, "target_logits"), _ptr(draft_logits, "draft_logits"),
+                                     rows, V, _dtype_code(target_logits), _ptr(temperature, "temperature"),
+                                     _ptr(alpha, "alpha"), _ptr(status, "status"), _stream(stream))
 
 
 def ds_reserve_persisting_l2(nbytes):

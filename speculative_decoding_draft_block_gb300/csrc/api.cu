@@ -570,6 +570,20 @@ ds_status ds_fetch_scheduled_rows(void* dst, const void* src, int32_t B, int32_t
                                      (cudaStream_t)stream));
 }
 
+ds_status ds_acceptance_rate(const void* target_logits, const void* draft_logits, int32_t rows, int32_t V,
+                             int32_t dtype, const float* temperature, float* alpha, int32_t* status,
+                             ds_stream_t stream) {
+  if (rows < 1 || V < 8 || V % 8 != 0) return DS_ERR_INVALID_ARG;
+  if (dtype != DS_F32 && dtype != DS_BF16) return DS_ERR_INVALID_ARG;
+  const void* ptrs[] = {target_logits, draft_logits, temperature, alpha, status};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return DS_ERR_INVALID_ARG;
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  return from_cuda(launch_acceptance(target_logits, draft_logits, rows, V, dtype, temperature, alpha, status,
+                                     (cudaStream_t)stream));
+}
+
 size_t ds_reserve_persisting_l2(size_t bytes) {
   int dev = 0, maxp = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||

@@ -227,6 +227,8 @@ cudaError_t launch_verify_finalize(const VerifyParams& p, cudaStream_t s);
 cudaError_t launch_fetch_rows(void* dst, const void* src_dev, int32_t B, int32_t K, size_t row_bytes,
                               const int32_t* sched_len, unsigned long long* bytes, cudaStream_t s);
 cudaError_t launch_confidence(const SchedParams& p, cudaStream_t s);
+cudaError_t launch_acceptance(const void* target, const void* draft, int32_t rows, int32_t V, int32_t dtype,
+                              const float* temperature, float* alpha, int32_t* status, cudaStream_t s);
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t s);
 cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t s);
 size_t schedule_smem_bytes(int32_t B, int32_t K);
