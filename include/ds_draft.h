@@ -167,6 +167,9 @@ typedef struct {
   const float* rnn_b_hh;      /* [3r] */
   void* states;               /* out [B][K][r] s_k of every position (bfloat16) */
   const uint64_t* seed_ptr;   /* optional device word holding the Philox key (overrides `seed`) */
+  const void* P_packed;       /* optional tile-packed copy of P written by ds_pack_projection
+                                 (bfloat16, 64 <= r <= 256, r % 64 == 0), or NULL; results do
+                                 not depend on it, the tensor-core tiles load it faster */
 } ds_draft_args;
 
 size_t ds_draft_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);
@@ -184,6 +187,23 @@ size_t ds_rnn_workspace_bytes(int32_t B, int32_t K, int32_t r);
  */
 ds_status ds_rnn_pack_weights(const void* W_ih, const void* W_hh, int32_t r, int32_t d, int32_t dtype,
                               void* W_step, ds_stream_t stream);
+
+/*
+ * Tile-packed copy of the Markov projection, once per model (like
+ * ds_transpose_projection): for each 128-token tile, its r x 128 slice of P in
+ * the 128-byte-swizzled shared-memory image the tensor cores read (64-row
+ * k-blocks of two 64-token halves; in each 64 x 128-byte half, the 16-byte
+ * unit u of row m stored at unit u ^ (m % 8)); tokens past V are zero. With it
+ * the tile kernel brings each 32 KB stage in with one bulk copy instead of one
+ * tensor copy per 128-byte row. bfloat16 only, 64 <= r <= 256, r % 64 == 0
+ * (DS_ERR_UNSUPPORTED otherwise); P and P_packed device pointers, 16-byte
+ * aligned, not overlapping; P_packed holds ds_packed_projection_bytes(r, V)
+ * bytes (0 for unsupported shapes), packed_bytes its size (DS_ERR_WORKSPACE if
+ * smaller). A bit-exact rearrangement of P.
+ */
+size_t ds_packed_projection_bytes(int32_t r, int32_t V);
+ds_status ds_pack_projection(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_packed,
+                             size_t packed_bytes, ds_stream_t stream);
 
 /*
  * Token-major copy of the Markov projection: P_t[v][k] = P[k][v] for
@@ -363,6 +383,7 @@ typedef struct {
                                  before the rejection was known, else -1; -1 for k > L_b.
                                  Greedy requests (T = 0): 1 if x_k is the target argmax, else
                                  0 (the point mass). */
+  const void* P_packed;       /* optional tile-packed copy of P, as in ds_draft_args */
 } ds_verify_args;
 
 size_t ds_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t r);

@@ -29,7 +29,7 @@ EXPORTS = ("ds_philox4x32_10", "ds_uniform", "ds_philox_fill", "ds_draft_workspa
            "ds_version", "ds_transpose_projection", "ds_verify_static", "ds_sts_workspace_bytes",
            "ds_sts_fit", "ds_rnn_workspace_bytes", "ds_rnn_pack_weights", "ds_copy_scheduled_rows",
            "ds_fetch_scheduled_rows", "ds_test_set_wait_hooks", "ds_reserve_persisting_l2",
-           "ds_acceptance_rate")
+           "ds_acceptance_rate", "ds_packed_projection_bytes", "ds_pack_projection")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -42,7 +42,8 @@ class DraftArgs(ctypes.Structure):
                 ("q_token", _vp), ("q_stats", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("status", _vp),
                 ("head", _i32), ("d", _i32), ("h", _vp), ("rnn_w_ih", _vp), ("rnn_w_step", _vp),
-                ("rnn_b_ih", _vp), ("rnn_b_hh", _vp), ("states", _vp), ("seed_ptr", _vp)]
+                ("rnn_b_ih", _vp), ("rnn_b_hh", _vp), ("states", _vp), ("seed_ptr", _vp),
+                ("P_packed", _vp)]
 
 
 class SchedArgs(ctypes.Structure):
@@ -70,7 +71,7 @@ class VerifyArgs(ctypes.Structure):
                 ("sched_len", _vp), ("temperature", _vp), ("seed", ctypes.c_uint64),
                 ("out_tokens", _vp), ("accept_count", _vp), ("num_emitted", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("status", _vp),
-                ("states", _vp), ("seed_ptr", _vp), ("p_token", _vp)]
+                ("states", _vp), ("seed_ptr", _vp), ("p_token", _vp), ("P_packed", _vp)]
 
 
 _lib = None
@@ -118,6 +119,10 @@ def load():
     lib.ds_copy_scheduled_rows.restype = ctypes.c_int
     lib.ds_fetch_scheduled_rows.argtypes = [_vp, _vp, _i32, _i32, ctypes.c_size_t, _vp, _vp, _vp]
     lib.ds_fetch_scheduled_rows.restype = ctypes.c_int
+    lib.ds_packed_projection_bytes.argtypes = [_i32, _i32]
+    lib.ds_packed_projection_bytes.restype = ctypes.c_size_t
+    lib.ds_pack_projection.argtypes = [_vp, _i32, _i32, _i32, _vp, ctypes.c_size_t, _vp]
+    lib.ds_pack_projection.restype = ctypes.c_int
     lib.ds_acceptance_rate.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
     lib.ds_acceptance_rate.restype = ctypes.c_int
     lib.ds_reserve_persisting_l2.argtypes = [ctypes.c_size_t]
@@ -210,7 +215,7 @@ def ds_verify_workspace_bytes(B, K, V, r):
 # ---- the three calls ----------------------------------------------------------
 
 def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q_token, q_stats,
-                   workspace, status, stream=None, P_t=None, rnn=None, seed_ptr=None):
+                   workspace, status, stream=None, P_t=None, rnn=None, seed_ptr=None, P_packed=None):
     """Draft one block. ``rnn`` selects the RNN head: a dict with h [B, K, d],
     w_ih [3r, r + d], w_step (from ds_rnn_pack_weights), b_ih, b_hh (float32
     [3r]) and states (output [B, K, r]); the workspace must then also hold
@@ -231,7 +236,8 @@ def ds_draft_block(base_logits, E, P, anchor, temperature, seed, draft_tokens, q
                   workspace=_ptr(workspace, "workspace"),
                   workspace_bytes=workspace.numel() * workspace.element_size(),
                   status=_ptr(status, "status"),
-                  seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"), **extra)
+                  seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"),
+                  P_packed=None if P_packed is None else _ptr(P_packed, "P_packed"), **extra)
     return load().ds_draft_block(ctypes.byref(a), _stream(stream))
 
 
@@ -270,7 +276,7 @@ def ds_confidence_schedule(h, E, anchor, draft_tokens, w_h, w_e, bias, sts_temp,
 
 def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats, sched_len,
               temperature, seed, out_tokens, accept_count, num_emitted, workspace, status,
-              stream=None, P_t=None, states=None, seed_ptr=None, p_token=None):
+              stream=None, P_t=None, states=None, seed_ptr=None, p_token=None, P_packed=None):
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
                    target_logits=_ptr(target_logits, "target_logits"),
@@ -287,8 +293,20 @@ def ds_verify(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q
                    status=_ptr(status, "status"),
                    states=None if states is None else _ptr(states, "states"),
                    seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"),
-                   p_token=None if p_token is None else _ptr(p_token, "p_token"))
+                   p_token=None if p_token is None else _ptr(p_token, "p_token"),
+                   P_packed=None if P_packed is None else _ptr(P_packed, "P_packed"))
     return load().ds_verify(ctypes.byref(a), _stream(stream))
+
+
+def ds_packed_projection_bytes(r, V):
+    return int(load().ds_packed_projection_bytes(r, V))
+
+
+def ds_pack_projection(P, P_packed, stream=None):
+    """Tile-packed copy of the bfloat16 projection P [r, V] (once per model; see ds_draft.h)."""
+    r, V = P.shape
+    return load().ds_pack_projection(_ptr(P, "P"), r, V, _dtype_code(P), _ptr(P_packed, "P_packed"),
+                                     P_packed.numel() * P_packed.element_size(), _stream(stream))
 
 
 def ds_transpose_projection(P, P_t, stream=None):
@@ -319,7 +337,7 @@ def ds_test_set_wait_hooks(wait_polls, withhold_cta):
 
 def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_token, q_stats,
                      sched_len, temperature, seed, out_tokens, accept_count, num_emitted, status,
-                     stream=None, P_t=None, states=None, seed_ptr=None, p_token=None):
+                     stream=None, P_t=None, states=None, seed_ptr=None, p_token=None, P_packed=None):
     """ds_verify with the library's static scratch (no workspace argument)."""
     B, K1, V = target_logits.shape
     a = VerifyArgs(B=B, K=K1 - 1, V=V, r=E.shape[1], dtype=_dtype_code(target_logits),
@@ -335,7 +353,8 @@ def ds_verify_static(target_logits, base_logits, E, P, anchor, draft_tokens, q_t
                    workspace=None, workspace_bytes=0, status=_ptr(status, "status"),
                    states=None if states is None else _ptr(states, "states"),
                    seed_ptr=None if seed_ptr is None else _ptr(seed_ptr, "seed_ptr"),
-                   p_token=None if p_token is None else _ptr(p_token, "p_token"))
+                   p_token=None if p_token is None else _ptr(p_token, "p_token"),
+                   P_packed=None if P_packed is None else _ptr(P_packed, "P_packed"))
     return load().ds_verify_static(ctypes.byref(a), _stream(stream))
 
 

@@ -223,6 +223,26 @@ ds_status ds_philox_fill(const uint32_t* ctr, uint32_t key0, uint32_t key1, uint
   return from_cuda(launch_philox_fill(ctr, key0, key1, out, n, (cudaStream_t)stream));
 }
 
+size_t ds_packed_projection_bytes(int32_t r, int32_t V) {
+  if (!shape_ok(1, 1, V, r) || !tc_path_supported(DS_BF16, r, V)) return 0;
+  return packed_projection_bytes(r, V);
+}
+
+ds_status ds_pack_projection(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_packed,
+                             size_t packed_bytes, ds_stream_t stream) {
+  if (!shape_ok(1, 1, V, r)) return DS_ERR_INVALID_ARG;
+  if (dtype != DS_BF16 || !tc_path_supported(dtype, r, V)) return DS_ERR_UNSUPPORTED;
+  if (P == nullptr || P_packed == nullptr || !aligned16(P) || !aligned16(P_packed)) return DS_ERR_INVALID_ARG;
+  const size_t need = packed_projection_bytes(r, V);
+  if (packed_bytes < need) return DS_ERR_WORKSPACE;
+  const char* a = static_cast<const char*>(P);
+  const char* b = static_cast<const char*>(P_packed);
+  if (a < b + need && b < a + (size_t)r * V * 2) return DS_ERR_INVALID_ARG;  // overlapping
+  const ds_status st = device_supported();
+  if (st != DS_OK) return st;
+  return from_cuda(launch_pack_projection(P, r, V, P_packed, (cudaStream_t)stream));
+}
+
 ds_status ds_transpose_projection(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_t,
                                   ds_stream_t stream) {
   if (!shape_ok(1, 1, V, r)) return DS_ERR_INVALID_ARG;
@@ -251,6 +271,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
   if (a->P_t != nullptr && !aligned16(a->P_t)) return DS_ERR_INVALID_ARG;
+  if (a->P_packed != nullptr && !aligned16(a->P_packed)) return DS_ERR_INVALID_ARG;
   if (a->seed_ptr != nullptr && ((uintptr_t)a->seed_ptr & 7u) != 0) return DS_ERR_INVALID_ARG;
   const bool rnn = a->head == DS_HEAD_RNN;
   if (a->head != DS_HEAD_MARKOV && !rnn) return DS_ERR_INVALID_ARG;
@@ -282,6 +303,7 @@ ds_status ds_draft_block(const ds_draft_args* a, ds_stream_t stream) {
   p.E = a->E;
   p.P = a->P;
   p.P_t = a->P_t;
+  p.P_packed = a->P_packed;
   p.anchor = a->anchor;
   p.draft_tokens = a->draft_tokens;
   p.temperature = a->temperature;
@@ -447,6 +469,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   for (const void* p : ptrs)
     if (!aligned16(p)) return DS_ERR_INVALID_ARG;
   if (a->P_t != nullptr && !aligned16(a->P_t)) return DS_ERR_INVALID_ARG;
+  if (a->P_packed != nullptr && !aligned16(a->P_packed)) return DS_ERR_INVALID_ARG;
   const VerifyLayout l = verify_layout(a->B, a->K, a->V, a->r);
   const bool tc = tc_path_supported(a->dtype, a->r, a->V);
   if (a->workspace == nullptr || !aligned16(a->workspace) || a->workspace_bytes < l.total)
@@ -505,6 +528,7 @@ ds_status ds_verify(const ds_verify_args* a, ds_stream_t stream) {
   p.E = a->E;
   p.P = a->P;
   p.P_t = a->P_t;
+  p.P_packed = a->P_packed;
   p.anchor = a->anchor;
   p.draft_tokens = a->draft_tokens;
   p.temperature = a->temperature;

@@ -62,7 +62,10 @@ static_assert(32 * kCtrlWarps * kCtrlRegs + 32 * kEpiWarps * kEpiRegs <= kTcThre
 static_assert(kTcThreads * kLaunchRegs <= 65536, "launch pool exceeds the register file");
 constexpr int kUnrollChunks = 1;                // code size over TMEM-load overlap
 constexpr int kTileN = 128;
-constexpr int kPStages = 6;           // 64 k-rows x 128 tokens of P each
+// The P ring is kPRing bytes: kPStages stages of one 64-row k-block (16 KB,
+// two tensor copies of 64 rows each), or, with the tile-packed copy of P,
+// kPStages / 2 stages of two k-blocks (32 KB, one bulk copy).
+constexpr int kPStages = 6;
 constexpr int kZSlots = 4;            // 128 rows x 64 tokens of logits each
 constexpr int kAccum = 2;             // TMEM accumulators (128 columns each)
 constexpr uint32_t kASize = 65536;    // up to r = 256
@@ -81,6 +84,11 @@ struct TcParams {
   SampleParams sp;
   int32_t n_mt, n_nt, nkb, tiles;
 
+  int32_t packed;        // P from the tile-packed copy: 32 KB stages by bulk copy
+  int32_t pring;         // stages in the P ring (6 or 3)
+  int32_t pstage_bytes;  // ring stage size (16 or 32 KB)
+  int32_t kb_stage;      // 64-row k-blocks per stage (1 or 2)
+  int32_t pstages;       // stages per tile: ceil(nkb / kb_stage)
   uint32_t wait_polls;   // polls of a bounded wait before it gives up
   int32_t withhold_cta;  // test hook (-1: none), see set_tile_test_hooks
 };
@@ -349,14 +357,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int t = t0, i = 0; t < t1 && ok; ++t, ++i) {
       const int mt = t / prm.n_nt, nt = t - mt * prm.n_nt;
       const int n0 = nt * kTileN;
-      for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
-        const uint32_t ps = pc % kPStages;
+      for (int st = 0; st < prm.pstages && ok; ++st, ++pc) {
+        const uint32_t ps = pc % (uint32_t)prm.pring;
         if (lane == 0) {
-          ok = wait_bar(&sh.p_empty[ps], ((pc / kPStages) & 1) ^ 1, abort_flag, sp.status, prm.wait_polls);
+          ok = wait_bar(&sh.p_empty[ps], ((pc / (uint32_t)prm.pring) & 1) ^ 1, abort_flag, sp.status,
+                        prm.wait_polls);
           if (ok) {
-            mbar_expect_tx(&sh.p_full[ps], kPStage);
-            tma_load_2d(sP + ps * kPStage, &tmP, &sh.p_full[ps], n0, c * 64, pol_p);
-            tma_load_2d(sP + ps * kPStage + 8192, &tmP, &sh.p_full[ps], n0 + 64, c * 64, pol_p);
+            uint8_t* dst = sP + ps * (uint32_t)prm.pstage_bytes;
+            if (prm.packed) {
+              // k-blocks [st * 2, st * 2 + 1] of tile nt, contiguous in the packed copy
+              const int nk = min(prm.kb_stage, prm.nkb - st * prm.kb_stage);
+              const uint32_t bytes = (uint32_t)nk * 16384u;
+              mbar_expect_tx(&sh.p_full[ps], bytes);
+              bulk_load_hint(dst,
+                             reinterpret_cast<const uint8_t*>(sp.P_packed) +
+                                 ((size_t)nt * prm.nkb + (size_t)st * prm.kb_stage) * 16384u,
+                             bytes, &sh.p_full[ps], pol_p);
+            } else {
+              mbar_expect_tx(&sh.p_full[ps], kPStage);
+              tma_load_2d(dst, &tmP, &sh.p_full[ps], n0, st * 64, pol_p);
+              tma_load_2d(dst + 8192, &tmP, &sh.p_full[ps], n0 + 64, st * 64, pol_p);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -434,16 +455,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kTileN;
-        for (int c = 0; c < prm.nkb && ok; ++c, ++pc) {
-          const uint32_t ps = pc % kPStages;
-          ok = wait_bar(&sh.p_full[ps], (pc / kPStages) & 1, abort_flag, sp.status, prm.wait_polls);
+        for (int st = 0; st < prm.pstages && ok; ++st, ++pc) {
+          const uint32_t ps = pc % (uint32_t)prm.pring;
+          ok = wait_bar(&sh.p_full[ps], (pc / (uint32_t)prm.pring) & 1, abort_flag, sp.status, prm.wait_polls);
           if (!ok) break;
           tc_fence_after();
+          for (int cl = 0; cl < prm.kb_stage; ++cl) {
+            const int c = st * prm.kb_stage + cl;  // 64-row k-block of r
+            if (c >= prm.nkb) break;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(sA + c * 16384 + kk * 32, abits);
-            const uint64_t bd = smem_desc(sP + ps * kPStage + kk * 2048, bbits);
-            mma_bf16(d, ad, bd, idesc, (c | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(sA + c * 16384 + kk * 32, abits);
+              const uint64_t bd = smem_desc(sP + ps * (uint32_t)prm.pstage_bytes + cl * 16384 + kk * 2048, bbits);
+              mma_bf16(d, ad, bd, idesc, (c | kk) != 0 ? 1u : 0u);
+            }
           }
           mma_commit(&sh.p_empty[ps]);
         }
@@ -768,6 +793,11 @@ cudaError_t launch_tile_tc(const SampleParams& p, cudaStream_t s) {
   prm.n_mt = (p.B + 127) / 128;
   prm.n_nt = (p.V + kTileN - 1) / kTileN;
   prm.nkb = p.r / 64;
+  prm.packed = p.P_packed != nullptr ? 1 : 0;
+  prm.kb_stage = prm.packed ? 2 : 1;
+  prm.pstage_bytes = (int32_t)kPStage * prm.kb_stage;
+  prm.pring = kPStages / prm.kb_stage;
+  prm.pstages = (prm.nkb + prm.kb_stage - 1) / prm.kb_stage;
   if (p.r % 64 != 0 || p.r > 256) return cudaErrorInvalidValue;
   prm.tiles = prm.n_mt * prm.n_nt;
   prm.wait_polls = g_wait_polls.load(std::memory_order_relaxed);

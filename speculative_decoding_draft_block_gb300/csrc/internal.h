@@ -56,6 +56,7 @@ struct SampleParams {
   const void* E;
   const void* P;
   const void* P_t;              // [V][r] token-major copy of P, or null
+  const void* P_packed;         // tile-packed copy of P (ds_pack_projection), or null
   const int32_t* anchor;
   const int32_t* draft_tokens;  // [B][K] (read: previous positions; written by locate)
   const float* temperature;
@@ -234,6 +235,8 @@ cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t s);
 size_t schedule_smem_bytes(int32_t B, int32_t K);
 cudaError_t launch_transpose(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_t,
                              cudaStream_t s);
+size_t packed_projection_bytes(int32_t r, int32_t V);
+cudaError_t launch_pack_projection(const void* P, int32_t r, int32_t V, void* P_packed, cudaStream_t s);
 cudaError_t launch_philox_fill(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_t* out,
                                int32_t n, cudaStream_t s);
 

@@ -1,4 +1,5 @@
-// Weight layout step: the token-major copy of the Markov projection.
+// Weight layout steps: the token-major and the tile-packed copies of the Markov
+// projection.
 //
 // DSpark summary page, 방법론 › 반자기회귀 생성: the Markov head's bias for
 // token v is E[x] . P[:, v]. The tile kernels stream P row-major ([r][V]) into
@@ -37,7 +38,42 @@ __global__ void __launch_bounds__(256) transpose_kernel(const T* __restrict__ P,
   }
 }
 
+// Tile-packed copy of P for the tensor-core tile kernel: for each 128-token
+// tile nt, its r x 128 slice of P in exactly the shared-memory image the MMA
+// reads (64-row k-blocks c, each two 64-token halves h of 64 rows x 128 bytes,
+// the 16-byte unit u of row m stored at unit u ^ (m & 7), the 128-byte
+// swizzle), so that a stage of the tile arrives with one bulk copy instead of
+// a tensor copy per row. Tokens past V are zero. One thread per 16-byte unit.
+__global__ void __launch_bounds__(256) pack_kernel(const uint16_t* __restrict__ P, int32_t r, int32_t V,
+                                                    int32_t n_nt, uint4* __restrict__ out) {
+  const int nkb = r / 64;
+  const size_t units = (size_t)n_nt * nkb * 1024;  // 16 KB = 1024 units per (tile, k-block)
+  for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < units; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t blk = q >> 10;                    // (tile, k-block)
+    const int nt = (int)(blk / nkb), c = (int)(blk - (size_t)nt * nkb);
+    const int w = (int)(q & 1023);                 // destination unit within the 16 KB block
+    const int h = w >> 9, m = (w >> 3) & 63, us = w & 7;
+    const int u = us ^ (m & 7);                    // source unit stored at swizzled position us
+    const int v0 = nt * 128 + h * 64 + u * 8;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (v0 < V) val = *reinterpret_cast<const uint4*>(P + (size_t)(c * 64 + m) * V + v0);
+    out[q] = val;
+  }
+}
+
 }  // namespace
+
+size_t packed_projection_bytes(int32_t r, int32_t V) {
+  return (size_t)((V + 127) / 128) * (size_t)(r / 64) * 16384u;
+}
+
+cudaError_t launch_pack_projection(const void* P, int32_t r, int32_t V, void* P_packed, cudaStream_t s) {
+  const int n_nt = (V + 127) / 128;
+  const size_t units = (size_t)n_nt * (r / 64) * 1024;
+  const int blocks = (int)((units + 255) / 256 < 65535 * 8 ? (units + 255) / 256 : 65535 * 8);
+  pack_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(P), r, V, n_nt, static_cast<uint4*>(P_packed));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transpose(const void* P, int32_t r, int32_t V, int32_t dtype, void* P_t,
                              cudaStream_t s) {

@@ -40,12 +40,14 @@ GUARD_BYTE = 0xA5                 # the sentinel byte of the guard regions
 class DeviceCycle:
     def __init__(self, inp, device="cuda", mode=_lib.DS_SCHED_GREEDY_EARLYSTOP, threshold=0.0,
                  token_major_projection=True, initial_budget=None, rnn_weights=None,
-                 device_seed=False, guards=False):
+                 device_seed=False, guards=False, packed_projection=True):
         """``rnn_weights`` (dict w_ih, w_hh as bfloat16 bits, b_ih, b_hh float32)
         selects the RNN head; its step matrix is packed once here.
         ``device_seed``: the Philox key is read from a device word (``seed_dev``,
         set with ``set_seed``) instead of the ``seed`` argument, so that a
         captured cycle can be replayed with a fresh key each time.
+        ``packed_projection``: the tile-packed copy of P (ds_pack_projection) is
+        made once here and passed to draft and verify when the shape allows.
         ``guards``: every buffer the library writes (outputs and workspaces) sits
         between two GUARD_BYTES regions of sentinel bytes; ``guard_damage()``
         lists the buffers whose guards changed (a write out of bounds)."""
@@ -106,6 +108,12 @@ class DeviceCycle:
             P = self.t["P"]
             self.P_t = self._out("P_t", (P.shape[1], P.shape[0]), P.dtype)
             check(_lib.ds_transpose_projection(P, self.P_t), "ds_transpose_projection")
+        # weight layout step, once per model: the tile-packed copy of P
+        self.P_packed = None
+        nbytes = _lib.ds_packed_projection_bytes(r, V) if inp["bf16"] else 0
+        if packed_projection and nbytes > 0:
+            self.P_packed = self._out("P_packed", (nbytes,), torch.uint8)
+            check(_lib.ds_pack_projection(self.t["P"], self.P_packed), "ds_pack_projection")
 
     def _out(self, name, shape, dtype):
         """A zeroed device buffer; with guards, the middle of a larger buffer
@@ -150,7 +158,7 @@ class DeviceCycle:
         check(_lib.ds_draft_block(t["base_logits"], t["E"], t["P"], t["anchor"], t["temperature"],
                                   seed, self.draft_tokens, self.q_token, self.q_stats,
                                   self.ws_draft, self.status, stream, P_t=self.P_t, rnn=self.rnn,
-                                  seed_ptr=self.seed_dev),
+                                  seed_ptr=self.seed_dev, P_packed=self.P_packed),
               "ds_draft_block")
 
     def schedule(self, stream=None):
@@ -170,7 +178,7 @@ class DeviceCycle:
                              t["temperature"], seed, self.out_tokens, self.accept_count,
                              self.num_emitted, self.ws_verify, self.status, stream, P_t=self.P_t,
                              states=None if self.rnn is None else self.rnn["states"],
-                             seed_ptr=self.seed_dev, p_token=self.p_token),
+                             seed_ptr=self.seed_dev, p_token=self.p_token, P_packed=self.P_packed),
               "ds_verify")
 
     def run(self, seed, stream=None):

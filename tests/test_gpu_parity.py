@@ -136,6 +136,51 @@ def test_transpose_projection_exact(ds, bf16):
         assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("r,V", [(256, 4096), (64, 3000), (192, 1032), (128, 8)])
+def test_pack_projection_exact(ds, r, V):
+    """The tile-packed copy of P: for tile nt, k-block c, half h, row m, the
+    16-byte unit u of P[c*64 + m][nt*128 + h*64 + 8u ...] sits at unit
+    u ^ (m % 8) of its 128-byte row; tokens past V are zero (layout restated
+    here with NumPy)."""
+    import torch
+    from speculative_decoding_draft_block_gb300 import _lib
+    from speculative_decoding_draft_block_gb300.cycle import _to_device
+    rng = np.random.default_rng(r + V)
+    P = (rng.standard_normal((r, V), dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    nbytes = _lib.ds_packed_projection_bytes(r, V)
+    n_nt = (V + 127) // 128
+    assert nbytes == n_nt * (r // 64) * 16384
+    out = torch.zeros((nbytes,), dtype=torch.uint8, device="cuda")
+    assert _lib.ds_pack_projection(_to_device(P, "cuda"), out) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16).reshape(n_nt, r // 64, 2, 64, 8, 8)
+    Pp = np.zeros((r, n_nt * 128), dtype=np.uint16)
+    Pp[:, :V] = P
+    # want[nt, c, h, m, u_stored, 8 tokens]
+    src = Pp.reshape(r // 64, 64, n_nt, 2, 8, 8).transpose(2, 0, 3, 1, 4, 5)  # nt, c, h, m, u, e
+    want = np.empty_like(src)
+    for m in range(64):
+        for u in range(8):
+            want[:, :, :, m, u ^ (m % 8), :] = src[:, :, :, m, u, :]
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("bf16", [True])
+def test_ragged_tensor_copies_of_projection(ds, bf16):
+    """The tensor-core tile fed by per-row tensor copies of P (no packed copy)."""
+    inp = _ragged(bf16, (0.0, 0.6, 1.0), 37, B=37, K=5, V=3000, r=64, d=64)
+    _, g = _run(inp, packed_projection=False)
+    rep = _parity.assert_parity(inp, g, SEED)
+    assert rep["draft"]["draws"] == 37 * 5
+
+
+def test_full_size_without_packed_projection(ds):
+    from speculative_decoding_draft_block_gb300.workloads import WORKLOADS, make_inputs
+    inp = make_inputs(WORKLOADS["B32_K8_V151936"])
+    _, g = _run(inp, packed_projection=False)
+    _parity.assert_parity(inp, g, SEED)
+
+
 def test_independent_cycle_matches_oracle_cycle(ds):
     """No teacher forcing: the oracle's own cycle and the GPU's agree end to end.
 
