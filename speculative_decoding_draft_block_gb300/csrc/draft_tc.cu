@@ -99,6 +99,7 @@ struct Shared {
   uint64_t z_full[kZSlots], z_empty[kZSlots];
   uint64_t t_full[kAccum], t_empty[kAccum];
   uint64_t x_bar;  // barrier of the epilogue threads (all arrive)
+  uint64_t drain;  // the MMA issuer's last commit, waited for before TMEM is freed
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -117,6 +118,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   *abort_flag = 1;
   report(status, kErrTimeout);
   return false;
+}
+
+// Wait for a copy or commit already issued by this thread to land, also after
+// an abort, so that nothing is in flight when the CTA exits; bounded.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, uint32_t polls) {
+  for (uint32_t i = 0; i <= polls; ++i)
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return;
 }
 
 // Barrier over the epilogue threads only, bounded like every other wait.
@@ -329,6 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sh.t_empty[i], kEpiWarps);
     }
     mbar_init(&sh.x_bar, 32 * kEpiWarps);
+    mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_barrier_init();
   }
@@ -405,6 +414,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         a_mt = mt;
       }
     }
+    // nothing of this CTA may be in flight when it exits (also after an abort)
+    if (lane == 0) {
+      const uint32_t ring = (uint32_t)prm.pring;
+      for (uint32_t j = pc > ring ? pc - ring : 0; j < pc; ++j)
+        drain_bar(&sh.p_full[j % ring], (j / ring) & 1, prm.wait_polls);
+      if (a_loads > 0) drain_bar(&sh.a_full, (a_loads - 1) & 1, prm.wait_polls);
+    }
+    __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ logit producer
     // the draft step's base-logit tiles (inputs: no dependent wait), in a ring
@@ -430,6 +447,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
       }
+      if (lane == 0)
+        for (uint32_t j = zc > (uint32_t)kZSlots ? zc - kZSlots : 0; j < zc; ++j)
+          drain_bar(&sh.z_full[j % kZSlots], (j / kZSlots) & 1, prm.wait_polls);
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -474,6 +495,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (ok) mma_commit(&sh.t_full[buf]);
       }
+      // every MMA this thread issued has completed before TMEM is freed
+      mma_commit(&sh.drain);
+      drain_bar(&sh.drain, 0, prm.wait_polls);
     }
     __syncwarp();
   }

@@ -214,7 +214,7 @@ __host__ __device__ inline int32_t last_group(const SampleParams& p, int32_t mt)
 void tc_group_layout(SampleParams& p);
 void simt_group_layout(SampleParams& p);
 size_t sample_tile_smem_bytes(int32_t r);
-size_t locate_smem_bytes(int32_t V);
+size_t locate_smem_bytes(const SampleParams& p);
 bool tc_path_supported(int32_t dtype, int32_t r, int32_t V);
 // Test hooks of the tensor-core tile kernel (ds_test_set_wait_hooks).
 void set_tile_test_hooks(uint32_t wait_polls, int32_t withhold_cta);

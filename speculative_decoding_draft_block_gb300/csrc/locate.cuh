@@ -63,38 +63,36 @@ __device__ __forceinline__ DF shfl_df(DF v, int l) {
 // crosses u*S; (2) scan that group's chunk records to find the crossing chunk;
 // (3) recompute that chunk's 32 weights with the arithmetic its record used
 // and pick the token: x = min{i : u*S < C_i}. Levels 1 and 2 run in warp 0
-// alone; the E row of the bias is loaded by every thread at the start and only
-// stored for level 3, so its latency overlaps levels 1 and 2. Each level costs
-// one round of independent loads. Called by kLocThreads threads (tid), with
-// `sync` a barrier over exactly those threads; sgrp holds sup_stride records.
+// alone. Every load that does not depend on an earlier result is issued
+// together at the start (group records, seed, the row's token and temperature;
+// then the E row of the bias, only stored for level 3), so that each level
+// costs one round of loads. Called by kLocThreads threads (tid), with `sync` a
+// barrier over exactly those threads; sgrp holds the row's group records
+// (up to sup_stride). `step` is the 1-based draft position (p.step outside
+// the persistent draft kernel).
 template <typename Tin, typename Sync>
-__device__ __forceinline__ void locate_row(const SampleParams& p, int b, int tid, LocShared& sm,
-                                           ChunkRec* sgrp, Sync sync) {
+__device__ __forceinline__ void locate_row(const SampleParams& p, int b, int step, int tid,
+                                           LocShared& sm, ChunkRec* sgrp, Sync sync) {
   const int lane = tid & 31, wid = tid >> 5;
   const int nc = p.n_chunks;
   const int r = p.r;
   const int mt = b / p.sup_rows;
   const int g_lo = first_group(p, mt);
   const int ng = last_group(p, mt) - g_lo + 1;
-  // group records first: they do not depend on the row's context
+  // group records and the seed first: they do not depend on the row's context
+  const uint4* gsrc = reinterpret_cast<const uint4*>(p.supers + (size_t)b * p.sup_stride);
+  uint4 gv[8];
+  uint64_t seed = p.seed;
   if (wid == 0) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.supers + (size_t)b * p.sup_stride);
-    uint4* dst = reinterpret_cast<uint4*>(sgrp);
-    for (int i0 = 0; i0 < ng; i0 += 32 * 8) {
-      uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * 32 + lane;
-        if (i < ng) v[u] = __ldcg(src + i);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * 32 + lane;
-        if (i < ng) dst[i] = v[u];
-      }
+    for (int u = 0; u < 8; ++u) {
+      const int i = u * 32 + lane;
+      if (i < ng) gv[u] = __ldcg(gsrc + i);
     }
+    if (p.seed_ptr != nullptr) seed = *p.seed_ptr;  // after the dependent wait
   }
-  const RowCtx c = make_row_ctx<Tin>(p, b);
+  const RowInputs rin = load_row_inputs(p, b, step);  // in flight with the records
+  const RowCtx c = make_row_ctx<Tin>(p, b, rin, step);
   if (c.mode == kSkip) return;
   const Tin* Erow = bias_row<Tin>(p, b, c);
   float erow[4];
@@ -103,10 +101,28 @@ __device__ __forceinline__ void locate_row(const SampleParams& p, int b, int tid
     const int k = tid + q * kLocThreads;
     erow[q] = (c.a_token >= 0 && k < r) ? to_f32(Erow[k]) : 0.f;
   }
+  if (wid == 0) {
+    uint4* dst = reinterpret_cast<uint4*>(sgrp);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = u * 32 + lane;
+      if (i < ng) dst[i] = gv[u];
+    }
+    for (int i0 = 32 * 8; i0 < ng; i0 += 32 * 8) {  // more than 256 groups (SIMT tiles)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i < ng) gv[u] = __ldcg(gsrc + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i < ng) dst[i] = gv[u];
+      }
+    }
+  }
 
   if (wid == 0) {
-    // the row's uniform does not depend on the records: draw it while they load
-    const uint64_t seed = p.seed_ptr != nullptr ? *p.seed_ptr : p.seed;  // after the dependent wait
     const DF u01 = uniform_df(seed, (uint32_t)b, c.upos, c.ustage);
     __syncwarp();
     const int seg = (ng + 31) / 32;
@@ -330,7 +346,7 @@ __device__ __forceinline__ void locate_row(const SampleParams& p, int b, int tid
       const int ref = cr.ref;
       if (lane < n && ref != kEmptyRef) {
         if (cr.idx == -2)
-          w = fast_w1(zl, bsum, make_g16(p.temperature[b]), ref);
+          w = fast_w1(zl, bsum, make_g16_from(c.g), ref);
         else
           w = weight_rel(zl, bsum, c.g, ref);
       }

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kLocThreads) sample_locate_kernel(SampleParams
   __shared__ LocShared sm;
   sm100::pdl_launch_dependents();
   sm100::pdl_wait();
-  locate_row<Tin>(p, blockIdx.x, threadIdx.x, sm, sgrp, BlockSync{});
+  locate_row<Tin>(p, blockIdx.x, p.step, threadIdx.x, sm, sgrp, BlockSync{});
 }
 
 }  // namespace
@@ -182,7 +182,7 @@ cudaError_t launch_sample_tile(const SampleParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-size_t locate_smem_bytes(int32_t V) { return (size_t)sup_stride_for(V) * sizeof(ChunkRec); }
+size_t locate_smem_bytes(const SampleParams& p) { return (size_t)p.sup_stride * sizeof(ChunkRec); }
 
 void simt_group_layout(SampleParams& p) {
   p.sup_stride = sup_stride_for(p.V);
@@ -210,7 +210,7 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 }
 
 cudaError_t launch_sample_locate(const SampleParams& p, cudaStream_t s) {
-  const size_t smem = locate_smem_bytes(p.V);
+  const size_t smem = locate_smem_bytes(p);
   if (p.dtype == DS_BF16) {
     static cudaError_t attr = cudaFuncSetAttribute(
         sample_locate_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);

@@ -24,8 +24,34 @@ struct RowCtx {
   int32_t zk;             // draft: 0-based position of the base row; final: row index j
 };
 
+// The values a row's context is built from, loaded with no dependence on one
+// another so that they travel in one round: the temperature, and the
+// conditioning token (draft) or the final-draw descriptor (verify).
+struct RowInputs {
+  float T;
+  int32_t tok;
+  FinalDesc d;
+};
+
+// The tokens of earlier positions are written by other CTAs of the same
+// launch in the persistent draft kernel: read them at L2 (never a stale L1
+// line). `step` is the 1-based draft position (p.step outside that kernel).
+__device__ __forceinline__ RowInputs load_row_inputs(const SampleParams& p, int b, int step) {
+  RowInputs in;
+  in.T = 0.f;
+  in.tok = 0;
+  in.d = FinalDesc{kSkip, 0, 0, 0, 0, 0, 0.f, 0.f};
+  if (b >= p.B) return in;
+  in.T = p.temperature[b];
+  if (p.src == 0)
+    in.tok = (step == 1) ? p.anchor[b] : __ldcg(p.draft_tokens + (size_t)b * p.K + (step - 2));
+  else
+    in.d = p.final_desc[b];
+  return in;
+}
+
 template <typename Tin>
-__device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
+__device__ RowCtx make_row_ctx(const SampleParams& p, int b, const RowInputs& in, int step) {
   RowCtx c;
   c.mode = kSkip;
   c.a_token = -1;
@@ -41,7 +67,7 @@ __device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
   if (b >= p.B) return c;
   const Tin* base = reinterpret_cast<const Tin*>(p.base_logits);
   const Tin* tgt = reinterpret_cast<const Tin*>(p.target_logits);
-  const float T = p.temperature[b];
+  const float T = in.T;
   const bool greedy = (T == 0.f);
   if (!greedy && !(T >= 1e-3f && T <= 1e3f)) {
     report(p.status, kErrInvalidArg);
@@ -49,8 +75,8 @@ __device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
   }
   if (!greedy) c.g = make_gscale(T);
   if (p.src == 0) {
-    const int k = p.step;  // 1-based
-    int tok = (k == 1) ? p.anchor[b] : p.draft_tokens[(size_t)b * p.K + (k - 2)];
+    const int k = step;  // 1-based
+    int tok = in.tok;
     if (tok < 0 || tok >= p.V) {
       report(p.status, kErrBounds);
       tok = 0;
@@ -63,7 +89,7 @@ __device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
     c.out_index = b * p.K + (k - 1);
     c.zk = k - 1;
   } else {
-    const FinalDesc d = p.final_desc[b];
+    const FinalDesc d = in.d;
     if (greedy || d.mode == kSkip) return c;
     c.mode = d.mode;
     c.trow = tgt + ((size_t)b * (p.K + 1) + d.row) * (size_t)p.V;
@@ -86,6 +112,16 @@ __device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
     }
   }
   return c;
+}
+
+template <typename Tin>
+__device__ RowCtx make_row_ctx(const SampleParams& p, int b, int step) {
+  return make_row_ctx<Tin>(p, b, load_row_inputs(p, b, step), step);
+}
+
+template <typename Tin>
+__device__ RowCtx make_row_ctx(const SampleParams& p, int b) {
+  return make_row_ctx<Tin>(p, b, p.step);
 }
 
 // The r-vector whose product with P is the row's bias: E[a_token] for the
