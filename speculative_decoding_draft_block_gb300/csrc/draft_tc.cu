@@ -171,38 +171,26 @@ __device__ __forceinline__ EpiRow epi_row_draft(const SampleParams& sp, int row)
   return c;
 }
 
-// Fast path of a full chunk of the final draw (bf16; see fastpath.cuh): bonus
-// weights 2^(t g - Np), or residual weights max(0, 2^(t g - Np) - R 2^((z + b) g - Nq)),
-// both against the rows' global references. False when the chunk needs the
-// general path.
-__device__ __forceinline__ bool final_chunk_fast(const EpiRow& c, const uint32_t* zp,
-                                                 const uint32_t* tp, const uint32_t* braw,
-                                                 ChunkRec& rec) {
-  const bool res = (c.mode == kResidual);
-  if (!fast_span_ok(tp, c.g16.G, c.Np)) return false;
-  if (res && !fast_span_ok(zp, c.g16.G, c.Nq)) return false;
-  const FastConsts kp = make_fast_consts(c.g16, c.Np);
-  float2 s = make_float2(0.f, 0.f);
-  if (res) {
-    const FastConsts kq = make_fast_consts(c.g16, c.Nq);
+// One 16-token half of a final-draw chunk's fast path (bf16; see
+// fastpath.cuh): tokens 16h .. 16h + 15, tp8 / zp8 their 8 packed target and
+// base logit words, b16 their bias columns. Bonus weights 2^(t g - Np), or
+// residual weights max(0, 2^(t g - Np) - R 2^((z + b) g - Nq)), both against
+// the rows' global references; the pairs are added in token order, as a
+// whole-chunk pass would add them.
+__device__ __forceinline__ void final_half(const uint32_t* tp8, const uint32_t* zp8, const uint32_t* b16,
+                                           bool res, const FastConsts& kp, const FastConsts& kq, float Rhi,
+                                           float Rlo, float2& s) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 wp = fast_w2(tp[i], make_float2(0.f, 0.f), kp);
+  for (int i = 0; i < 8; ++i) {
+    const float2 wp = fast_w2(tp8[i], make_float2(0.f, 0.f), kp);
+    if (res) {
       const float2 wq =
-          fast_w2(zp[i], make_float2(__uint_as_float(braw[2 * i]), __uint_as_float(braw[2 * i + 1])), kq);
-      s = __fadd2_rn(s, make_float2(residual_w(wp.x, wq.x, c.Rhi, c.Rlo), residual_w(wp.y, wq.y, c.Rhi, c.Rlo)));
+          fast_w2(zp8[i], make_float2(__uint_as_float(b16[2 * i]), __uint_as_float(b16[2 * i + 1])), kq);
+      s = __fadd2_rn(s, make_float2(residual_w(wp.x, wq.x, Rhi, Rlo), residual_w(wp.y, wq.y, Rhi, Rlo)));
+    } else {
+      s = __fadd2_rn(s, wp);
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) fast_pair(tp[i], make_float2(0.f, 0.f), kp, s);
   }
-  const float sum = __fadd_rn(s.x, s.y);
-  if (!(sum >= 0.f && isfinite(sum))) return false;
-  rec.hi = sum;
-  rec.lo = 0.f;
-  rec.ref = 0;
-  rec.idx = -2;  // fast-path record
-  return true;
 }
 
 // One 16-token half of a sampling chunk's fast path: tokens 16h .. 16h + 15,
@@ -608,24 +596,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ChunkRec* out = sp.chunks + (size_t)(col0 >> 5) * sp.B + row;  // chunk-major: coalesced
         bool done = !active;
         if constexpr (kFinal) {
-          uint32_t braw[32];
-          tmem_ld32_issue(tbase + (cg * kChunks + j) * 32, braw);
-          tmem_ld_wait(braw);
-          if (active && n == 32 && (c.mode == kResidual || c.mode == kBonus)) {
-            uint32_t zp[16], tp[16];
+          // the bias in two 16-column loads (warp-collective), as in the draft
+          const bool fast = active && n == 32 && (c.mode == kResidual || c.mode == kBonus);
+          const bool res = c.mode == kResidual;
+          uint32_t zp[16], tp[16];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint4 t = ft[j][u], v = fz[j][u];
-              tp[4 * u] = t.x; tp[4 * u + 1] = t.y; tp[4 * u + 2] = t.z; tp[4 * u + 3] = t.w;
-              zp[4 * u] = v.x; zp[4 * u + 1] = v.y; zp[4 * u + 2] = v.z; zp[4 * u + 3] = v.w;
-            }
-            ChunkRec rec;
-            done = final_chunk_fast(c, zp, tp, braw, rec);
-            if (done) {
+          for (int u = 0; u < 4; ++u) {
+            const uint4 t = ft[j][u], v = fz[j][u];
+            tp[4 * u] = t.x; tp[4 * u + 1] = t.y; tp[4 * u + 2] = t.z; tp[4 * u + 3] = t.w;
+            zp[4 * u] = v.x; zp[4 * u + 1] = v.y; zp[4 * u + 2] = v.z; zp[4 * u + 3] = v.w;
+          }
+          bool ok = fast && fast_span_ok(tp, c.g16.G, c.Np) && (!res || fast_span_ok(zp, c.g16.G, c.Nq));
+          const FastConsts kp = make_fast_consts(c.g16, c.Np);
+          const FastConsts kq = make_fast_consts(c.g16, c.Nq);
+          float2 sum2 = make_float2(0.f, 0.f);
+          const uint32_t taddr = tbase + (cg * kChunks + j) * 32;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t b16[16];
+            tmem_ld16_issue(taddr + 16 * h, b16);
+            tmem_ld16_wait(b16);
+            if (ok) final_half(tp + 8 * h, zp + 8 * h, b16, res, kp, kq, c.Rhi, c.Rlo, sum2);
+          }
+          if (ok) {
+            const float sum = __fadd_rn(sum2.x, sum2.y);
+            ok = sum >= 0.f && isfinite(sum);
+            if (ok) {
+              const ChunkRec rec = {sum, 0.f, 0, -2};  // fast-path record
               *out = rec;
               group_merge(c.mode, gacc, rec);
             }
           }
+          done = fast ? ok : !active;
         } else {
           // the bias in two 16-column loads (warp-collective: every lane issues
           // them), so only 16 bias registers are live
