@@ -34,7 +34,7 @@ namespace ds {
 
 namespace {
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 256;
 
 // Row sum of one thread's 8-token groups of bf16 target logits, relative to a
 // running integer reference R (the largest group reference seen so far).
