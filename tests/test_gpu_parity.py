@@ -397,6 +397,7 @@ def test_minimal_shapes(ds):
     (256, 64, 1024, 64, True, 24),      # B*K at its limit (16384 drafted tokens)
     (5, 3, 2048, 1024, True, None),     # r at its limit (SIMT tile: A rows wider than 256)
     (4, 2, 1024, 1024, False, None),    # r at its limit, float32
+    (1536, 2, 1024, 64, True, 32),      # more requests than scheduler threads (sort network, no merge tree)
 ])
 def test_limit_shapes(ds, B, K, V, r, bf16, rows):
     inp = _ragged(bf16, (0.0, 0.6, 1.0), 29 + K, B=B, K=K, V=V, r=r, d=64)
