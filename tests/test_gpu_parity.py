@@ -260,34 +260,47 @@ def _selection_size(survival):
     return max(_select(surv, cap)[0], _select(surv, 1024)[0])
 
 
-@pytest.mark.parametrize("case", ["stop_past_selection", "one_bin", "async_budget_past_selection"])
+@pytest.mark.parametrize("case", ["stop_past_selection", "one_bin", "async_budget_past_selection",
+                                  "second_tier", "async_budget_inside_selection"])
 def test_schedule_sorts_every_key_past_the_selection(ds, case):
     """B*K = 2048 candidates where the early stop (or the asynchronous budget)
     lies beyond the top bins the scheduler sorts first, or every survival
-    sits in one bin: the full sort runs, and its order decides sched_len."""
+    sits in one bin: the full sort runs, and its order decides sched_len.
+    Also a stop past the first selection (at most 4B = 512 candidates) but
+    inside the second (at most 1024), and an asynchronous budget inside the
+    selection."""
     from speculative_decoding_draft_block_gb300 import _lib
     import oracle
     inp = _ragged(True, (1.0,), 29, B=128, K=16, V=1024, r=32, d=64)
     n_max = len(inp["sps"])
     if case == "one_bin":
         inp["conf_bias"] = 60.0  # c rounds to 1 in float32: every survival is 1
+    elif case == "second_tier":
+        # J = A while N <= 828, then 828 A / N: the stop falls near 700 candidates
+        inp["sps"] = np.minimum(np.arange(1, n_max + 1), 128 + 700).astype(np.float32)
+    elif case == "async_budget_inside_selection":
+        pass
     else:
         # J = A while N <= 1700, then 1700 A / N: the stop falls near N = 1700,
         # past any selection of at most 1024 candidates
         inp["sps"] = np.minimum(np.arange(1, n_max + 1), 1700).astype(np.float32)
     kw = {}
-    if case == "async_budget_past_selection":
-        kw = dict(mode=_lib.DS_SCHED_ASYNC, initial_budget=1500)
+    budget = {"async_budget_past_selection": 1500, "async_budget_inside_selection": 300}.get(case)
+    if budget is not None:
+        kw = dict(mode=_lib.DS_SCHED_ASYNC, initial_budget=budget)
     _, g = _run(inp, **kw)
     c = oracle.confidence(inp["h"], inp["E"], inp["anchor"], g["tokens"], inp["w_h"], inp["w_e"],
                           inp["conf_bias"], inp["sts_temp"])
     s = oracle.survival(c)
-    if case == "async_budget_past_selection":
-        assert _selection_size(g["survival"]) < 1500
-        want = oracle.schedule(s, inp["sps"], mode=oracle.SCHED_ASYNC, budget=1500)
-        assert int(g["L"].sum()) == 1500
+    if budget is not None:
+        if budget == 1500:
+            assert _selection_size(g["survival"]) < budget
+        else:
+            assert _selection_size(g["survival"]) > budget
+        want = oracle.schedule(s, inp["sps"], mode=oracle.SCHED_ASYNC, budget=budget)
+        assert int(g["L"].sum()) == budget
         top = np.sort(s.ravel())[::-1]
-        if (top[1499] - top[1500]) > _parity.SCHED_NEAR_TIE * top[1499]:
+        if (top[budget - 1] - top[budget]) > _parity.SCHED_NEAR_TIE * top[budget - 1]:
             assert np.array_equal(g["L"], want["L"])
     else:
         want = oracle.schedule(s, inp["sps"])
@@ -295,6 +308,10 @@ def test_schedule_sorts_every_key_past_the_selection(ds, case):
         if case == "one_bin":
             assert _selection_size(g["survival"]) == 0 and np.all(g["survival"] == 1.0)
             assert np.all(g["L"] == 16)
+        elif case == "second_tier":
+            from tests.test_sched_network import _select
+            surv = [float(x) for x in g["survival"].reshape(-1)]
+            assert _select(surv, 512)[0] <= M < _select(surv, 1024)[0]
         else:
             assert _selection_size(g["survival"]) < M < 2048
         if min(want["stop_rel_gain"], want["survival_gap"]) >= _parity.SCHED_NEAR_TIE:
